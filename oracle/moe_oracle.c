@@ -1,0 +1,263 @@
+/*
+ * moe_oracle.c -- plain, slow, single-threaded CPU oracle for MoE token
+ * dispatch and combine.  TEST INFRASTRUCTURE ONLY (see moe_oracle.h).
+ *
+ * Every function is the plain definition written out as loops.  There is no
+ * blocking, fusion or reordering.  Build with -O2 -ffp-contract=off and
+ * without -ffast-math, so that float arithmetic is IEEE binary32 with
+ * round-to-nearest-even and only the fmaf() calls below fuse.
+ */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Number formats, written from the format definitions.                      */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 is the upper half of an IEEE binary32: the value is exact. */
+float oracle_bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* Keep the upper 16 bits; round the dropped lower 16 bits to nearest, ties
+ * to the even upper half.  A carry out of the mantissa moves to the next
+ * binade (and to infinity past the largest finite value), as IEEE does. */
+uint16_t oracle_f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if (isnan(f)) return (uint16_t)(((u >> 16) & 0x8000u) | 0x7FC0u);
+  uint32_t upper = u >> 16;
+  uint32_t lower = u & 0xFFFFu;
+  if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;
+  return (uint16_t)upper;
+}
+
+/* OCP 8-bit floating point, E4M3 ("FN"): 1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits.  Exponent field 0 holds subnormals m * 2^-9;
+ * field 15 with mantissa 7 is NaN; there is no infinity; the largest finite
+ * magnitude is 1.75 * 2^8 = 448. */
+float oracle_e4m3_to_f32(uint8_t q) {
+  int sign = (q & 0x80) ? -1 : 1;
+  int ex = (q >> 3) & 0xF;
+  int m = q & 0x7;
+  if (ex == 0xF && m == 0x7) return NAN;
+  double v;
+  if (ex == 0) v = ldexp((double)m, -9);
+  else v = ldexp(1.0 + (double)m / 8.0, ex - 7);
+  return (float)(sign * v);
+}
+
+/* Round |f| to the E4M3 grid: find the spacing of the grid in the binade of
+ * |f| (2^-9 in the subnormal range, 2^(k-3) in [2^k, 2^(k+1)) for k >= -6),
+ * round |f| / spacing to an integer with ties to even (rint() in the
+ * default rounding mode), and encode the result.  Magnitudes >= 448 saturate
+ * to 448: those in [448, 464) round to 448 and those above would overflow. */
+uint8_t oracle_f32_to_e4m3(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint8_t sign = (u >> 31) ? 0x80 : 0x00;
+  if (isnan(f)) return (uint8_t)(0x7F | sign);
+  double a = fabs((double)f);
+  if (a >= 448.0) return (uint8_t)(0x7E | sign);
+  if (a == 0.0) return sign;
+
+  int e2;
+  (void)frexp(a, &e2);       /* a = m * 2^e2, m in [0.5, 1) */
+  int k = e2 - 1;            /* a in [2^k, 2^(k+1)) */
+  if (k < -6) k = -6;        /* subnormals share the spacing of 2^-6's binade */
+  double spacing = ldexp(1.0, k - 3);
+  double n = rint(a / spacing); /* exact quotient; ties to even */
+  double v = n * spacing;       /* the rounded magnitude, exactly */
+
+  if (v == 0.0) return sign;
+  if (v < ldexp(1.0, -6)) {     /* subnormal: v = m * 2^-9, m in 1..7 */
+    int m = (int)(v / ldexp(1.0, -9));
+    return (uint8_t)(sign | m);
+  }
+  (void)frexp(v, &e2);
+  int kv = e2 - 1;                                 /* v in [2^kv, 2^(kv+1)) */
+  int m = (int)((v / ldexp(1.0, kv) - 1.0) * 8.0); /* 0..7, exact */
+  return (uint8_t)(sign | ((kv + 7) << 3) | m);
+}
+
+void oracle_bf16_to_f32_n(int64_t n, const uint16_t *in, float *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_f32(in[i]);
+}
+void oracle_f32_to_bf16_n(int64_t n, const float *in, uint16_t *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(in[i]);
+}
+void oracle_e4m3_to_f32_n(int64_t n, const uint8_t *in, float *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_to_f32(in[i]);
+}
+void oracle_f32_to_e4m3_n(int64_t n, const float *in, uint8_t *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_e4m3(in[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Plan.                                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* "Efficient and portable mixture-of-experts communication", Dispatch: the
+ * sender counts how many tokens each expert receives, and the receiver keeps
+ * (source rank, expert, token) so that combine knows where each row goes.
+ * "Enabling trillion-parameter models on AWS EFA", Send and Receive Buffers /
+ * Dispatch and Combine: per-expert counts are exchanged first and a
+ * cumulative sum of them gives each sender's offset inside the receiver's
+ * contiguous buffer.
+ *
+ * Reading taken for the slot order (the pages' receiver order is not
+ * deterministic): stable by (source logical rank, token, k).  Ranks are
+ * contiguous token ranges, so this is ascending global (g, k) order.
+ *
+ *   expert_num_tokens[e]      = #{(g,k) : idx[g,k] = e}
+ *   expert_rank_offsets[e][r] = #{(g,k) : idx[g,k] = e and g < r*T}, r = 0..R
+ *   slot_of[g,k]              = #{(g',k') before (g,k) : idx[g',k'] = idx[g,k]}
+ *   src_of[e][slot_of[g,k]]   = g*K + k
+ */
+int oracle_plan(int R, int T, int E, int K, int cap, const int32_t *topk_idx,
+                int32_t *expert_num_tokens, int32_t *expert_rank_offsets,
+                int32_t *slot_of, int32_t *src_of) {
+  if (R <= 0 || T <= 0 || E <= 0 || K <= 0 || cap <= 0) return ORACLE_BAD_SHAPE;
+  const int64_t N = (int64_t)R * T;
+
+  for (int64_t i = 0; i < N * K; ++i)
+    if (topk_idx[i] < 0 || topk_idx[i] >= E) return ORACLE_BAD_EXPERT;
+
+  /* counts */
+  for (int e = 0; e < E; ++e) expert_num_tokens[e] = 0;
+  for (int64_t g = 0; g < N; ++g)
+    for (int k = 0; k < K; ++k) expert_num_tokens[topk_idx[g * K + k]] += 1;
+
+  /* per-rank offsets, straight from the definition */
+  for (int e = 0; e < E; ++e)
+    for (int r = 0; r <= R; ++r) expert_rank_offsets[(int64_t)e * (R + 1) + r] = 0;
+  for (int r = 0; r <= R; ++r)
+    for (int64_t g = 0; g < (int64_t)r * T; ++g)
+      for (int k = 0; k < K; ++k)
+        expert_rank_offsets[(int64_t)topk_idx[g * K + k] * (R + 1) + r] += 1;
+
+  /* stable slots and return addresses */
+  int32_t *fill = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+  if (!fill) abort();
+  int status = ORACLE_OK;
+  for (int64_t g = 0; g < N; ++g) {
+    for (int k = 0; k < K; ++k) {
+      int e = topk_idx[g * K + k];
+      int s = fill[e];
+      fill[e] += 1;
+      slot_of[g * K + k] = s;
+      if (s < cap) src_of[(int64_t)e * cap + s] = (int32_t)(g * K + k);
+      else status = ORACLE_CAPACITY;
+    }
+  }
+  free(fill);
+  return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dispatch.                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Each token row is written to every (expert, slot) it is routed to. */
+void oracle_dispatch_bf16(int N, int H, int E, int K, int cap,
+                          const uint16_t *x, const int32_t *topk_idx,
+                          const int32_t *slot_of, uint16_t *expert_x) {
+  for (int64_t g = 0; g < N; ++g) {
+    for (int k = 0; k < K; ++k) {
+      int e = topk_idx[g * K + k];
+      int s = slot_of[g * K + k];
+      if (e < 0 || e >= E || s < 0 || s >= cap) continue;
+      uint16_t *dst = expert_x + ((int64_t)e * cap + s) * H;
+      for (int h = 0; h < H; ++h) dst[h] = x[g * H + h];
+    }
+  }
+}
+
+/* "Lower latency and higher throughput with multi-node DeepSeek
+ * deployment", Quantization: activations are quantised on the fly with one
+ * scale per 128-element vector along the hidden dimension (scale shape
+ * M x ceil_div(K, 128) for an M x K activation), found from the largest
+ * absolute value of the block.
+ *
+ * Readings taken (the pages fix only "absmax per 128 elements" and fp8):
+ *   amax  = max |x_i| over the block (exact in fp32)
+ *   scale = amax / 448   (IEEE binary32 division; 448 = largest E4M3)
+ *   q_i   = e4m3(x_i / scale)   (binary32 division, then RNE + saturate)
+ *   a block of zeros has scale 0 and q_i = +0.
+ */
+void oracle_quant_row_e4m3(int H, const uint16_t *row, uint8_t *q,
+                           float *scale) {
+  for (int b = 0; b < H / 128; ++b) {
+    float amax = 0.0f;
+    for (int i = b * 128; i < (b + 1) * 128; ++i) {
+      float a = fabsf(oracle_bf16_to_f32(row[i]));
+      if (a > amax) amax = a;
+    }
+    float s = amax / 448.0f;
+    scale[b] = s;
+    for (int i = b * 128; i < (b + 1) * 128; ++i) {
+      if (amax == 0.0f) q[i] = 0x00;
+      else q[i] = oracle_f32_to_e4m3(oracle_bf16_to_f32(row[i]) / s);
+    }
+  }
+}
+
+void oracle_dispatch_fp8(int N, int H, int E, int K, int cap,
+                         const uint16_t *x, const int32_t *topk_idx,
+                         const int32_t *slot_of, uint8_t *expert_x,
+                         float *expert_x_scale) {
+  const int nb = H / 128;
+  uint8_t *q = (uint8_t *)malloc((size_t)H);
+  float *sc = (float *)malloc((size_t)nb * sizeof(float));
+  if (!q || !sc) abort();
+  for (int64_t g = 0; g < N; ++g) {
+    oracle_quant_row_e4m3(H, x + g * H, q, sc);
+    for (int k = 0; k < K; ++k) {
+      int e = topk_idx[g * K + k];
+      int s = slot_of[g * K + k];
+      if (e < 0 || e >= E || s < 0 || s >= cap) continue;
+      int64_t row = (int64_t)e * cap + s;
+      for (int h = 0; h < H; ++h) expert_x[row * H + h] = q[h];
+      for (int b = 0; b < nb; ++b) expert_x_scale[row * nb + b] = sc[b];
+    }
+  }
+  free(q);
+  free(sc);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Combine.                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* "Efficient and portable mixture-of-experts communication", Introduction and
+ * Combine: the output of a token is the sum of its experts' outputs, each
+ * multiplied by the router weight, computed where the token came from, from
+ * 16-bit expert outputs.
+ *
+ * Reading taken for the arithmetic (not fixed by the pages): one fp32
+ * accumulator per element starting at +0, one fused multiply-add per k in
+ * ascending k, and a single round to bf16 at the end. */
+void oracle_combine(int N, int H, int E, int K, int cap,
+                    const uint16_t *expert_y, const int32_t *topk_idx,
+                    const int32_t *slot_of, const float *topk_weights,
+                    uint16_t *y) {
+  for (int64_t g = 0; g < N; ++g) {
+    for (int h = 0; h < H; ++h) {
+      float acc = 0.0f;
+      for (int k = 0; k < K; ++k) {
+        int e = topk_idx[g * K + k];
+        int s = slot_of[g * K + k];
+        if (e < 0 || e >= E || s < 0 || s >= cap) continue;
+        float v = oracle_bf16_to_f32(expert_y[((int64_t)e * cap + s) * H + h]);
+        acc = fmaf(topk_weights[g * K + k], v, acc);
+      }
+      y[g * H + h] = oracle_f32_to_bf16(acc);
+    }
+  }
+}

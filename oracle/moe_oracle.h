@@ -1,0 +1,116 @@
+/*
+ * moe_oracle.h -- plain, slow, single-threaded CPU oracle for MoE token
+ * dispatch and combine.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load this library.  The product
+ * path (the CUDA library under combine_moe_dispatch_gb300/) never calls it,
+ * shares no code with it, and fails loudly when its own extension is missing.
+ *
+ * What is computed, and where the pages define it:
+ *  - Routing: each token goes to K experts and the layer output is the
+ *    router-weighted sum of the expert outputs ("Efficient and portable
+ *    mixture-of-experts communication", Introduction).
+ *  - Plan: per-expert token counts (in the pages a single warp per block
+ *    tallies them while the others pack; same page, Dispatch), the cumulative
+ *    sum of those counts giving packing offsets ("Enabling trillion-parameter
+ *    models on AWS EFA", Dispatch and Combine; Send and Receive Buffers), and
+ *    return addresses (source rank, expert, token index) kept for combine
+ *    ("Efficient and portable mixture-of-experts communication", Dispatch).
+ *  - Dispatch payload: a bf16 copy, or fp8 with one scale per 128-element
+ *    activation vector computed on the fly from the absolute maximum ("Lower
+ *    latency and higher throughput with multi-node DeepSeek deployment",
+ *    Quantization).
+ *  - Combine: 16-bit un-quantised expert outputs, weighted average computed
+ *    at the receiver ("Efficient and portable mixture-of-experts
+ *    communication", Combine).
+ *
+ * Readings where the pages leave a step open (slot order, scale formula,
+ * rounding, accumulation order) are stated next to each function.
+ *
+ * Layouts (all row-major, global token id g = r*T + t, N = R*T):
+ *   topk_idx      [N, K]        int32
+ *   topk_weights  [N, K]        float
+ *   x             [N, H]        bf16 bit patterns (uint16)
+ *   expert_num_tokens [E]       int32
+ *   expert_rank_offsets [E, R+1] int32
+ *   slot_of       [N, K]        int32
+ *   src_of        [E, cap]      int32 (only [0, count) written)
+ *   expert_x      [E, cap, H]   bf16 bits, or e4m3 bytes
+ *   expert_x_scale [E, cap, H/128] float
+ *   expert_y      [E, cap, H]   bf16 bits
+ *   y             [N, H]        bf16 bits
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Result codes of the oracle (its own numbering; not shared with the CUDA
+ * library). */
+enum {
+  ORACLE_OK = 0,
+  ORACLE_BAD_EXPERT = 1, /* some topk_idx outside [0, E) */
+  ORACLE_CAPACITY = 2,   /* some expert receives more than cap rows */
+  ORACLE_BAD_SHAPE = 3   /* non-positive or inconsistent sizes */
+};
+
+/* ---- number formats ---------------------------------------------------- */
+/* bf16 bits -> float (exact). */
+float oracle_bf16_to_f32(uint16_t b);
+/* float -> bf16 bits, round to nearest, ties to even; NaN -> 0x7FC0 with the
+ * input's sign. */
+uint16_t oracle_f32_to_bf16(float f);
+/* OCP FP8 E4M3 ("FN") byte -> float (exact; 0x7F/0xFF -> NaN). */
+float oracle_e4m3_to_f32(uint8_t q);
+/* float -> OCP FP8 E4M3 byte: round to nearest, ties to even, finite
+ * overflow saturated to +-448, sign of zero kept, NaN -> 0x7F | sign. */
+uint8_t oracle_f32_to_e4m3(float f);
+/* Element-wise array forms of the four conversions above (for the tests). */
+void oracle_bf16_to_f32_n(int64_t n, const uint16_t *in, float *out);
+void oracle_f32_to_bf16_n(int64_t n, const float *in, uint16_t *out);
+void oracle_e4m3_to_f32_n(int64_t n, const uint8_t *in, float *out);
+void oracle_f32_to_e4m3_n(int64_t n, const float *in, uint8_t *out);
+
+/* ---- plan ---------------------------------------------------------------- */
+/* Counts, per-rank offsets, stable slots and return addresses.
+ * Returns ORACLE_OK, ORACLE_BAD_EXPERT (nothing written) or ORACLE_CAPACITY
+ * (counts/offsets written, slot_of written, src_of written only below cap). */
+int oracle_plan(int R, int T, int E, int K, int cap, const int32_t *topk_idx,
+                int32_t *expert_num_tokens, int32_t *expert_rank_offsets,
+                int32_t *slot_of, int32_t *src_of);
+
+/* ---- dispatch ------------------------------------------------------------ */
+/* bf16 payload: expert_x[e][slot_of[g,k]][:] = x[g][:] bit for bit. */
+void oracle_dispatch_bf16(int N, int H, int E, int K, int cap,
+                          const uint16_t *x, const int32_t *topk_idx,
+                          const int32_t *slot_of, uint16_t *expert_x);
+
+/* Quantise one H-element bf16 row to e4m3 with one fp32 scale per
+ * 128-element block.  H must be a multiple of 128. */
+void oracle_quant_row_e4m3(int H, const uint16_t *row, uint8_t *q,
+                           float *scale);
+
+/* fp8 payload: the quantised row of x[g] and its scales written to every
+ * (expert, slot) the token goes to. */
+void oracle_dispatch_fp8(int N, int H, int E, int K, int cap,
+                         const uint16_t *x, const int32_t *topk_idx,
+                         const int32_t *slot_of, uint8_t *expert_x,
+                         float *expert_x_scale);
+
+/* ---- combine ------------------------------------------------------------- */
+/* y[g][h] = bf16( fp32 fma chain over k = 0..K-1 of
+ *                 w[g,k] * expert_y[topk_idx[g,k]][slot_of[g,k]][h] ). */
+void oracle_combine(int N, int H, int E, int K, int cap,
+                    const uint16_t *expert_y, const int32_t *topk_idx,
+                    const int32_t *slot_of, const float *topk_weights,
+                    uint16_t *y);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_ORACLE_H */

@@ -1,0 +1,437 @@
+"""Checks that pin the CPU oracle to facts other than its own code.
+
+Every check takes an ``oracle.Oracle`` (the real build, or a deliberately
+broken copy compiled by ``test_oracle_mutants.py``) and raises
+AssertionError when the oracle disagrees with:
+
+* library routines that implement a special case of the same definition
+  (torch's bf16 and float8_e4m3fn casts, numpy's stable argsort),
+* brute force written differently from the oracle (nearest value in the
+  full E4M3 code table; exhaustive routings of tiny shapes),
+* closed forms and invariants (sum of counts = N*K; offsets end at the count;
+  slot_of and src_of are inverse maps; identity experts return x),
+* error bounds (combine within half a bf16 ulp plus the fp32 fma-chain error
+  of the exact fp64 sum; E4M3 dequantisation within half a grid step),
+* worked examples under ``tests/golden/`` (derivations in each file).
+"""
+from __future__ import annotations
+
+import itertools
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------------------
+# fixture parsing
+# ---------------------------------------------------------------------------
+
+def _ints(s):
+    return [int(t, 0) for t in s.split()]
+
+
+def read_kv(name):
+    """Parse a golden file of ``key: values`` lines (``#`` comments).  Keys
+    that repeat (``case:``) start a new record."""
+    recs, cur = [], {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, val = line.split(":", 1)
+            key, val = key.strip(), val.strip()
+            if key == "case" and cur:
+                recs.append(cur)
+                cur = {}
+            cur[key] = val
+    if cur:
+        recs.append(cur)
+    return recs
+
+
+# ---------------------------------------------------------------------------
+# independent references (library routines and brute force)
+# ---------------------------------------------------------------------------
+
+def torch_bf16_bits(v):
+    t = torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def torch_e4m3_bits(v):
+    t = torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def e4m3_table():
+    """Values of all 256 E4M3 codes, decoded by torch."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def e4m3_nearest(v):
+    """Brute force: the non-negative finite code nearest to |v| (ties to the
+    even code), signed like v; |v| >= 448 saturates.  NaN not handled."""
+    v = np.asarray(v, np.float32)
+    tab = e4m3_table()[:0x7F]                 # codes 0x00..0x7E, increasing
+    a = np.abs(v.astype(np.float64))
+    d = np.abs(a[:, None] - tab[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best                           # one code, or two on a tie
+    idx = np.where(cand.sum(axis=1) == 1, cand.argmax(axis=1), 0)
+    two = cand.sum(axis=1) == 2
+    if two.any():
+        lo = cand[two].argmax(axis=1)          # the tie is between lo and lo+1
+        idx[two] = np.where(lo % 2 == 0, lo, lo + 1)
+    code = idx.astype(np.uint8)
+    code[a >= 448.0] = 0x7E
+    sign = np.signbit(v)
+    return np.where(sign, code | 0x80, code).astype(np.uint8)
+
+
+def plan_by_sort(R, T, E, K, topk_idx):
+    """Plan outputs from numpy's stable argsort of the flattened routing."""
+    flat = np.asarray(topk_idx, np.int64).ravel()
+    order = np.argsort(flat, kind="stable")      # entries grouped by expert, in (g,k) order
+    cnt = np.bincount(flat, minlength=E).astype(np.int32)
+    start = np.concatenate([[0], np.cumsum(cnt)[:-1]])
+    slot = np.empty(flat.size, np.int64)
+    slot[order] = np.arange(flat.size) - start[flat[order]]
+    off = np.zeros((E, R + 1), np.int32)
+    for e in range(E):
+        pos = np.sort(np.nonzero(flat == e)[0])
+        off[e] = np.searchsorted(pos, np.arange(R + 1) * T * K)
+    return cnt, off, slot.reshape(-1, K).astype(np.int32), order, start
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+
+def _probe_floats():
+    rng = np.random.default_rng(1234)
+    all_bf16 = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    rand_bits = rng.integers(0, 2**32, 200000, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    normals = rng.standard_normal(100000).astype(np.float32)
+    # exact bf16 midpoints (ties) and their neighbours
+    up = np.arange(0, 65536, 7, dtype=np.uint32) << 16
+    ties = (up | 0x8000).view(np.float32)
+    near = np.concatenate([(up | 0x7FFF).view(np.float32), (up | 0x8001).view(np.float32)])
+    v = np.concatenate([all_bf16, rand_bits, normals, ties, near])
+    return v[~np.isnan(v)]
+
+
+def check_bf16(o):
+    v = _probe_floats()
+    got = o.f32_to_bf16(v)
+    assert np.array_equal(got, torch_bf16_bits(v)), "f32->bf16 differs from torch's cast"
+    nan = np.array([np.nan, -np.nan], np.float32)
+    back = o.bf16_to_f32(o.f32_to_bf16(nan))
+    assert np.isnan(back).all(), "NaN must stay NaN"
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    got = o.bf16_to_f32(bits)
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.array_equal(got.view(np.uint32)[~both_nan], ref.view(np.uint32)[~both_nan]), \
+        "bf16->f32 differs from torch's widening"
+
+
+def check_e4m3_decode(o):
+    tab = e4m3_table()
+    got = o.e4m3_to_f32(np.arange(256, dtype=np.uint8)).astype(np.float64)
+    nan = np.isnan(tab)
+    assert np.array_equal(np.isnan(got), nan), "E4M3 NaN codes"
+    assert np.array_equal(got[~nan], tab[~nan]), "E4M3 decode differs from torch"
+    assert nan.sum() == 2 and np.isnan(tab[0x7F]) and np.isnan(tab[0xFF])
+
+
+def _e4m3_probe():
+    with np.errstate(all="ignore"):
+        return _e4m3_probe_values()
+
+
+def _e4m3_probe_values():
+    rng = np.random.default_rng(99)
+    tab = e4m3_table()[:0x7F]
+    mids = (tab[:-1] + tab[1:]) / 2                      # exact ties
+    eps = np.abs(mids) * 2.0**-20
+    all_bf16 = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    v = np.concatenate([
+        mids, mids + eps, mids - eps, -mids, tab, -tab,
+        all_bf16, all_bf16 * np.float32(128.0), all_bf16 * np.float32(2.0**-7),
+        rng.standard_normal(50000) * 200, rng.standard_normal(20000) * 2.0**-8,
+        [0.0, -0.0, 448.0, -448.0, 449.0, 463.99, 464.0, 465.0, 479.0, 480.0, 1e30,
+         -1e30, np.inf, -np.inf, 2.0**-9, 2.0**-10, 1.5 * 2.0**-9, 2.0**-6, 2.0**-6 - 2.0**-10],
+    ]).astype(np.float32)
+    return v[~np.isnan(v)]
+
+
+def check_e4m3_encode(o):
+    v = _e4m3_probe()
+    got = o.f32_to_e4m3(v)
+    brute = e4m3_nearest(v)
+    bad = np.nonzero(got != brute)[0]
+    assert bad.size == 0, f"E4M3 encode differs from nearest-code search at {v[bad[:5]]}: " \
+                          f"{got[bad[:5]]} vs {brute[bad[:5]]}"
+    lib = torch_e4m3_bits(np.clip(v, -448.0, 448.0))
+    bad = np.nonzero(got != lib)[0]
+    assert bad.size == 0, f"E4M3 encode differs from torch's cast at {v[bad[:5]]}"
+    q = o.f32_to_e4m3(np.array([np.nan, -np.nan], np.float32))
+    assert set((q & 0x7F).tolist()) == {0x7F}, "NaN -> NaN code"
+
+
+# ---------------------------------------------------------------------------
+# plan
+# ---------------------------------------------------------------------------
+
+def _check_plan_matches_sort(o, R, T, E, K, cap, idx):
+    st, cnt, off, slot, src = o.plan(R, T, E, K, cap, idx)
+    rcnt, roff, rslot, order, start = plan_by_sort(R, T, E, K, idx)
+    assert np.array_equal(cnt, rcnt), "counts"
+    assert np.array_equal(off, roff), "rank offsets"
+    assert np.array_equal(slot, rslot), "slots"
+    exp_st = 0 if rcnt.max(initial=0) <= cap else 2
+    assert st == exp_st, f"status {st} != {exp_st}"
+    for e in range(E):
+        members = order[start[e]:start[e] + rcnt[e]]
+        n = min(rcnt[e], cap)
+        assert np.array_equal(src[e, :n], members[:n]), "src_of"
+        assert (src[e, n:] == -1).all(), "src_of written beyond count/capacity"
+
+
+def check_plan_exhaustive(o):
+    shapes = [(1, 3, 3, 2, 6), (3, 1, 4, 2, 3), (2, 2, 2, 2, 8), (2, 1, 3, 3, 2), (1, 2, 4, 1, 2)]
+    for R, T, E, K, cap in shapes:
+        N = R * T
+        for combo in itertools.product(range(E), repeat=N * K):
+            idx = np.array(combo, np.int32).reshape(N, K)
+            _check_plan_matches_sort(o, R, T, E, K, cap, idx)
+
+
+def check_plan_random(o):
+    rng = np.random.default_rng(7)
+    for R, T, E, K in [(4, 33, 16, 4), (8, 64, 256, 8), (3, 100, 384, 8), (5, 17, 8, 2), (1, 1, 1, 1)]:
+        N = R * T
+        keys = rng.random((N, E))
+        idx = np.argsort(keys, axis=1)[:, :K].astype(np.int32)
+        _check_plan_matches_sort(o, R, T, E, K, N, idx)
+        # invariants, stated without the sort
+        st, cnt, off, slot, src = o.plan(R, T, E, K, N, idx)
+        assert st == 0 and cnt.sum() == N * K, "sum of counts must equal R*T*K"
+        assert (cnt <= N).all(), "distinct experts: a count is at most N"
+        assert np.array_equal(off[:, R], cnt) and (off[:, 0] == 0).all()
+        assert (np.diff(off, axis=1) >= 0).all(), "offsets are a cumulative sum"
+        flat = idx.ravel()
+        for e in range(E):
+            row = src[e, :cnt[e]]
+            assert (np.diff(row) > 0).all(), "src_of strictly increasing"
+            assert (flat[row] == e).all()
+            assert np.array_equal(slot.ravel()[row], np.arange(cnt[e])), "slot_of o src_of = id"
+
+
+def check_plan_errors(o):
+    idx = np.array([[0, 1], [2, 3]], np.int32)
+    for bad in (-1, 4, 1 << 20):
+        b = idx.copy()
+        b[1, 0] = bad
+        st, cnt, off, slot, src = o.plan(1, 2, 4, 2, 2, b)
+        assert st == 1, "bad expert id -> BAD_EXPERT"
+        assert (cnt == -1).all() and (slot == -1).all() and (src == -1).all(), \
+            "nothing written on BAD_EXPERT"
+
+
+def check_plan_golden(o):
+    for name in ("plan_small.txt", "plan_small_capacity.txt"):
+        g = read_kv(name)[0]
+        R, T, E, K, cap = (int(g[k]) for k in ("R", "T", "E", "K", "cap"))
+        idx = np.array(_ints(g["topk_idx"]), np.int32).reshape(R * T, K)
+        st, cnt, off, slot, src = o.plan(R, T, E, K, cap, idx)
+        assert st == int(g["status"]), f"{name}: status"
+        assert cnt.tolist() == _ints(g["expert_num_tokens"]), f"{name}: counts"
+        assert off.ravel().tolist() == _ints(g["expert_rank_offsets"]), f"{name}: offsets"
+        assert slot.ravel().tolist() == _ints(g["slot_of"]), f"{name}: slots"
+        assert src.ravel().tolist() == _ints(g["src_of"]), f"{name}: src_of"
+
+
+# ---------------------------------------------------------------------------
+# dispatch
+# ---------------------------------------------------------------------------
+
+def _routing(rng, N, E, K):
+    return np.argsort(rng.random((N, E)), axis=1)[:, :K].astype(np.int32)
+
+
+def check_dispatch_bf16(o):
+    rng = np.random.default_rng(3)
+    R, T, E, K, H = 2, 40, 6, 3, 136
+    N = R * T
+    idx = _routing(rng, N, E, K)
+    x = rng.integers(0, 65536, (N, H), dtype=np.uint16)
+    st, cnt, off, slot, src = o.plan(R, T, E, K, N, idx)
+    sentinel = np.uint16(0xA5A5)
+    out = np.full((E, N, H), sentinel, np.uint16)
+    o.dispatch_bf16(x, idx, slot, E, N, out=out)
+    for g in range(N):
+        for k in range(K):
+            assert np.array_equal(out[idx[g, k], slot[g, k]], x[g]), "row copied bit for bit"
+    for e in range(E):
+        assert (out[e, cnt[e]:] == sentinel).all(), "rows beyond the count untouched"
+
+
+def check_fp8_golden(o):
+    for name in ("fp8_block.txt", "fp8_division.txt"):
+        _check_fp8_golden_file(o, name)
+
+
+def _check_fp8_golden_file(o, name):
+    g = read_kv(name)[0]
+    H = int(g["H"])
+    x = np.zeros(H, np.uint16)
+    pairs = _ints(g["x"])
+    for i, b in zip(pairs[0::2], pairs[1::2]):
+        x[i] = b
+    q_exp = np.zeros(H, np.uint8)
+    pairs = _ints(g["q"])
+    for i, b in zip(pairs[0::2], pairs[1::2]):
+        q_exp[i] = b
+    sc_exp = np.array(_ints(g["scale"]), np.uint32)
+    q, sc = o.quant_row_e4m3(x)
+    bad = np.nonzero(q != q_exp)[0]
+    assert bad.size == 0, f"{name}: bytes differ at {bad.tolist()}: {q[bad]} vs {q_exp[bad]}"
+    assert np.array_equal(sc.view(np.uint32), sc_exp), f"{name}: scales {sc}"
+
+
+def check_fp8_properties(o):
+    """Pins that hold for any row: the block maximum maps to +-448, the scale
+    times 448 recovers the maximum to within one fp32 rounding, every value
+    dequantises to within half an E4M3 grid step (plus the rounding of the
+    division), zero blocks give scale 0 and q = +0."""
+    rng = np.random.default_rng(11)
+    H = 1024
+    for trial in range(40):
+        f = rng.standard_normal(H).astype(np.float32) * np.float32(10.0 ** rng.uniform(-30, 30))
+        if trial % 5 == 0:
+            f[256:384] = 0.0                 # a zero block
+        row = torch_bf16_bits(f)
+        xv = torch.from_numpy(row.view(np.int16)).view(torch.bfloat16).float().numpy()
+        q, sc = o.quant_row_e4m3(row)
+        deq = e4m3_table()[q].astype(np.float64)
+        for b in range(H // 128):
+            blk = xv[b * 128:(b + 1) * 128].astype(np.float64)
+            amax = np.abs(blk).max()
+            s = float(sc[b])
+            if amax == 0:
+                assert s == 0.0 and (q[b * 128:(b + 1) * 128] == 0).all(), "zero block"
+                continue
+            assert abs(s * 448.0 - amax) <= amax * 2.0**-23, "scale = amax/448"
+            j = np.abs(blk).argmax()
+            assert (q[b * 128 + j] & 0x7F) == 0x7E, "block max maps to 448"
+            t = blk / s                                       # exact target in fp64
+            step = np.where(np.abs(t) < 2.0**-6, 2.0**-9,
+                            2.0 ** (np.floor(np.log2(np.maximum(np.abs(t), 2.0**-6))) - 3))
+            err = np.abs(deq[b * 128:(b + 1) * 128] - np.clip(t, -448, 448))
+            assert (err <= 0.5 * step + np.abs(t) * 2.0**-23).all(), "E4M3 rounding bound"
+
+
+def check_dispatch_fp8(o):
+    rng = np.random.default_rng(5)
+    R, T, E, K, H = 3, 21, 5, 2, 384
+    N = R * T
+    idx = _routing(rng, N, E, K)
+    x = torch_bf16_bits(rng.standard_normal((N, H)).astype(np.float32))
+    st, cnt, off, slot, src = o.plan(R, T, E, K, N, idx)
+    out = np.full((E, N, H), 0xA5, np.uint8)
+    sc = np.full((E, N, H // 128), np.float32(-7.0), np.float32)
+    o.dispatch_fp8(x, idx, slot, E, N, out=out, out_scale=sc)
+    for g in range(N):
+        q, s = o.quant_row_e4m3(x[g])
+        for k in range(K):
+            e, sl = idx[g, k], slot[g, k]
+            assert np.array_equal(out[e, sl], q) and np.array_equal(sc[e, sl], s), \
+                "quantised row and scales written to every slot of the token"
+    for e in range(E):
+        assert (out[e, cnt[e]:] == 0xA5).all() and (sc[e, cnt[e]:] == -7.0).all()
+
+
+# ---------------------------------------------------------------------------
+# combine
+# ---------------------------------------------------------------------------
+
+def check_combine_golden(o):
+    for c in read_kv("combine_small.txt"):
+        w = np.array(_ints(c["w"]), np.uint32).view(np.float32)
+        v = np.array(_ints(c["v"]), np.uint16)
+        K, H = w.size, 8
+        ey = np.repeat(v[:, None, None], H, axis=2).astype(np.uint16)    # [E=K, cap=1, H]
+        idx = np.arange(K, dtype=np.int32)[None, :]
+        slot = np.zeros((1, K), np.int32)
+        y = o.combine(ey, idx, slot, w[None, :])
+        assert (y == int(c["y"], 0)).all(), f"combine golden case {c['case']}: {hex(y[0, 0])}"
+
+
+def _combine_case(o, rng, R, T, E, K, H):
+    N = R * T
+    idx = _routing(rng, N, E, K)
+    z = rng.standard_normal((N, K))
+    w = (np.exp(z) / np.exp(z).sum(axis=1, keepdims=True)).astype(np.float32)
+    st, cnt, off, slot, src = o.plan(R, T, E, K, N, idx)
+    return N, idx, w, slot, cnt
+
+
+def check_combine_identity(o):
+    """Identity experts (expert_y = dispatched x) with weights summing to 1
+    return x exactly; K = 1 with weight 1 is a pure gather."""
+    rng = np.random.default_rng(21)
+    R, T, E, K, H = 2, 24, 7, 3, 264
+    N, idx, w, slot, cnt = _combine_case(o, rng, R, T, E, K, H)
+    x = torch_bf16_bits(rng.standard_normal((N, H)).astype(np.float32))
+    ey = o.dispatch_bf16(x, idx, slot, E, N)
+    y = o.combine(ey, idx, slot, w)
+    assert np.array_equal(y, x), "identity experts must return x"
+    # fp8 payload through identity experts: y = bf16(q * scale)
+    H8 = 256
+    x8 = torch_bf16_bits(rng.standard_normal((N, H8)).astype(np.float32))
+    q, sc = o.dispatch_fp8(x8, idx, slot, E, N)
+    deq = (e4m3_table()[q] * np.repeat(sc.astype(np.float64), 128, axis=2)).astype(np.float32)
+    ey8 = torch_bf16_bits(deq)
+    y8 = o.combine(ey8, idx, slot, w)
+    first = ey8[idx[:, 0], slot[:, 0]]
+    assert np.array_equal(y8, first), "identity experts on the fp8 payload"
+    # pure gather
+    idx1 = idx[:, :1].copy()
+    st, cnt1, off1, slot1, src1 = o.plan(R, T, E, 1, N, idx1)
+    ey1 = torch_bf16_bits(rng.standard_normal((E, N, H)).astype(np.float32))
+    y1 = o.combine(ey1, idx1, slot1, np.ones((N, 1), np.float32))
+    assert np.array_equal(y1, ey1[idx1[:, 0], slot1[:, 0]]), "K=1, w=1 is a gather"
+
+
+def check_combine_bound(o):
+    """|y - S| <= half a bf16 ulp of S plus the fp32 fma-chain error bound,
+    where S is the weighted sum in fp64 (error bound of the arithmetic)."""
+    rng = np.random.default_rng(31)
+    for R, T, E, K, H in [(2, 16, 9, 4, 128), (1, 40, 32, 8, 72)]:
+        N, idx, w, slot, cnt = _combine_case(o, rng, R, T, E, K, H)
+        ey = torch_bf16_bits(rng.standard_normal((E, N, H)).astype(np.float32))
+        y = o.combine(ey, idx, slot, w)
+        eyf = torch.from_numpy(ey.view(np.int16)).view(torch.bfloat16).double().numpy()
+        rows = eyf[idx, slot]                                 # [N, K, H]
+        terms = w.astype(np.float64)[:, :, None] * rows
+        S = terms.sum(axis=1)
+        A = np.abs(terms).sum(axis=1)
+        yf = torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).double().numpy()
+        e = np.floor(np.log2(np.maximum(np.abs(S), 2.0**-126)))
+        half_ulp = 2.0 ** (e - 8)
+        bound = half_ulp + (K + 1) * 2.0**-24 * A * 1.01 + 2.0**-133
+        assert (np.abs(yf - S) <= bound).all(), "combine outside the fp32 error bound"
+
+
+ALL_CHECKS = [
+    check_bf16, check_e4m3_decode, check_e4m3_encode,
+    check_plan_exhaustive, check_plan_random, check_plan_errors, check_plan_golden,
+    check_dispatch_bf16, check_fp8_golden, check_fp8_properties, check_dispatch_fp8,
+    check_combine_golden, check_combine_identity, check_combine_bound,
+]
