@@ -123,7 +123,7 @@ void oracle_f32_to_e4m3_n(int64_t n, const float *in, uint8_t *out) {
 int oracle_plan(int R, int T, int E, int K, int cap, const int32_t *topk_idx,
                 int32_t *expert_num_tokens, int32_t *expert_rank_offsets,
                 int32_t *slot_of, int32_t *src_of) {
-  if (R <= 0 || T <= 0 || E <= 0 || K <= 0 || cap <= 0) return ORACLE_BAD_SHAPE;
+  if (R <= 0 || T < 0 || E <= 0 || K <= 0 || cap <= 0) return ORACLE_BAD_SHAPE;
   const int64_t N = (int64_t)R * T;
 
   for (int64_t i = 0; i < N * K; ++i)

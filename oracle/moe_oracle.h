@@ -77,7 +77,8 @@ void oracle_e4m3_to_f32_n(int64_t n, const uint8_t *in, float *out);
 void oracle_f32_to_e4m3_n(int64_t n, const float *in, uint8_t *out);
 
 /* ---- plan ---------------------------------------------------------------- */
-/* Counts, per-rank offsets, stable slots and return addresses.
+/* Counts, per-rank offsets, stable slots and return addresses.  T may be 0
+ * (an empty batch: every count and offset is 0).
  * Returns ORACLE_OK, ORACLE_BAD_EXPERT (nothing written) or ORACLE_CAPACITY
  * (counts/offsets written, slot_of written, src_of written only below cap). */
 int oracle_plan(int R, int T, int E, int K, int cap, const int32_t *topk_idx,

@@ -233,6 +233,12 @@ def check_plan_random(o):
             assert np.array_equal(slot.ravel()[row], np.arange(cnt[e])), "slot_of o src_of = id"
 
 
+def check_plan_empty(o):
+    """An empty batch: the definitions give zero counts and offsets."""
+    st, cnt, off, slot, src = o.plan(3, 0, 5, 2, 4, np.zeros((0, 2), np.int32))
+    assert st == 0 and (cnt == 0).all() and (off == 0).all() and (src == -1).all()
+
+
 def check_plan_errors(o):
     idx = np.array([[0, 1], [2, 3]], np.int32)
     for bad in (-1, 4, 1 << 20):
@@ -431,7 +437,8 @@ def check_combine_bound(o):
 
 ALL_CHECKS = [
     check_bf16, check_e4m3_decode, check_e4m3_encode,
-    check_plan_exhaustive, check_plan_random, check_plan_errors, check_plan_golden,
+    check_plan_exhaustive, check_plan_random, check_plan_empty, check_plan_errors,
+    check_plan_golden,
     check_dispatch_bf16, check_fp8_golden, check_fp8_properties, check_dispatch_fp8,
     check_combine_golden, check_combine_identity, check_combine_bound,
 ]
