@@ -1,0 +1,469 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE dispatch/combine hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole path over one batch of seeded synthetic
+input: moe_plan, moe_dispatch (bf16 payload), moe_dispatch (fp8 e4m3 1x128
+payload, reusing the plan) and moe_combine, on the DeepSeek-V3-shaped decode
+layer by default (8 logical ranks x 128 tokens, H=7168, E=256, top-8).
+
+Timing: every call is bracketed by CUDA events on the stream it runs on, and
+L2 is flushed before the plan, before the fp8 dispatch and before the
+combine, outside the events (a write of twice the L2 size, then a read of
+the L2 size, so that no dirty flush lines are left for the timed call to
+write back); ms_per_step is the sum of the per-call event times.  ``value`` is algorithmic bytes per step over
+that time (padding rows and unused capacity are not counted).  ``e2e`` is the
+same metric through the same public calls with the inputs coming from
+pinned host memory and the result read back every step, copies inside the
+timed region.  ``cpu_baseline`` times the CPU oracle (single-threaded) on a
+bounded sample of the same workload.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--workload NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from combine_moe_dispatch_gb300 import inputs  # noqa: E402
+from combine_moe_dispatch_gb300.configs import WORKLOADS  # noqa: E402
+
+with open(os.path.join(ROOT, "BASELINE.json")) as _f:
+    METRIC = json.load(_f)["metric"]
+UNIT = "GB/s"
+KERNEL_SOURCES = {
+    "plan": "combine_moe_dispatch_gb300/csrc/moe_plan.cu",
+    "dispatch_bf16": "combine_moe_dispatch_gb300/csrc/moe_dispatch.cu",
+    "dispatch_fp8": "combine_moe_dispatch_gb300/csrc/moe_dispatch.cu",
+    "combine": "combine_moe_dispatch_gb300/csrc/moe_combine.cu",
+}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what the method must move; padding is not counted)
+# ---------------------------------------------------------------------------
+
+def call_bytes(wl) -> dict:
+    N, H, E, K, R = wl.N, wl.H, wl.E, wl.K, wl.R
+    maps = N * K * 4
+    return {
+        # read topk_idx; write slot_of, src_of, counts, rank offsets
+        "plan": maps + 2 * maps + E * 4 + E * (R + 1) * 4,
+        # read x, topk_idx, slot_of; write K copies of every row
+        "dispatch_bf16": N * H * 2 + 2 * maps + N * K * H * 2,
+        # read x, topk_idx, slot_of; write K copies of the e4m3 row and its H/128 scales
+        "dispatch_fp8": N * H * 2 + 2 * maps + N * K * H + N * K * (H // 128) * 4,
+        # read K expert rows per token, topk_idx, slot_of, weights; write y
+        "combine": N * K * H * 2 + 3 * maps + N * H * 2,
+    }
+
+
+def step_calls(wl) -> list:
+    """Every row of the hot path: plan, both dispatch payloads (fp8 needs
+    H % 128 == 0), combine."""
+    return ["plan", "dispatch_bf16"] + (["dispatch_fp8"] if wl.H % 128 == 0 else []) + ["combine"]
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    pat = re.compile(r"^traffic\s+(\S+)\s+(\S+)\s+(\d+)\s+(\S+)")
+    with open(path) as f:
+        for line in f:
+            m = pat.match(line.strip().strip("`"))
+            if m and m.group(1) == kernel and m.group(2) == workload:
+                return int(m.group(3)) if m.group(4) == sha else None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names[1:], parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, seed=0):
+    """One logical rank of the workload (its first T tokens), capacity T."""
+    import oracle
+    d = inputs.make(wl, seed)
+    T, H, E, K = wl.T, wl.H, wl.E, wl.K
+    idx = np.ascontiguousarray(d["topk_idx"][:T])
+    x = np.ascontiguousarray(d["x"][:T])
+    w = np.ascontiguousarray(d["topk_weights"][:T])
+    cap = T
+    bufs = {
+        "ex16": np.zeros((E, cap, H), np.uint16),
+        "ex8": np.zeros((E, cap, H), np.uint8),
+        "sc": np.zeros((E, cap, H // 128), np.float32),
+        "ey": np.zeros((E, cap, H), np.uint16),
+    }
+
+    class S:  # the sample as a one-rank workload, for byte counting
+        pass
+    s = S()
+    s.N, s.H, s.E, s.K, s.R, s.T, s.payloads = T, H, E, K, 1, T, wl.payloads
+    calls = step_calls(wl)
+
+    def step():
+        st, cnt, off, slot, src = oracle.plan(1, T, E, K, cap, idx)
+        if "dispatch_bf16" in calls:
+            oracle.dispatch_bf16(x, idx, slot, E, cap, out=bufs["ex16"])
+        if "dispatch_fp8" in calls:
+            oracle.dispatch_fp8(x, idx, slot, E, cap, out=bufs["ex8"], out_scale=bufs["sc"])
+        oracle.combine(bufs["ey"], idx, slot, w)
+    nbytes = sum(call_bytes(s)[c] for c in calls)
+    desc = (f"first logical rank of the workload ({T} tokens x K={K}, H={H}, E={E}), capacity {T}; "
+            f"one oracle pass of {', '.join(calls)} per step")
+    return step, nbytes, desc
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def run_cpu_baseline(wl, min_seconds=10.0, max_steps=1000):
+    step, nbytes, desc = oracle_sample(wl)
+    step()                                   # first touch of the output pages
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_steps and (time.perf_counter() - t0) < min_seconds:
+        step()
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": desc, "seconds_per_step": dt, "steps": n,
+            "host": f"{os.cpu_count()} cores, {cpu_model()}"}
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    step, nbytes, desc = oracle_sample(wl)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.description, "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc, "host": f"{os.cpu_count()} cores, {cpu_model()}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the GPU path
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_gpu(args, wl):
+    import torch
+    import combine_moe_dispatch_gb300 as moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    moe.load_library()
+    d = inputs.make(wl, args.seed)
+    N, H, E, K, R, T, cap = wl.N, wl.H, wl.E, wl.K, wl.R, wl.T, wl.cap
+    idx = torch.from_numpy(d["topk_idx"]).to(device)
+    x = torch.from_numpy(d["x"].view(np.int16)).to(device).view(torch.bfloat16)
+    w = torch.from_numpy(d["topk_weights"]).to(device)
+    calls = step_calls(wl)
+    sh16 = moe.make_shape(R, T, H, E, K, cap, moe.PAYLOAD_BF16)
+    sh8 = moe.make_shape(R, T, H, E, K, cap, moe.PAYLOAD_FP8_E4M3)
+    b16 = moe.Buffers(sh16, device=device, expert_y=False,
+                      expert_x="dispatch_bf16" in calls)
+    b8 = moe.Buffers(sh8, device=device, expert_y=False) if "dispatch_fp8" in calls else None
+    ey = inputs.expert_outputs_device(E, cap, H, args.seed, device=device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_w = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
+    flush_r = torch.zeros(max(l2, 64 << 20) // 2, dtype=torch.int32, device=device)
+    flush_sink = torch.empty(1, dtype=torch.int32, device=device)
+
+    class _Flush:
+        """Write a buffer of twice the L2 size, then read another one of the
+        L2 size, so the timed call starts with no data of its own in L2 and
+        no dirty lines of the flush left to write back."""
+        @staticmethod
+        def zero_():
+            flush_w.zero_()
+            torch.amax(flush_r, dim=0, keepdim=True, out=flush_sink)
+    flush = _Flush()
+    stream = torch.cuda.current_stream(device)
+
+    def do(name):
+        if name == "plan":
+            b16.plan(idx, stream)
+        elif name == "dispatch_bf16":
+            moe.dispatch(sh16, x, idx, b16.slot_of, b16.expert_x, None, b16.workspace, stream)
+        elif name == "dispatch_fp8":
+            moe.dispatch(sh8, x, idx, b16.slot_of, b8.expert_x, b8.expert_x_scale, b16.workspace,
+                         stream)
+        elif name == "combine":
+            moe.combine(sh16, ey, idx, b16.slot_of, w, b16.y, b16.workspace, stream)
+
+    flush_before = {"plan", "dispatch_fp8", "combine"}
+
+    def one_step(evs=None):
+        for i, name in enumerate(calls):
+            if name in flush_before:
+                flush.zero_()
+            if evs is not None:
+                evs[i][0].record(stream)
+            do(name)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    barrier()
+    assert moe.read_status(b16.workspace) == moe.Status.OK
+
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in calls] for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier()
+    for s in range(args.steps):
+        one_step(evs[s])
+    barrier()
+    clk = clocks.stop()
+    per_call = {c: [evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)]
+                for i, c in enumerate(calls)}
+    step_ms = sum(sum(v) for v in per_call.values()) / args.steps
+    step_ms = max_over_ranks(step_ms, world, device)
+    cb = call_bytes(wl)
+    step_bytes = sum(cb[c] for c in calls)
+    value = step_bytes * world / (step_ms * 1e-3) / 1e9
+
+    # e2e: pinned host inputs in, result out, copies inside the timed region
+    hx = torch.from_numpy(d["x"].view(np.int16)).pin_memory()
+    hidx = torch.from_numpy(d["topk_idx"]).pin_memory()
+    hw = torch.from_numpy(d["topk_weights"]).pin_memory()
+    hy = torch.empty((N, H), dtype=torch.int16).pin_memory()
+    hcnt = torch.empty(E, dtype=torch.int32).pin_memory()
+    h2d = hx.numel() * 2 + hidx.numel() * 4 + hw.numel() * 4
+    d2h = hy.numel() * 2 + hcnt.numel() * 4
+
+    def e2e_step():
+        x.view(torch.int16).copy_(hx, non_blocking=True)
+        idx.copy_(hidx, non_blocking=True)
+        w.copy_(hw, non_blocking=True)
+        for name in calls:
+            do(name)
+        hy.copy_(b16.y.view(torch.int16), non_blocking=True)
+        hcnt.copy_(b16.expert_num_tokens, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    barrier()
+    assert moe.read_status(b16.workspace) == moe.Status.OK
+    e2e_step_ms = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world, device)
+    e2e_value = step_bytes * world / (e2e_step_ms * 1e-3) / 1e9
+
+    # roofline of the dominant kernel
+    peak, peak_kind = read_peaks()
+    means = {c: statistics.mean(v) for c, v in per_call.items()}
+    dom = max(means, key=means.get)
+    achieved = cb[dom] / (means[dom] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                "peak_source": f"{peak_kind} hbm_gbs", "unit": UNIT, "frac": achieved / peak,
+                "traffic": recorded_traffic(dom, wl.name),
+                "algorithmic_bytes": cb[dom]}
+    calls_out = {}
+    for c in calls:
+        v = sorted(per_call[c])
+        calls_out[c] = {"us_median": 1e3 * statistics.median(v), "us_p10": 1e3 * v[len(v) // 10],
+                        "us_p90": 1e3 * v[min(len(v) - 1, (9 * len(v)) // 10)],
+                        "bytes": cb[c], "gbs": cb[c] / (means[c] * 1e-3) / 1e9,
+                        "frac_of_peak": cb[c] / (means[c] * 1e-3) / 1e9 / peak}
+    disp = {}
+    for p in ("bf16", "fp8"):
+        c = f"dispatch_{p}"
+        if c in calls:
+            us = 1e3 * (statistics.median(per_call["plan"]) + statistics.median(per_call[c]))
+            b = cb["plan"] + cb[c]
+            disp[p] = {"us": us, "gbs": b / (us * 1e-6) / 1e9, "frac_of_peak": b / (us * 1e-6) / 1e9 / peak}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(wl, min_seconds=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.description, "name": wl.name, "ranks": R,
+                       "tokens_per_rank": T, "hidden": H, "experts": E, "top_k": K,
+                       "capacity": cap, "routing": wl.routing, "calls_per_step": calls,
+                       "io": "bf16 activations and expert outputs, e4m3 + fp32 scales for the fp8 payload",
+                       "l2": "flushed before plan, fp8 dispatch and combine, outside the timed events (2x L2 write, then 2x L2 read so no dirty lines remain)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roofline,
+            "calls": calls_out,
+            "dispatch_incl_plan": disp,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
+                    "note": "expert_y stays resident on the device, as the expert GEMM leaves it"},
+            "gpu_launches": len(calls) * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dsv3_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_gpu(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,201 @@
+// moe_api.cu -- the C ABI of libmoe_gb300.so (declared in moe_dispatch.h):
+// host-side argument checks, workspace sizing and kernel launches.  Every
+// check here happens before anything is enqueued, so a rejected call leaves
+// the stream and the caller's buffers untouched.
+#include <stdint.h>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+int device_sm_count() {
+  static int cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+moe_status check_shape(const moe_shape *s) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (s->num_ranks <= 0 || s->tokens_per_rank < 0 || s->hidden <= 0 || s->num_experts <= 0 ||
+      s->top_k <= 0 || s->capacity <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (s->payload != MOE_PAYLOAD_BF16 && s->payload != MOE_PAYLOAD_FP8_E4M3)
+    return MOE_ERR_INVALID_ARG;
+  if (s->top_k > kMaxTopK || s->num_experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  const int64_t N = (int64_t)s->num_ranks * s->tokens_per_rank;
+  if (N * s->top_k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)s->num_experts * s->capacity >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (s->hidden % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (s->payload == MOE_PAYLOAD_FP8_E4M3 && s->hidden % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+WsHeader *header(void *ws) { return static_cast<WsHeader *>(ws); }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_shape *shape) {
+  if (check_shape(shape) != MOE_OK) return 0;
+  return ws_layout(*shape).total;
+}
+
+moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+  if (!workspace || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return MOE_ERR_ALIGNMENT;
+  return from_cuda(cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream));
+}
+
+moe_status moe_plan(const moe_shape *shape, const int32_t *topk_idx, int32_t *expert_num_tokens,
+                    int32_t *expert_rank_offsets, int32_t *slot_of, int32_t *src_of,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!topk_idx || !expert_num_tokens || !expert_rank_offsets || !slot_of || !src_of)
+    return MOE_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < ws_layout(*shape).total) return MOE_ERR_WORKSPACE;
+  if (!aligned(topk_idx, 4) || !aligned(expert_num_tokens, 4) || !aligned(expert_rank_offsets, 4) ||
+      !aligned(slot_of, 4) || !aligned(src_of, 4) || !aligned(workspace, 16))
+    return MOE_ERR_ALIGNMENT;
+
+  const PlanGeometry g = plan_geometry(*shape);
+  const WsLayout L = ws_layout(*shape);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (g.num_tiles == 0) {   // empty batch: zero counts and offsets, status OK
+    if (cudaMemsetAsync(expert_num_tokens, 0, sizeof(int32_t) * shape->num_experts, s) != cudaSuccess ||
+        cudaMemsetAsync(expert_rank_offsets, 0,
+                        sizeof(int32_t) * shape->num_experts * (shape->num_ranks + 1), s) != cudaSuccess ||
+        cudaMemsetAsync(&header(workspace)->status, 0, sizeof(int32_t), s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  char *base = static_cast<char *>(workspace);
+  PlanParams p;
+  p.topk_idx = topk_idx;
+  p.expert_num_tokens = expert_num_tokens;
+  p.expert_rank_offsets = expert_rank_offsets;
+  p.slot_of = slot_of;
+  p.src_of = src_of;
+  p.hdr = header(workspace);
+  p.agg_tag = reinterpret_cast<uint32_t *>(base + L.tags_off);
+  p.incl_tag = p.agg_tag + g.num_tiles;
+  p.agg = reinterpret_cast<int32_t *>(base + L.rows_off);
+  p.incl = p.agg + (size_t)g.num_tiles * shape->num_experts;
+  p.R = shape->num_ranks;
+  p.T = shape->tokens_per_rank;
+  p.E = shape->num_experts;
+  p.K = shape->top_k;
+  p.cap = shape->capacity;
+  p.tile_tokens = g.tile_tokens;
+  p.tiles_per_rank = g.tiles_per_rank;
+  p.num_tiles = g.num_tiles;
+  return from_cuda(launch_plan(p, s));
+}
+
+moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *topk_idx,
+                        const int32_t *slot_of, void *expert_x, float *expert_x_scale,
+                        void *workspace, void *stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  const bool fp8 = shape->payload == MOE_PAYLOAD_FP8_E4M3;
+  if (!x || !topk_idx || !slot_of || !expert_x || (fp8 && !expert_x_scale))
+    return MOE_ERR_INVALID_ARG;
+  if (!workspace) return MOE_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(expert_x, 16) || !aligned(topk_idx, 4) || !aligned(slot_of, 4) ||
+      (fp8 && !aligned(expert_x_scale, 4)) || !aligned(workspace, 16))
+    return MOE_ERR_ALIGNMENT;
+  if (shape->tokens_per_rank == 0) return MOE_OK;   // empty batch
+  DispatchParams p;
+  p.x = static_cast<const uint16_t *>(x);
+  p.topk_idx = topk_idx;
+  p.slot_of = slot_of;
+  p.expert_x = expert_x;
+  p.expert_x_scale = fp8 ? expert_x_scale : nullptr;
+  p.hdr = header(workspace);
+  p.N = shape->num_ranks * shape->tokens_per_rank;
+  p.H = shape->hidden;
+  p.E = shape->num_experts;
+  p.K = shape->top_k;
+  p.cap = shape->capacity;
+  cudaStream_t s = (cudaStream_t)stream;
+  return from_cuda(fp8 ? launch_dispatch_fp8(p, s) : launch_dispatch_bf16(p, s));
+}
+
+moe_status moe_combine(const moe_shape *shape, const void *expert_y, const int32_t *topk_idx,
+                       const int32_t *slot_of, const float *topk_weights, void *y,
+                       void *workspace, void *stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!expert_y || !topk_idx || !slot_of || !topk_weights || !y) return MOE_ERR_INVALID_ARG;
+  if (!workspace) return MOE_ERR_WORKSPACE;
+  if (!aligned(expert_y, 16) || !aligned(y, 16) || !aligned(topk_idx, 4) || !aligned(slot_of, 4) ||
+      !aligned(topk_weights, 4) || !aligned(workspace, 16))
+    return MOE_ERR_ALIGNMENT;
+  if (shape->tokens_per_rank == 0) return MOE_OK;   // empty batch
+  CombineParams p;
+  p.expert_y = static_cast<const uint16_t *>(expert_y);
+  p.topk_idx = topk_idx;
+  p.slot_of = slot_of;
+  p.topk_weights = topk_weights;
+  p.y = static_cast<uint16_t *>(y);
+  p.hdr = header(workspace);
+  p.N = shape->num_ranks * shape->tokens_per_rank;
+  p.H = shape->hidden;
+  p.E = shape->num_experts;
+  p.K = shape->top_k;
+  p.cap = shape->capacity;
+  return from_cuda(launch_combine(p, (cudaStream_t)stream));
+}
+
+moe_status moe_read_status(const void *workspace, void *stream, moe_status *out) {
+  if (!workspace || !out) return MOE_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&v, &static_cast<const WsHeader *>(workspace)->status, sizeof v,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  *out = (moe_status)v;
+  return MOE_OK;
+}
+
+const char *moe_status_string(moe_status status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_ALIGNMENT: return "misaligned pointer";
+    case MOE_ERR_BAD_EXPERT: return "expert id out of range";
+    case MOE_ERR_CAPACITY: return "expert capacity exceeded";
+    case MOE_ERR_TIMEOUT: return "wait between thread blocks timed out";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+moe_status moe_workspace_set_debug(void *workspace, uint32_t flags, uint64_t timeout_ns,
+                                   void *stream) {
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return MOE_ERR_ALIGNMENT;
+  return from_cuda(launch_set_debug(header(workspace), flags, timeout_ns, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,156 @@
+// moe_combine.cu -- gather-weighted-reduce of expert outputs back to tokens.
+//
+// What it computes ("Efficient and portable mixture-of-experts
+// communication", Introduction and Combine; "Enabling trillion-parameter
+// models on AWS EFA", Dispatch and Combine):
+//   y[g][h] = bf16_rn( acc ),  acc = 0; for k = 0..K-1:
+//             acc = fma(w[g,k], float(expert_y[idx[g,k]][slot_of[g,k]][h]), acc)
+// i.e. the receiver-side weighted sum of the 16-bit expert outputs, one fp32
+// accumulator per element, fixed k order, one final rounding.
+//
+// How: a warp takes one (token, segment) task at a time; lanes 0..K-1 hold
+// the token's K (expert, slot, weight) and broadcast them by shuffle.  For a
+// group of KG experts the warp issues all KG x U 16-byte loads before the
+// first multiply-add, so each lane keeps KG*U*16 bytes of reads in flight
+// (256 B per lane, 8 KB per warp); only populated rows are read.  The
+// accumulators stay in registers and the bf16 result is stored once, 16
+// bytes per lane.
+#include <cuda_bf16.h>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+constexpr int kCombineThreads = 256;
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+
+__device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4 &v) {
+  const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] = __fmaf_rn(w, __uint_as_float(a[i] << 16), acc[2 * i]);
+    acc[2 * i + 1] = __fmaf_rn(w, __uint_as_float(a[i] & 0xFFFF0000u), acc[2 * i + 1]);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return l | (h << 16);
+}
+
+template <int KG, int U>
+__global__ void __launch_bounds__(kCombineThreads)
+combine_kernel(CombineParams p) {
+  __shared__ int32_t s_status;
+  if (threadIdx.x == 0) s_status = read_status(p.hdr);
+  __syncthreads();
+  if (s_status != MOE_OK) return;
+
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kCombineThreads) >> 5;
+  const int cpr = p.H / 8;           // 16-byte chunks per row
+  constexpr int cpt = 32 * U;        // chunks per task
+  const int tpr = (cpr + cpt - 1) / cpt;
+  const int64_t ntasks = (int64_t)p.N * tpr;
+
+  for (int64_t task = warp0; task < ntasks; task += nwarps) {
+    const int64_t g = task / tpr;
+    const int seg = (int)(task - g * tpr);
+    int e_l = -1, s_l = -1;
+    float w_l = 0.0f;
+    if (lane < p.K) {
+      e_l = __ldg(p.topk_idx + g * p.K + lane);
+      s_l = __ldg(p.slot_of + g * p.K + lane);
+      w_l = __ldg(p.topk_weights + g * p.K + lane);
+    }
+    const bool e_ok = e_l >= 0 && e_l < p.E;
+    const bool ok = lane < p.K && e_ok && s_l >= 0 && s_l < p.cap;
+    if (seg == 0 && lane < p.K && !ok)
+      report_status(p.hdr, e_ok ? MOE_ERR_CAPACITY : MOE_ERR_BAD_EXPERT);
+    const unsigned okmask = __ballot_sync(kFullMask, ok);
+
+    const int c0 = seg * cpt + lane;
+    float acc[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+
+    for (int kb = 0; kb < p.K; kb += KG) {
+      uint4 v[KG][U];
+#pragma unroll
+      for (int kk = 0; kk < KG; ++kk) {
+        const int k = kb + kk;
+        const int e = __shfl_sync(kFullMask, e_l, k & 31);
+        const int s = __shfl_sync(kFullMask, s_l, k & 31);
+        const bool use = k < p.K && ((okmask >> (k & 31)) & 1u);
+        const uint16_t *row = p.expert_y + ((int64_t)(use ? e : 0) * p.cap + (use ? s : 0)) * p.H;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + u * 32;
+          v[kk][u] = (use && c < cpr) ? __ldcs(reinterpret_cast<const uint4 *>(row + (int64_t)c * 8))
+                                      : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < KG; ++kk) {
+        const int k = kb + kk;
+        const float w = __shfl_sync(kFullMask, w_l, k & 31);
+        if (k < p.K && ((okmask >> (k & 31)) & 1u)) {
+#pragma unroll
+          for (int u = 0; u < U; ++u) fma8(acc[u], w, v[kk][u]);
+        }
+      }
+    }
+
+    uint16_t *out = p.y + g * p.H;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u * 32;
+      if (c < cpr) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+        o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+        o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+        o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+        *reinterpret_cast<uint4 *>(out + (int64_t)c * 8) = o;
+      }
+    }
+  }
+}
+
+namespace {
+int combine_occ[3][64];
+
+template <int KG, int U>
+cudaError_t launch_variant(const CombineParams &p, cudaStream_t stream, int which) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  int per_sm = combine_occ[which][dev];
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<KG, U>,
+                                                      kCombineThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    combine_occ[which][dev] = per_sm;
+  }
+  const int cpr = p.H / 8;
+  const int64_t tasks = (int64_t)p.N * ((cpr + 32 * U - 1) / (32 * U));
+  const int64_t want = (tasks + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
+  const int64_t cap = (int64_t)device_sm_count() * per_sm;
+  const int grid = (int)(want < cap ? (want < 1 ? 1 : want) : cap);
+  combine_kernel<KG, U><<<grid, kCombineThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
+  if (p.K <= 2) return launch_variant<2, 8>(p, stream, 0);
+  if (p.K <= 4) return launch_variant<4, 4>(p, stream, 1);
+  return launch_variant<8, 2>(p, stream, 2);
+}
+
+}  // namespace moe

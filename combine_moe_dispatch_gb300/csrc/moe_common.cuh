@@ -1,0 +1,178 @@
+// moe_common.cuh -- definitions shared by the kernels and the C ABI of
+// libmoe_gb300.so: workspace layout, plan geometry, launch parameters and a
+// few PTX helpers (acquire/release flags, the global timer).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_dispatch.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Plan geometry.  The routed entries are cut into tiles of whole tokens that
+// never straddle a rank boundary, so that rank r's offsets are the exclusive
+// prefix of tile (r, 0).  One thread block handles one tile.
+// ---------------------------------------------------------------------------
+constexpr int kPlanThreads = 512;
+constexpr int kPlanWarps = kPlanThreads / 32;
+constexpr int kPlanTileEntries = 1024;                          // entries (g,k) per tile, at most
+constexpr int kPlanBatchesPerWarp = kPlanTileEntries / (32 * kPlanWarps);  // 2
+constexpr int kMaxExperts = 2048;
+constexpr int kMaxTopK = 32;
+
+struct PlanGeometry {
+  int tile_tokens;     // TT: tokens per tile
+  int tiles_per_rank;  // ceil(T / TT)
+  int num_tiles;       // R * tiles_per_rank
+};
+
+inline PlanGeometry plan_geometry(const moe_shape &s) {
+  PlanGeometry g;
+  if (s.tokens_per_rank == 0) {   // empty batch: no tiles
+    g.tile_tokens = 1;
+    g.tiles_per_rank = 0;
+    g.num_tiles = 0;
+    return g;
+  }
+  int tt = kPlanTileEntries / s.top_k;
+  if (tt < 1) tt = 1;
+  if (tt > s.tokens_per_rank) tt = s.tokens_per_rank;
+  g.tile_tokens = tt;
+  g.tiles_per_rank = (s.tokens_per_rank + tt - 1) / tt;
+  g.num_tiles = s.num_ranks * g.tiles_per_rank;
+  return g;
+}
+
+// ---------------------------------------------------------------------------
+// Workspace: a 256-byte header, then per-tile flags and per-tile count rows.
+// ---------------------------------------------------------------------------
+struct WsHeader {
+  uint32_t ticket;      // next tile id to hand out (reset by the last tile)
+  uint32_t done;        // tiles finished in the running plan (reset by the last tile)
+  uint32_t epoch;       // plan launches so far; tags this launch's flags
+  uint32_t err_bits;    // errors seen by the running plan (kErr*)
+  int32_t status;       // moe_status of the last plan (and of later dispatch/combine)
+  uint32_t debug_flags; // kDebug* test hooks
+  uint64_t timeout_ns;  // limit of every wait; 0 = kDefaultTimeoutNs
+  uint32_t reserved[56];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+constexpr uint32_t kErrBadExpert = 1u;
+constexpr uint32_t kErrCapacity = 2u;
+constexpr uint32_t kErrTimeout = 4u;
+constexpr uint32_t kDebugHoldTile0 = 1u;
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t tags_off;    // uint32 agg_tag[num_tiles], incl_tag[num_tiles]
+  size_t rows_off;    // int32 agg[num_tiles][E], incl[num_tiles][E]
+  size_t total;
+};
+
+inline WsLayout ws_layout(const moe_shape &s) {
+  PlanGeometry g = plan_geometry(s);
+  WsLayout L;
+  L.tags_off = sizeof(WsHeader);
+  L.rows_off = L.tags_off + align_up(2 * (size_t)g.num_tiles * sizeof(uint32_t), 256);
+  L.total = L.rows_off + align_up(2 * (size_t)g.num_tiles * s.num_experts * sizeof(int32_t), 256);
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel parameters.
+// ---------------------------------------------------------------------------
+struct PlanParams {
+  const int32_t *topk_idx;
+  int32_t *expert_num_tokens;
+  int32_t *expert_rank_offsets;
+  int32_t *slot_of;
+  int32_t *src_of;
+  WsHeader *hdr;
+  uint32_t *agg_tag;
+  uint32_t *incl_tag;
+  int32_t *agg;
+  int32_t *incl;
+  int R, T, E, K, cap;
+  int tile_tokens, tiles_per_rank, num_tiles;
+};
+
+struct DispatchParams {
+  const uint16_t *x;
+  const int32_t *topk_idx;
+  const int32_t *slot_of;
+  void *expert_x;
+  float *expert_x_scale;
+  WsHeader *hdr;
+  int N, H, E, K, cap;
+};
+
+struct CombineParams {
+  const uint16_t *expert_y;
+  const int32_t *topk_idx;
+  const int32_t *slot_of;
+  const float *topk_weights;
+  uint16_t *y;
+  WsHeader *hdr;
+  int N, H, E, K, cap;
+};
+
+// Launchers (return the cudaError_t of the launch).
+cudaError_t launch_plan(const PlanParams &p, cudaStream_t stream);
+cudaError_t launch_dispatch_bf16(const DispatchParams &p, cudaStream_t stream);
+cudaError_t launch_dispatch_fp8(const DispatchParams &p, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+cudaError_t launch_set_debug(WsHeader *hdr, uint32_t flags, uint64_t timeout_ns,
+                             cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// ---------------------------------------------------------------------------
+// Device helpers.
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait until *flag == want, for at most `deadline` (global timer, ns) and a
+// bounded number of polls.  Returns false when the wait ran out.
+__device__ __forceinline__ bool wait_flag(const uint32_t *flag, uint32_t want, uint64_t deadline) {
+  constexpr uint32_t kMaxPolls = 1u << 26;
+  for (uint32_t it = 0; it < kMaxPolls; ++it) {
+    if (ld_acquire_gpu(flag) == want) return true;
+    if ((it & 15u) == 15u && global_timer_ns() > deadline) return false;
+    __nanosleep(32);
+  }
+  return false;
+}
+
+// The status the dispatch and combine kernels see; read once per block.
+__device__ __forceinline__ int32_t read_status(const WsHeader *hdr) {
+  return *reinterpret_cast<const volatile int32_t *>(&hdr->status);
+}
+
+// Record a data error found by dispatch/combine (first error wins).
+__device__ __forceinline__ void report_status(WsHeader *hdr, int32_t code) {
+  atomicCAS(reinterpret_cast<int *>(&hdr->status), 0, code);
+}
+#endif
+
+}  // namespace moe

@@ -1,0 +1,188 @@
+/*
+ * moe_dispatch.h -- C ABI of the GB300 (sm_103a) MoE token dispatch/combine
+ * library, libmoe_gb300.so.
+ *
+ * The problem, as the pages state it: every token of a data-parallel group
+ * goes to its top-K experts; a dispatch step moves each token's hidden row
+ * into contiguous per-expert buffers that feed the grouped expert GEMM, and a
+ * combine step returns the experts' outputs to the token and forms their
+ * router-weighted sum ("Efficient and portable mixture-of-experts
+ * communication", Introduction, Portable Kernels, Dispatch, Combine).  Here
+ * the R "ranks" are logical partitions of one GPU's HBM: rank r owns tokens
+ * [r*T, (r+1)*T) of every token-indexed array.  No call talks to another GPU.
+ *
+ * Notation: R ranks, T tokens per rank, N = R*T, H hidden size, E experts,
+ * K experts per token, cap rows per expert in the padded buffers, global
+ * token id g = r*T + t, routed entry (g, k).  All arrays are row-major.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers: every array is caller-owned DEVICE memory on the current
+ *    device, unless stated otherwise.  The library allocates no memory and
+ *    keeps no global state; everything that persists lives in the caller's
+ *    workspace.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Every call only enqueues work on `stream` and returns
+ *    without waiting for the device, except moe_read_status.  Calls are
+ *    therefore usable inside CUDA-graph capture.
+ *  - One workspace must not be used by two calls that may run at the same
+ *    time (different streams without ordering).
+ *  - Errors: argument errors are detected on the host and returned at once,
+ *    with nothing enqueued.  Errors that depend on the data (an expert id out
+ *    of range, more rows for an expert than `cap`, a wait that timed out) are
+ *    found by the plan kernel and stored in the workspace status word; the
+ *    dispatch and combine kernels read it first and write nothing when it is
+ *    set.  moe_read_status returns it.
+ */
+#ifndef MOE_DISPATCH_H
+#define MOE_DISPATCH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, size overflow */
+  MOE_ERR_UNSUPPORTED = 2,  /* shape outside the supported limits (below) */
+  MOE_ERR_ALIGNMENT = 3,    /* a pointer is not aligned as required */
+  MOE_ERR_BAD_EXPERT = 4,   /* device: some topk_idx outside [0, E) */
+  MOE_ERR_CAPACITY = 5,     /* device: some expert receives more than cap rows */
+  MOE_ERR_TIMEOUT = 6,      /* device: a wait between thread blocks ran out */
+  MOE_ERR_CUDA = 7,         /* a CUDA runtime call or kernel launch failed */
+  MOE_ERR_WORKSPACE = 8     /* workspace missing or smaller than required */
+} moe_status;
+
+typedef enum {
+  MOE_PAYLOAD_BF16 = 0,     /* expert_x rows are bf16 copies of x */
+  MOE_PAYLOAD_FP8_E4M3 = 1  /* expert_x rows are OCP E4M3 bytes + fp32 scales */
+} moe_payload;
+
+/* Problem shape.  Limits: all sizes >= 1 except T, which may be 0 (an empty
+ * batch: moe_plan writes zero counts and offsets, dispatch and combine do
+ * nothing); K <= 32; E <= 2048; N*K < 2^31; E*cap < 2^31; H % 8 == 0
+ * (H % 128 == 0 for the fp8 payload). */
+typedef struct {
+  int32_t num_ranks;        /* R */
+  int32_t tokens_per_rank;  /* T */
+  int32_t hidden;           /* H */
+  int32_t num_experts;      /* E */
+  int32_t top_k;            /* K */
+  int32_t capacity;         /* cap: rows per expert in expert_x / expert_y */
+  int32_t payload;          /* a moe_payload value */
+} moe_shape;
+
+/* Bytes of workspace the calls need for this shape (host only, no CUDA
+ * call).  Returns 0 when the shape is invalid or unsupported. */
+size_t moe_workspace_size(const moe_shape *shape);
+
+/* Zero a workspace before its first use (enqueued on `stream`).  After
+ * that the workspace keeps its counters consistent by itself, across shapes
+ * and across calls that reported an error (the last thread block of every
+ * moe_plan resets them).  A zero-filled allocation is already initialised.
+ * Errors: INVALID_ARG (null), ALIGNMENT (not 16-byte aligned), CUDA. */
+moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/* Plan: per-expert counts, per-rank offsets and stable slots.
+ *
+ * Follows "Efficient and portable mixture-of-experts communication",
+ * Dispatch (the sender counts the tokens each expert receives; the receiver
+ * records source rank, expert and token index so combine can send each row
+ * back) and "Enabling trillion-parameter models on AWS EFA", Send and Receive
+ * Buffers / Dispatch and Combine (counts are known before any row is
+ * written; a cumulative sum of per-expert counts gives every sender its
+ * offset in the receiver's contiguous buffer).  The pages' receivers place
+ * rows in arrival order; here the order is stable by (rank, token, k).
+ *
+ * In:   topk_idx            [N, K] int32, expert of routed entry (g, k)
+ * Out:  expert_num_tokens   [E] int32:   count[e] = #{(g,k): idx = e}
+ *       expert_rank_offsets [E, R+1] int32: entry r = #{(g,k): idx = e, g < r*T};
+ *                           entry R = count[e]
+ *       slot_of             [N, K] int32: row of (g,k) inside its expert's
+ *                           buffer = #{(g',k') before (g,k) with the same expert}
+ *       src_of              [E, cap] int32: src_of[e][slot_of[g,k]] = g*K + k;
+ *                           only rows [0, min(count, cap)) are written
+ * Work: `workspace` of at least moe_workspace_size(shape) bytes, 16-byte
+ *       aligned, initialised once by moe_workspace_init.
+ * Device errors (status word): BAD_EXPERT (outputs unspecified), CAPACITY
+ *       (counts, offsets and slot_of are exact; src_of rows stop at cap),
+ *       TIMEOUT.  The status word is replaced by each moe_plan call.
+ * Host errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT (int32 arrays need 4-byte
+ *       alignment), WORKSPACE, CUDA. */
+moe_status moe_plan(const moe_shape *shape, const int32_t *topk_idx,
+                    int32_t *expert_num_tokens, int32_t *expert_rank_offsets,
+                    int32_t *slot_of, int32_t *src_of,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* Dispatch: write each token's row to every (expert, slot) it is routed to.
+ *
+ * Follows "Efficient and portable mixture-of-experts communication", Dispatch
+ * (tokens with their block scales are packed and moved into contiguous
+ * per-expert tensors for the grouped GEMM) and, for the fp8 payload, "Lower
+ * latency and higher throughput with multi-node DeepSeek deployment",
+ * Quantization (activations quantised on the fly, one scale per 128-element
+ * vector from its absolute maximum).
+ *
+ * In:   x            [N, H] bf16, 16-byte aligned
+ *       topk_idx     [N, K] int32, slot_of [N, K] int32 (from moe_plan)
+ * Out:  expert_x     [E, cap, H]: bf16 (payload BF16) or E4M3 bytes (payload
+ *                    FP8_E4M3), 16-byte aligned.  Row (e, s) is written only
+ *                    for s < count[e]; other rows are not touched.
+ *       expert_x_scale [E, cap, H/128] fp32 for FP8_E4M3 (4-byte aligned),
+ *                    NULL for BF16.  Per 128-block: scale = amax / 448,
+ *                    q = e4m3_rn_satfinite(x / scale); an all-zero block has
+ *                    scale 0 and q = 0.
+ * Work: the workspace moe_plan used; the call writes nothing if its status
+ *       word is set.  Requires moe_plan on the same topk_idx, ordered before
+ *       this call.  An entry whose expert or slot is out of range is skipped
+ *       and sets the status word (BAD_EXPERT / CAPACITY).
+ * Host errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA. */
+moe_status moe_dispatch(const moe_shape *shape, const void *x,
+                        const int32_t *topk_idx, const int32_t *slot_of,
+                        void *expert_x, float *expert_x_scale,
+                        void *workspace, void *stream);
+
+/* Combine: y[g] = bf16( sum over k of w[g,k] * expert_y[idx[g,k]][slot_of[g,k]] ).
+ *
+ * Follows "Efficient and portable mixture-of-experts communication",
+ * Introduction and Combine (the receiver reads the 16-bit expert outputs of
+ * each token and forms their router-weighted sum) and "Enabling
+ * trillion-parameter models on AWS EFA", Dispatch and Combine.  Arithmetic:
+ * one fp32 accumulator from +0, one fused multiply-add per k in ascending k,
+ * one round-to-nearest-even to bf16.
+ *
+ * In:   expert_y     [E, cap, H] bf16, 16-byte aligned; only rows
+ *                    (idx[g,k], slot_of[g,k]) are read
+ *       topk_idx, slot_of [N, K] int32; topk_weights [N, K] fp32
+ * Out:  y            [N, H] bf16, 16-byte aligned
+ * Work: the workspace moe_plan used; nothing is written if its status word
+ *       is set; entries out of range are skipped and set it.
+ * Host errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA. */
+moe_status moe_combine(const moe_shape *shape, const void *expert_y,
+                       const int32_t *topk_idx, const int32_t *slot_of,
+                       const float *topk_weights, void *y,
+                       void *workspace, void *stream);
+
+/* Synchronise `stream` and read the workspace status word into *out (MOE_OK
+ * or a device error).  The only call that waits for the device; meant for
+ * tests and error handling, not for the hot path.
+ * Errors: INVALID_ARG, CUDA. */
+moe_status moe_read_status(const void *workspace, void *stream, moe_status *out);
+
+/* Static description of a status code (never NULL). */
+const char *moe_status_string(moe_status status);
+
+/* Test hook (enqueued on `stream`): `flags` bit 0 makes the first tile of
+ * the next moe_plan calls withhold its counts from the others, so their
+ * bounded waits run out and the call reports MOE_ERR_TIMEOUT;
+ * `timeout_ns` replaces the 1 s default limit of those waits (0 = default).
+ * Errors: INVALID_ARG, CUDA. */
+moe_status moe_workspace_set_debug(void *workspace, uint32_t flags,
+                                   uint64_t timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_DISPATCH_H */

@@ -1,0 +1,107 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every entry
+point ``include/*.h`` declares, sizes workspaces on the host, and rejects bad
+arguments before enqueuing anything.  Only calls that must fail argument
+checks are made here, so no kernel is ever launched."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import combine_moe_dispatch_gb300 as moe
+from combine_moe_dispatch_gb300 import Shape, Status, make_shape
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe.build()
+    return moe.load_library()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(moe_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "moe_plan" in names and "moe_dispatch" in names and "moe_combine" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+        assert n in moe.SIGNATURES, f"{n} has no binding"
+
+
+def test_status_strings(lib):
+    for s in Status:
+        assert moe.status_string(s) and moe.status_string(s) != "unknown status"
+    assert moe.status_string(99) == "unknown status"
+
+
+def test_workspace_size(lib):
+    s = make_shape(8, 128, 7168, 256, 8, 1024, moe.PAYLOAD_FP8_E4M3)
+    ws = moe.workspace_size(s)
+    # 256-byte header + tags + 2 count rows per tile (8 ranks x 1 tile of 128 tokens)
+    assert ws == 256 + 256 + 2 * 8 * 256 * 4
+    assert moe.workspace_size(make_shape(0, 1, 8, 1, 1, 1)) == 0
+    assert moe.workspace_size(make_shape(1, 1, 8, 1, 33, 1)) == 0          # K > 32
+    assert moe.workspace_size(make_shape(1, 1, 8, 4096, 1, 1)) == 0        # E > 2048
+    assert moe.workspace_size(make_shape(1, 1, 12, 1, 1, 1)) == 0          # H % 8
+    assert moe.workspace_size(make_shape(1, 1, 136, 1, 1, 1, moe.PAYLOAD_FP8_E4M3)) == 0
+    assert moe.workspace_size(make_shape(1, 1, 8, 2, 1, 1 << 30)) == 0     # E*cap >= 2^31
+    assert moe.workspace_size(make_shape(1, 1, 8, 1, 1, 1, 7)) == 0        # payload
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_host_rejections_enqueue_nothing(lib):
+    s = make_shape(2, 4, 256, 8, 2, 8)
+    ws_bytes = moe.workspace_size(s)
+    A = 0x100000   # aligned fake address: never dereferenced, every call below fails its checks
+    sp = ctypes.byref(s)
+    # null pointers
+    assert lib.moe_plan(sp, None, _p(A), _p(A), _p(A), _p(A), _p(A), ws_bytes, None) == Status.INVALID_ARG
+    assert lib.moe_dispatch(sp, None, _p(A), _p(A), _p(A), None, _p(A), None) == Status.INVALID_ARG
+    assert lib.moe_combine(sp, _p(A), _p(A), _p(A), None, _p(A), _p(A), None) == Status.INVALID_ARG
+    # workspace too small / missing
+    assert lib.moe_plan(sp, _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), ws_bytes - 1, None) == Status.WORKSPACE
+    assert lib.moe_dispatch(sp, _p(A), _p(A), _p(A), _p(A), None, None, None) == Status.WORKSPACE
+    # misaligned pointers
+    assert lib.moe_plan(sp, _p(A + 2), _p(A), _p(A), _p(A), _p(A), _p(A), ws_bytes, None) == Status.ALIGNMENT
+    assert lib.moe_dispatch(sp, _p(A + 8), _p(A), _p(A), _p(A), None, _p(A), None) == Status.ALIGNMENT
+    assert lib.moe_combine(sp, _p(A), _p(A), _p(A), _p(A), _p(A + 4), _p(A), None) == Status.ALIGNMENT
+    # fp8 payload needs the scale array
+    s8 = make_shape(2, 4, 256, 8, 2, 8, moe.PAYLOAD_FP8_E4M3)
+    assert lib.moe_dispatch(ctypes.byref(s8), _p(A), _p(A), _p(A), _p(A), None, _p(A), None) \
+        == Status.INVALID_ARG
+    # bad shapes
+    bad = make_shape(2, 4, 256, 8, 0, 8)
+    assert lib.moe_plan(ctypes.byref(bad), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), 1 << 20, None) \
+        == Status.INVALID_ARG
+    big_k = make_shape(2, 4, 256, 64, 40, 8)
+    assert lib.moe_combine(ctypes.byref(big_k), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None) \
+        == Status.UNSUPPORTED
+    assert lib.moe_plan(None, _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), 1 << 20, None) == Status.INVALID_ARG
+    out = ctypes.c_int(0)
+    assert lib.moe_read_status(None, None, ctypes.byref(out)) == Status.INVALID_ARG
+    assert lib.moe_workspace_init(None, 256, None) == Status.INVALID_ARG
+    assert lib.moe_workspace_init(_p(A + 4), 256, None) == Status.ALIGNMENT
+    assert lib.moe_workspace_set_debug(None, 1, 0, None) == Status.INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = moe._lib
+    moe._lib = None
+    try:
+        with pytest.raises(moe.LibraryNotBuilt):
+            moe.load_library(str(tmp_path / "nope.so"))
+    finally:
+        moe._lib = saved

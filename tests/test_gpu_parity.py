@@ -1,0 +1,107 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Small shapes (whole outputs compared) span several plan tiles per rank,
+ragged last tiles, ragged hidden segments, K = 1 and K = 32, E = 1 and
+E = 2048, duplicate experts per token, and an empty batch.  The five
+workloads run at full size in the launch configuration the benchmark times;
+there the oracle recomputes every plan output and dispatched row, and the
+combine output of all tokens (or of a seeded sample of 1024 tokens when the
+expert outputs are generated on the device)."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from combine_moe_dispatch_gb300 import inputs
+from combine_moe_dispatch_gb300.configs import WORKLOADS
+import gpu_check
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand_case(seed, R, T, H, E, K, distinct=True):
+    rng = np.random.default_rng(seed)
+    N = R * T
+    if distinct:
+        idx = np.argsort(rng.random((N, E)), axis=1)[:, :K].astype(np.int32)
+    else:
+        idx = rng.integers(0, E, (N, K)).astype(np.int32)
+    x = inputs.to_bf16_bits(rng.standard_normal((N, H)).astype(np.float32))
+    z = rng.standard_normal((N, K))
+    w = (np.exp(z) / np.exp(z).sum(1, keepdims=True)).astype(np.float32)
+    return idx, x, w
+
+
+SMALL = [
+    # name, R, T, H, E, K, payloads
+    ("tiles_ragged_k5", 2, 500, 392, 37, 5, ("bf16",)),
+    ("tiles_ragged_fp8", 3, 300, 640, 64, 8, ("bf16", "fp8")),
+    ("k_equals_e", 5, 7, 128, 3, 3, ("bf16", "fp8")),
+    ("one_expert", 2, 33, 256, 1, 1, ("bf16", "fp8")),
+    ("k32", 1, 50, 256, 40, 32, ("bf16", "fp8")),
+    ("many_ranks", 64, 40, 256, 16, 2, ("bf16",)),
+    ("many_tiles", 1, 20000, 128, 96, 8, ("fp8",)),
+    ("e2048", 1, 256, 256, 2048, 8, ("bf16", "fp8")),
+    ("h8", 3, 17, 8, 5, 2, ("bf16",)),
+]
+
+
+@pytest.mark.parametrize("name,R,T,H,E,K,payloads", SMALL, ids=[c[0] for c in SMALL])
+def test_small_shapes(name, R, T, H, E, K, payloads):
+    idx, x, w = _rand_case(zlib.crc32(name.encode()), R, T, H, E, K)
+    res = gpu_check.run_case(R, T, H, E, K, R * T, idx, x, w, payloads)
+    assert res["not_bit_exact"] == 0, f"expected bit-exact combine, {res}"
+
+
+def test_duplicate_experts_per_token():
+    idx, x, w = _rand_case(5, 2, 64, 256, 4, 4, distinct=False)
+    gpu_check.run_case(2, 64, 256, 4, 4, 2 * 64 * 4, idx, x, w, ("bf16", "fp8"))
+
+
+def test_empty_batch():
+    R, T, H, E, K = 3, 0, 256, 8, 2
+    idx = np.zeros((0, K), np.int32)
+    x = np.zeros((0, H), np.uint16)
+    w = np.zeros((0, K), np.float32)
+    gpu_check.run_case(R, T, H, E, K, 4, idx, x, w, ("bf16", "fp8"))
+
+
+def test_tight_capacity_is_exact_fit():
+    # cap equal to the largest count: every row of the busiest expert is used
+    idx, x, w = _rand_case(9, 2, 200, 256, 8, 2)
+    cap = int(np.bincount(idx.ravel(), minlength=8).max())
+    gpu_check.run_case(2, 200, 256, 8, 2, cap, idx, x, w, ("bf16", "fp8"))
+
+
+def test_repeated_calls_reuse_workspace():
+    # the same buffers through several plans of different routings
+    import combine_moe_dispatch_gb300 as moe
+    R, T, H, E, K = 4, 300, 256, 32, 4
+    shape = moe.make_shape(R, T, H, E, K, R * T)
+    buf = moe.Buffers(shape, expert_y=False)
+    import oracle
+    for seed in range(6):
+        idx, x, w = _rand_case(100 + seed, R, T, H, E, K)
+        buf.plan(gpu_check.dev(idx))
+        assert moe.read_status(buf.workspace) == moe.Status.OK
+        st, cnt, off, slot, src = oracle.plan(R, T, E, K, R * T, idx)
+        assert np.array_equal(buf.slot_of.cpu().numpy(), slot)
+        assert np.array_equal(buf.expert_rank_offsets.cpu().numpy(), off)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "dsv3_decode", "dsv3_prefill", "kimi_decode"])
+def test_workload_full_size(name):
+    wl = WORKLOADS[name]
+    d = inputs.make(wl, 0)
+    big = wl.E * wl.cap * wl.H > (1 << 28)
+    sample = None
+    if big and wl.N > 1024:
+        sample = np.sort(np.random.default_rng(0).choice(wl.N, 1024, replace=False))
+        sample[0], sample[-1] = 0, wl.N - 1
+    payloads = wl.payloads
+    res = gpu_check.run_case(wl.R, wl.T, wl.H, wl.E, wl.K, wl.cap, d["topk_idx"], d["x"],
+                             d["topk_weights"], payloads,
+                             expert_y="device" if big else "host", combine_tokens=sample)
+    print(name, res)
+    torch.cuda.empty_cache()
