@@ -77,6 +77,7 @@ SIGNATURES = {
     "moe_read_status": ([_P, _P, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "moe_workspace_set_debug": ([_P, _U32, _U64, _P], ctypes.c_int),
+    "moe_plan_noalloc": ([_SP, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
 }
 
 _lib = None
@@ -165,6 +166,18 @@ def combine(shape: Shape, expert_y, topk_idx, slot_of, topk_weights, y, workspac
                                     _ptr(slot_of), _ptr(topk_weights), _ptr(y), _ptr(workspace),
                                     _stream(stream))
     return _check(st, "moe_combine", check)
+
+
+def plan_noalloc(shape: Shape, topk_idx, expert_num_tokens, expert_rank_offsets, slot_of, src_of,
+                 status_out, stream=None, check=True) -> Status:
+    """moe_plan for callers that cannot allocate: scratch in the library's
+    static device array; the plan's status goes to the device int32
+    ``status_out``."""
+    st = load_library().moe_plan_noalloc(ctypes.byref(shape), _ptr(topk_idx),
+                                         _ptr(expert_num_tokens), _ptr(expert_rank_offsets),
+                                         _ptr(slot_of), _ptr(src_of), _ptr(status_out),
+                                         _stream(stream))
+    return _check(st, "moe_plan_noalloc", check)
 
 
 def read_status(workspace, stream=None) -> Status:

@@ -174,6 +174,32 @@ moe_status moe_read_status(const void *workspace, void *stream, moe_status *out)
 /* Static description of a status code (never NULL). */
 const char *moe_status_string(moe_status status);
 
+/* moe_plan without a workspace, for callers that cannot allocate device
+ * memory: code that is handed only its inputs and outputs, such as a plugin
+ * whose host framework owns every device allocation, or a latency-critical
+ * caller that must not call cudaMalloc because it can synchronise the
+ * device.  The pages have no counterpart; it computes exactly what moe_plan
+ * computes.
+ *
+ * Scratch: a 1 MiB static device array inside the library, held by every
+ * GPU that loads the library until the process exits.  Shapes whose
+ * moe_workspace_size exceeds 1 MiB are rejected with MOE_ERR_WORKSPACE.  All
+ * calls on a device share the array: calls that may run at the same time on
+ * the GPU (different streams without ordering) race, and must not be issued.
+ * Each call clears the array's counters and flags before its kernel runs.
+ * The first call on each device looks up the array's device address with
+ * that device current (a one-time set-up); make that first call before any
+ * stream capture.
+ * In/Out: as moe_plan; status_out is a device int32 that receives the plan's
+ *       status (MOE_OK or a device error, as moe_read_status would report).
+ *       Nothing is allocated and nothing waits for the device.
+ * Host errors: INVALID_ARG, UNSUPPORTED, WORKSPACE (shape too large for the
+ *       static scratch), ALIGNMENT, CUDA. */
+moe_status moe_plan_noalloc(const moe_shape *shape, const int32_t *topk_idx,
+                            int32_t *expert_num_tokens, int32_t *expert_rank_offsets,
+                            int32_t *slot_of, int32_t *src_of, int32_t *status_out,
+                            void *stream);
+
 /* Test hook (enqueued on `stream`): `flags` bit 0 makes the first tile of
  * the next moe_plan calls withhold its counts from the others, so their
  * bounded waits run out and the call reports MOE_ERR_TIMEOUT;
