@@ -6,11 +6,13 @@ input: moe_plan, moe_dispatch (bf16 payload), moe_dispatch (fp8 e4m3 1x128
 payload, reusing the plan) and moe_combine, on the DeepSeek-V3-shaped decode
 layer by default (8 logical ranks x 128 tokens, H=7168, E=256, top-8).
 
-Timing: every call is bracketed by CUDA events on the stream it runs on, and
-L2 is flushed before the plan, before the fp8 dispatch and before the
-combine, outside the events (a write of twice the L2 size, then a read of
-the L2 size, so that no dirty flush lines are left for the timed call to
-write back); ms_per_step is the sum of the per-call event times.  ``value`` is algorithmic bytes per step over
+Timing: each step is one CUDA-graph replay of the calls (how a serving
+engine runs a layer: one graph per batch size); K steps run back to back
+between two CUDA events, rotating through several buffer sets so that no
+call finds its inputs, or dirty lines of its outputs, left in L2 by the
+previous call (every step moves more than twice the L2 size).  Per-kernel
+times come from graphs of back-to-back launches of one call over the same
+rotating sets.  ``value`` is algorithmic bytes per step over
 that time (padding rows and unused capacity are not counted).  ``e2e`` is the
 same metric through the same public calls with the inputs coming from
 pinned host memory and the result read back every step, copies inside the
@@ -262,6 +264,49 @@ def max_over_ranks(value: float, world: int, device) -> float:
     return float(t.item())
 
 
+class BufferSet:
+    """Inputs and outputs of one step on the device; the timed loops rotate
+    through several sets so no call finds the previous call's data in L2."""
+
+    def __init__(self, moe, torch, wl, d, device, calls, cap, seed):
+        import numpy as np
+        R, T, H, E, K = wl.R, wl.T, wl.H, wl.E, wl.K
+        self.sh16 = moe.make_shape(R, T, H, E, K, cap, moe.PAYLOAD_BF16)
+        self.sh8 = moe.make_shape(R, T, H, E, K, cap, moe.PAYLOAD_FP8_E4M3)
+        self.idx = torch.from_numpy(d["topk_idx"]).to(device)
+        self.x = torch.from_numpy(d["x"].view(np.int16)).to(device).view(torch.bfloat16)
+        self.w = torch.from_numpy(d["topk_weights"]).to(device)
+        self.b16 = moe.Buffers(self.sh16, device=device, expert_y=False,
+                               expert_x="dispatch_bf16" in calls)
+        self.b8 = (moe.Buffers(self.sh8, device=device, expert_y=False, expert_x=True)
+                   if "dispatch_fp8" in calls else None)
+        self.ey = inputs.expert_outputs_device(E, cap, H, seed, device=device)
+        self.moe = moe
+
+    def do(self, name, stream):
+        moe, b16, b8 = self.moe, self.b16, self.b8
+        if name == "plan":
+            b16.plan(self.idx, stream)
+        elif name == "dispatch_bf16":
+            moe.dispatch(self.sh16, self.x, self.idx, b16.slot_of, b16.expert_x, None,
+                         b16.workspace, stream)
+        elif name == "dispatch_fp8":
+            moe.dispatch(self.sh8, self.x, self.idx, b16.slot_of, b8.expert_x, b8.expert_x_scale,
+                         b16.workspace, stream)
+        elif name == "combine":
+            moe.combine(self.sh16, self.ey, self.idx, b16.slot_of, self.w, b16.y, b16.workspace,
+                        stream)
+
+    @staticmethod
+    def nbytes(wl, cap, calls):
+        per = wl.N * wl.H * 2 * 2 + wl.E * cap * wl.H * 2           # x, y, expert_y
+        if "dispatch_bf16" in calls:
+            per += wl.E * cap * wl.H * 2
+        if "dispatch_fp8" in calls:
+            per += wl.E * cap * wl.H + wl.E * cap * (wl.H // 128) * 4
+        return per
+
+
 def run_gpu(args, wl):
     import torch
     import combine_moe_dispatch_gb300 as moe
@@ -285,76 +330,114 @@ def run_gpu(args, wl):
     moe.load_library()
     d = inputs.make(wl, args.seed)
     N, H, E, K, R, T, cap = wl.N, wl.H, wl.E, wl.K, wl.R, wl.T, wl.cap
-    idx = torch.from_numpy(d["topk_idx"]).to(device)
-    x = torch.from_numpy(d["x"].view(np.int16)).to(device).view(torch.bfloat16)
-    w = torch.from_numpy(d["topk_weights"]).to(device)
     calls = step_calls(wl)
-    sh16 = moe.make_shape(R, T, H, E, K, cap, moe.PAYLOAD_BF16)
-    sh8 = moe.make_shape(R, T, H, E, K, cap, moe.PAYLOAD_FP8_E4M3)
-    b16 = moe.Buffers(sh16, device=device, expert_y=False,
-                      expert_x="dispatch_bf16" in calls)
-    b8 = moe.Buffers(sh8, device=device, expert_y=False) if "dispatch_fp8" in calls else None
-    ey = inputs.expert_outputs_device(E, cap, H, args.seed, device=device)
+    if args.only:
+        calls = [c for c in calls if c in ("plan", args.only)]
+    if args.tight_capacity:
+        cap = int(np.bincount(d["topk_idx"].ravel(), minlength=E).max())
+    cb = call_bytes(wl)
+    step_bytes = sum(cb[c] for c in calls)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush_w = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
-    flush_r = torch.zeros(max(l2, 64 << 20) // 2, dtype=torch.int32, device=device)
-    flush_sink = torch.empty(1, dtype=torch.int32, device=device)
 
-    class _Flush:
-        """Write a buffer of twice the L2 size, then read another one of the
-        L2 size, so the timed call starts with no data of its own in L2 and
-        no dirty lines of the flush left to write back."""
-        @staticmethod
-        def zero_():
-            flush_w.zero_()
-            torch.amax(flush_r, dim=0, keepdim=True, out=flush_sink)
-    flush = _Flush()
-    stream = torch.cuda.current_stream(device)
+    # Enough buffer sets that one rotation moves >= 2x L2 in its smallest call,
+    # within half of the free device memory.
+    smallest = min(cb[c] for c in calls if c != "plan") if len(calls) > 1 else cb["plan"]
+    nsets = max(2, min(6, -(-2 * l2 // max(1, smallest))))
+    free = torch.cuda.mem_get_info(device)[0]
+    while nsets > 1 and nsets * BufferSet.nbytes(wl, cap, calls) > free // 2:
+        nsets -= 1
+    sets = [BufferSet(moe, torch, wl, d, device, calls, cap, args.seed + i) for i in range(nsets)]
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize()
 
-    def do(name):
-        if name == "plan":
-            b16.plan(idx, stream)
-        elif name == "dispatch_bf16":
-            moe.dispatch(sh16, x, idx, b16.slot_of, b16.expert_x, None, b16.workspace, stream)
-        elif name == "dispatch_fp8":
-            moe.dispatch(sh8, x, idx, b16.slot_of, b8.expert_x, b8.expert_x_scale, b16.workspace,
-                         stream)
-        elif name == "combine":
-            moe.combine(sh16, ey, idx, b16.slot_of, w, b16.y, b16.workspace, stream)
+    # warm-up, eager
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for bs in sets:
+                for c in calls:
+                    bs.do(c, stream)
+    stream.synchronize()
+    assert all(moe.read_status(bs.b16.workspace, stream) == moe.Status.OK for bs in sets)
 
-    flush_before = {"plan", "dispatch_fp8", "combine"}
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn(torch.cuda.current_stream(device))
+        return g
 
-    def one_step(evs=None):
-        for i, name in enumerate(calls):
-            if name in flush_before:
-                flush.zero_()
-            if evs is not None:
-                evs[i][0].record(stream)
-            do(name)
-            if evs is not None:
-                evs[i][1].record(stream)
+    # one graph per buffer set: one whole step
+    step_graphs = [capture(lambda st, bs=bs: [bs.do(c, st) for c in calls]) for bs in sets]
+    # one graph per call: M back-to-back launches over the rotating sets
+    reps = max(1, 24 // nsets)
+    call_graphs = {c: capture(lambda st, c=c: [bs.do(c, st) for _ in range(reps) for bs in sets])
+                   for c in calls}
+    # the dispatch as a user runs it: the plan, then the dispatch that may
+    # start while the plan finishes
+    for c in calls:
+        if c.startswith("dispatch_"):
+            call_graphs["plan+" + c] = capture(
+                lambda st, c=c: [(bs.do("plan", st), bs.do(c, st)) for _ in range(reps) for bs in sets])
+    with torch.cuda.stream(stream):
+        for g in step_graphs + list(call_graphs.values()):
+            for _ in range(args.warmup):
+                g.replay()
+    torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        one_step()
-    barrier()
-    assert moe.read_status(b16.workspace) == moe.Status.OK
-
-    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-            for _ in calls] for _ in range(args.steps)]
+    # timed region: exactly K steps, back to back
+    # (graph replays launch on the current stream: keep it the timed stream)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     barrier()
-    for s in range(args.steps):
-        one_step(evs[s])
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(args.steps):
+            step_graphs[s % nsets].replay()
+        e1.record(stream)
     barrier()
+    step_ms = e0.elapsed_time(e1) / args.steps
+    # per-kernel durations: M launches per replay, a few replays
+    per_call = {}
+    with torch.cuda.stream(stream):
+        for c, g in call_graphs.items():
+            ts = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b) / (reps * nsets))
+            per_call[c] = ts
     clk = clocks.stop()
-    per_call = {c: [evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)]
-                for i, c in enumerate(calls)}
-    step_ms = sum(sum(v) for v in per_call.values()) / args.steps
+    assert all(moe.read_status(bs.b16.workspace, stream) == moe.Status.OK for bs in sets)
+
     step_ms = max_over_ranks(step_ms, world, device)
-    cb = call_bytes(wl)
-    step_bytes = sum(cb[c] for c in calls)
     value = step_bytes * world / (step_ms * 1e-3) / 1e9
+
+    if args.only:
+        if rank == 0:
+            print(json.dumps({"only": args.only, "capacity": cap,
+                              "us": {c: 1e3 * statistics.median(v) for c, v in per_call.items()}}))
+        return 0
+
+    # cold single calls (diagnostic): eager, L2 flushed by a 2x L2 write before
+    # each, CUDA events around the call; includes the launch and event latency
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
+    cold = {c: [] for c in calls}
+    bs = sets[0]
+    with torch.cuda.stream(stream):
+        for it in range(13):
+            for c in calls:
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                bs.do(c, stream)
+                b.record(stream)
+                b.synchronize()
+                if it >= 3:
+                    cold[c].append(1e3 * a.elapsed_time(b))
+    del flush
 
     # e2e: pinned host inputs in, result out, copies inside the timed region
     hx = torch.from_numpy(d["x"].view(np.int16)).pin_memory()
@@ -365,36 +448,35 @@ def run_gpu(args, wl):
     h2d = hx.numel() * 2 + hidx.numel() * 4 + hw.numel() * 4
     d2h = hy.numel() * 2 + hcnt.numel() * 4
 
-    def e2e_step():
-        x.view(torch.int16).copy_(hx, non_blocking=True)
-        idx.copy_(hidx, non_blocking=True)
-        w.copy_(hw, non_blocking=True)
-        for name in calls:
-            do(name)
-        hy.copy_(b16.y.view(torch.int16), non_blocking=True)
-        hcnt.copy_(b16.expert_num_tokens, non_blocking=True)
+    def e2e_step(bs):
+        bs.x.view(torch.int16).copy_(hx, non_blocking=True)
+        bs.idx.copy_(hidx, non_blocking=True)
+        bs.w.copy_(hw, non_blocking=True)
+        for c in calls:
+            bs.do(c, stream)
+        hy.copy_(bs.b16.y.view(torch.int16), non_blocking=True)
+        hcnt.copy_(bs.b16.expert_num_tokens, non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    barrier()
-    e2e_ms = []
-    for _ in range(args.steps):
-        flush.zero_()
+    with torch.cuda.stream(stream):
+        for i in range(max(1, args.warmup)):
+            e2e_step(sets[i % nsets])
+        stream.synchronize()
+        barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        e2e_step()
+        for s in range(args.steps):
+            e2e_step(sets[s % nsets])
         b.record(stream)
         b.synchronize()
-        e2e_ms.append(a.elapsed_time(b))
     barrier()
-    assert moe.read_status(b16.workspace) == moe.Status.OK
-    e2e_step_ms = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world, device)
+    assert moe.read_status(sets[0].b16.workspace, stream) == moe.Status.OK
+    e2e_step_ms = max_over_ranks(a.elapsed_time(b) / args.steps, world, device)
     e2e_value = step_bytes * world / (e2e_step_ms * 1e-3) / 1e9
 
     # roofline of the dominant kernel
     peak, peak_kind = read_peaks()
-    means = {c: statistics.mean(v) for c, v in per_call.items()}
-    dom = max(means, key=means.get)
+    means = {c: statistics.median(v) for c, v in per_call.items()}
+    dom = max((c for c in calls), key=means.get)
     achieved = cb[dom] / (means[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "peak_source": f"{peak_kind} hbm_gbs", "unit": UNIT, "frac": achieved / peak,
@@ -402,18 +484,19 @@ def run_gpu(args, wl):
                 "algorithmic_bytes": cb[dom]}
     calls_out = {}
     for c in calls:
-        v = sorted(per_call[c])
-        calls_out[c] = {"us_median": 1e3 * statistics.median(v), "us_p10": 1e3 * v[len(v) // 10],
-                        "us_p90": 1e3 * v[min(len(v) - 1, (9 * len(v)) // 10)],
-                        "bytes": cb[c], "gbs": cb[c] / (means[c] * 1e-3) / 1e9,
-                        "frac_of_peak": cb[c] / (means[c] * 1e-3) / 1e9 / peak}
+        us = 1e3 * means[c]
+        calls_out[c] = {"us": us, "bytes": cb[c], "gbs": cb[c] / (us * 1e-6) / 1e9,
+                        "frac_of_peak": cb[c] / (us * 1e-6) / 1e9 / peak,
+                        "cold_call_us_median": statistics.median(cold[c])}
     disp = {}
-    for p in ("bf16", "fp8"):
-        c = f"dispatch_{p}"
+    for p_ in ("bf16", "fp8"):
+        c = f"dispatch_{p_}"
         if c in calls:
-            us = 1e3 * (statistics.median(per_call["plan"]) + statistics.median(per_call[c]))
-            b = cb["plan"] + cb[c]
-            disp[p] = {"us": us, "gbs": b / (us * 1e-6) / 1e9, "frac_of_peak": b / (us * 1e-6) / 1e9 / peak}
+            us = 1e3 * means["plan+" + c]
+            b_ = cb["plan"] + cb[c]
+            disp[p_] = {"us": us, "gbs": b_ / (us * 1e-6) / 1e9,
+                        "frac_of_peak": b_ / (us * 1e-6) / 1e9 / peak,
+                        "note": "moe_plan then moe_dispatch, back to back in one graph"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -429,7 +512,13 @@ def run_gpu(args, wl):
                        "tokens_per_rank": T, "hidden": H, "experts": E, "top_k": K,
                        "capacity": cap, "routing": wl.routing, "calls_per_step": calls,
                        "io": "bf16 activations and expert outputs, e4m3 + fp32 scales for the fp8 payload",
-                       "l2": "flushed before plan, fp8 dispatch and combine, outside the timed events (2x L2 write, then 2x L2 read so no dirty lines remain)",
+                       "l2": (f"no flush: inputs larger than L2 -- each step moves {step_bytes / 1e6:.0f} MB "
+                              f"({step_bytes / l2:.1f}x L2) and the timed loop rotates through "
+                              f"{nsets} buffer sets, so no call finds the previous call's data or "
+                              "dirty lines of its own outputs in L2"),
+                       "timing": ("each step is one CUDA-graph replay of the calls; K steps back to back "
+                                  "between two CUDA events; per-kernel times from graphs of "
+                                  f"{reps * nsets} back-to-back launches over the rotating sets"),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roofline,
             "calls": calls_out,
@@ -437,7 +526,7 @@ def run_gpu(args, wl):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
-                    "note": "expert_y stays resident on the device, as the expert GEMM leaves it"},
+                    "note": "eager public calls; expert_y stays resident on the device, as the expert GEMM leaves it"},
             "gpu_launches": len(calls) * args.steps,
             "clocks": clk,
         }
@@ -457,6 +546,11 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="profiling: time only this call (plus the plan it needs); no e2e")
+    ap.add_argument("--tight-capacity", action="store_true",
+                    help="profiling: capacity = the largest per-expert count (smaller buffers, "
+                         "same rows moved)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
     wl = WORKLOADS[args.workload]

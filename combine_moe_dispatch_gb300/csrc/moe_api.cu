@@ -4,6 +4,8 @@
 // the stream and the caller's buffers untouched.
 #include <stdint.h>
 
+#include <mutex>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -19,6 +21,39 @@ int device_sm_count() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+int occupancy_blocks(const void *kern, int threads, size_t smem) {
+  struct Entry {
+    const void *kern;
+    int dev, threads;
+    size_t smem;
+    int blocks;
+  };
+  static Entry cache[64];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].kern == kern && cache[i].dev == dev && cache[i].threads == threads &&
+        cache[i].smem == smem)
+      return cache[i].blocks;
+  int v = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, smem) != cudaSuccess || v < 1) {
+    cudaGetLastError();
+    v = 1;
+  }
+  if (used < 64) cache[used++] = Entry{kern, dev, threads, smem, v};
+  return v;
+}
+
+int persistent_grid(const void *kern, int threads, int64_t warp_tasks) {
+  const int64_t want = (warp_tasks + threads / 32 - 1) / (threads / 32);
+  const int64_t cap = (int64_t)device_sm_count() * occupancy_blocks(kern, threads, 0);
+  const int64_t g = want < cap ? want : cap;
+  return (int)(g < 1 ? 1 : g);
 }
 
 namespace {
@@ -68,7 +103,8 @@ moe_status moe_plan(const moe_shape *shape, const int32_t *topk_idx, int32_t *ex
                     void *workspace, size_t workspace_bytes, void *stream) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
-  if (!topk_idx || !expert_num_tokens || !expert_rank_offsets || !slot_of || !src_of)
+  const bool empty = shape->tokens_per_rank == 0;   // topk_idx, slot_of may then be NULL
+  if ((!empty && (!topk_idx || !slot_of)) || !expert_num_tokens || !expert_rank_offsets || !src_of)
     return MOE_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < ws_layout(*shape).total) return MOE_ERR_WORKSPACE;
   if (!aligned(topk_idx, 4) || !aligned(expert_num_tokens, 4) || !aligned(expert_rank_offsets, 4) ||
@@ -114,6 +150,7 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *to
                         void *workspace, void *stream) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
+  if (shape->tokens_per_rank == 0) return MOE_OK;   // empty batch: nothing to read or write
   const bool fp8 = shape->payload == MOE_PAYLOAD_FP8_E4M3;
   if (!x || !topk_idx || !slot_of || !expert_x || (fp8 && !expert_x_scale))
     return MOE_ERR_INVALID_ARG;
@@ -121,7 +158,6 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *to
   if (!aligned(x, 16) || !aligned(expert_x, 16) || !aligned(topk_idx, 4) || !aligned(slot_of, 4) ||
       (fp8 && !aligned(expert_x_scale, 4)) || !aligned(workspace, 16))
     return MOE_ERR_ALIGNMENT;
-  if (shape->tokens_per_rank == 0) return MOE_OK;   // empty batch
   DispatchParams p;
   p.x = static_cast<const uint16_t *>(x);
   p.topk_idx = topk_idx;
@@ -143,12 +179,12 @@ moe_status moe_combine(const moe_shape *shape, const void *expert_y, const int32
                        void *workspace, void *stream) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
+  if (shape->tokens_per_rank == 0) return MOE_OK;   // empty batch: nothing to read or write
   if (!expert_y || !topk_idx || !slot_of || !topk_weights || !y) return MOE_ERR_INVALID_ARG;
   if (!workspace) return MOE_ERR_WORKSPACE;
   if (!aligned(expert_y, 16) || !aligned(y, 16) || !aligned(topk_idx, 4) || !aligned(slot_of, 4) ||
       !aligned(topk_weights, 4) || !aligned(workspace, 16))
     return MOE_ERR_ALIGNMENT;
-  if (shape->tokens_per_rank == 0) return MOE_OK;   // empty batch
   CombineParams p;
   p.expert_y = static_cast<const uint16_t *>(expert_y);
   p.topk_idx = topk_idx;

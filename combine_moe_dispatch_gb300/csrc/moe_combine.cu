@@ -12,7 +12,9 @@
 // the token's K (expert, slot, weight) and broadcast them by shuffle.  For a
 // group of KG experts the warp issues all KG x U 16-byte loads before the
 // first multiply-add, so each lane keeps KG*U*16 bytes of reads in flight
-// (256 B per lane, 8 KB per warp); only populated rows are read.  The
+// (256 B per lane, 8 KB per warp, 16 warps per SM for K = 8; measured
+// faster than 128 B per lane at 32 warps per SM); only populated rows are
+// read.  The
 // accumulators stay in registers and the bf16 result is stored once, 16
 // bytes per lane.
 #include <cuda_bf16.h>
@@ -39,10 +41,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return l | (h << 16);
 }
 
-template <int KG, int U>
-__global__ void __launch_bounds__(kCombineThreads)
+// Loads in flight per lane are KG * U * 16 bytes; MINB resident blocks per SM
+// set the register budget (64 registers at 4, 85 at 3, 128 at 2).
+template <int KG, int U, int MINB>
+__global__ void __launch_bounds__(kCombineThreads, MINB)
 combine_kernel(CombineParams p) {
   __shared__ int32_t s_status;
+  pdl_wait_for_previous();
   if (threadIdx.x == 0) s_status = read_status(p.hdr);
   __syncthreads();
   if (s_status != MOE_OK) return;
@@ -121,36 +126,25 @@ combine_kernel(CombineParams p) {
   }
 }
 
-namespace {
-int combine_occ[3][64];
+#ifndef MOE_COMBINE_U8
+#define MOE_COMBINE_U8 2   // chunks per lane for K > 4: 16 loads (256 B) in flight per lane
+#endif
 
-template <int KG, int U>
-cudaError_t launch_variant(const CombineParams &p, cudaStream_t stream, int which) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  int per_sm = combine_occ[which][dev];
-  if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<KG, U>,
-                                                      kCombineThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-    combine_occ[which][dev] = per_sm;
-  }
+namespace {
+template <int KG, int U, int MINB>
+cudaError_t launch_variant(const CombineParams &p, cudaStream_t stream) {
   const int cpr = p.H / 8;
   const int64_t tasks = (int64_t)p.N * ((cpr + 32 * U - 1) / (32 * U));
-  const int64_t want = (tasks + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
-  const int64_t cap = (int64_t)device_sm_count() * per_sm;
-  const int grid = (int)(want < cap ? (want < 1 ? 1 : want) : cap);
-  combine_kernel<KG, U><<<grid, kCombineThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const int grid =
+      persistent_grid((const void *)combine_kernel<KG, U, MINB>, kCombineThreads, tasks);
+  return launch_after_previous(combine_kernel<KG, U, MINB>, grid, kCombineThreads, p, stream);
 }
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
-  if (p.K <= 2) return launch_variant<2, 8>(p, stream, 0);
-  if (p.K <= 4) return launch_variant<4, 4>(p, stream, 1);
-  return launch_variant<8, 2>(p, stream, 2);
+  if (p.K <= 2) return launch_variant<2, 4, 2>(p, stream);
+  if (p.K <= 4) return launch_variant<4, 2, 3>(p, stream);
+  return launch_variant<8, MOE_COMBINE_U8, (MOE_COMBINE_U8 == 1 ? 4 : 2)>(p, stream);
 }
 
 }  // namespace moe

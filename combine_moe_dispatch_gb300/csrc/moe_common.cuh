@@ -99,7 +99,17 @@ struct PlanParams {
   int32_t *incl;
   int R, T, E, K, cap;
   int tile_tokens, tiles_per_rank, num_tiles;
+  // single-cluster path (filled by launch_plan): one warp per chunk of whole
+  // tokens inside one rank
+  int chunk_tokens, chunks_per_rank, num_chunks, batches;
 };
+
+// Single-cluster plan limits: up to 16 CTAs of 16 warps, one chunk of at
+// most 32 * kClusterMaxBatches entries per warp.
+constexpr int kClusterMaxCtas = 16;
+constexpr int kClusterWarps = 16;
+constexpr int kClusterMaxBatches = 8;
+constexpr int kClusterMaxExperts = 1024;
 
 struct DispatchParams {
   const uint16_t *x;
@@ -132,6 +142,36 @@ cudaError_t launch_set_debug(WsHeader *hdr, uint32_t flags, uint64_t timeout_ns,
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Resident blocks per SM of `kern` at `threads` threads and `smem` bytes of
+// dynamic shared memory on the current device (cached per kernel and device).
+int occupancy_blocks(const void *kern, int threads, size_t smem);
+
+// Persistent grid for `tasks` warp tasks: enough blocks of `threads` for one
+// task per warp, at most SMs x resident blocks per SM.
+int persistent_grid(const void *kern, int threads, int64_t warp_tasks);
+
+// Launch `kern(params)` allowing a programmatic dependency on the previous
+// kernel in `stream` (see pdl_wait_for_previous).
+template <typename Params>
+cudaError_t launch_after_previous(void (*kern)(Params), int grid, int threads,
+                                  const Params &params, cudaStream_t stream) {
+#ifndef MOE_PDL
+#define MOE_PDL 1
+#endif
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, params);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 // Device helpers.
 // ---------------------------------------------------------------------------
@@ -162,6 +202,56 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *flag, uint32_t want, u
     __nanosleep(32);
   }
   return false;
+}
+
+__device__ __forceinline__ uint32_t cluster_cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Split cluster barrier without memory ordering: arrive early, wait later
+// (used to know that every CTA of the cluster has started).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// All threads of all CTAs of the cluster: writes before are visible after.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store an int to the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ void st_dsmem(int32_t *local, uint32_t rank, int32_t v) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(local), ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
+}
+
+// Load an int from the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ int ld_dsmem(const int32_t *local, uint32_t rank) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(local), ra;
+  int v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+// Programmatic dependent launch.  moe_plan's kernels allow the next kernel in
+// the stream to be scheduled as soon as all their blocks have started; the
+// dispatch and combine kernels do work that needs nothing from the plan
+// (loading and quantising x) and then wait here until the previous kernel
+// has completed and its writes are visible.  Without a programmatic
+// dependency the wait returns at once.
+__device__ __forceinline__ void pdl_allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_for_previous() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // The status the dispatch and combine kernels see; read once per block.

@@ -10,14 +10,25 @@
 //          the bytes and the H/128 scales go to every (e, s) of the token.
 //
 // How: work is cut by token, never by expert, so a skewed routing costs the
-// same as a uniform one.  A warp takes one (token, 2048-element segment)
-// task at a time from a grid sized to fill every SM: its lanes read the
-// segment once with 16-byte loads (all loads issued before any store), then
-// write it K times with coalesced 16-byte (bf16) or 8-byte (fp8) stores.  In
-// the fp8 path each half-warp owns one 128-element block: the absmax is a
-// 4-step butterfly over 16 lanes, and the block's scale is computed once and
-// shared by all K copies.  The 16 scales of a segment are gathered into
-// lanes 0..15 and stored as one 64-byte run per destination row.
+// same as a uniform one.  The kernel may start while moe_plan is still
+// running (programmatic dependent launch): each warp loads (and, for fp8,
+// quantises) its first task, and only then waits for the plan's slots.  A warp takes one (token, segment) task at a time
+// from a grid sized to fill every SM; segments are chosen to divide the row
+// evenly (1024 elements for H = 7168 or 4096), so all tasks are equal.  Its
+// lanes read the segment once with 16-byte loads (all loads issued before
+// any store), then write it K times with coalesced 16-byte (bf16) or 8-byte
+// (fp8) stores.  In the fp8 path each half-warp owns one 128-element block:
+// the absmax is a 4-step butterfly over 16 lanes, and the block's scale is
+// computed once and shared by all K copies; the segment's scales are
+// gathered into the first lanes and stored as one run per destination row.
+//
+// Exact division, cheaply: q must be e4m3(RN(x / scale)).  With r =
+// RN(1/scale), q~ = RN(x * r) is within 3 binary32 ulps of RN(x / scale)
+// (two roundings of 2^-24 each, plus half an ulp).  Rounding to E4M3 is
+// monotone, so if q~ moved 4 ulps down and 4 ulps up rounds to the same
+// byte, that byte is e4m3(RN(x / scale)); otherwise (a quotient next to an
+// E4M3 midpoint, or a zero) the lane divides with IEEE __fdiv_rn.  The
+// result is bit-identical to dividing every element.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -26,71 +37,109 @@
 namespace moe {
 
 constexpr int kDispatchThreads = 256;
-constexpr int kBf16ChunksPerLane = 8;   // 8 x 16 B per lane: a 2048-element segment
-constexpr int kFp8PairsPerTask = 8;     // 8 x 256 elements: 16 blocks of 128
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
   return __ldcs(reinterpret_cast<const uint4 *>(p));
 }
 
-// Routing of token g held by lanes 0..K-1; returns the mask of valid k and
-// reports out-of-range entries once per token.
-__device__ __forceinline__ unsigned load_routes(const DispatchParams &p, int64_t g, int lane,
-                                                bool report, int &e_l, int &s_l) {
-  e_l = -1;
-  s_l = -1;
+// Routing of one token: lane k < K holds (expert, slot) of entry (g, k).
+struct Routes {
+  int e, s;
+};
+
+__device__ __forceinline__ Routes load_routes(const DispatchParams &p, int64_t g, int lane) {
+  Routes r{-1, -1};
   if (lane < p.K) {
-    e_l = __ldg(p.topk_idx + g * p.K + lane);
-    s_l = __ldg(p.slot_of + g * p.K + lane);
+    r.e = __ldg(p.topk_idx + g * p.K + lane);
+    r.s = __ldg(p.slot_of + g * p.K + lane);
   }
-  const bool e_ok = e_l >= 0 && e_l < p.E;
-  const bool ok = lane < p.K && e_ok && s_l >= 0 && s_l < p.cap;
+  return r;
+}
+
+// Mask of the valid k; out-of-range entries are reported once per token.
+__device__ __forceinline__ unsigned check_routes(const DispatchParams &p, const Routes &r, int lane,
+                                                 bool report) {
+  const bool e_ok = r.e >= 0 && r.e < p.E;
+  const bool ok = lane < p.K && e_ok && r.s >= 0 && r.s < p.cap;
   if (report && lane < p.K && !ok)
     report_status(p.hdr, e_ok ? MOE_ERR_CAPACITY : MOE_ERR_BAD_EXPERT);
   return __ballot_sync(kFull, ok);
 }
 
+// Block-wide: wait for the plan (programmatic dependency), then read the
+// status word it left; false if the block must write nothing.
+__device__ __forceinline__ bool wait_plan_ok(const WsHeader *hdr) {
+  __shared__ int32_t s_status;
+  pdl_wait_for_previous();
+  if (threadIdx.x == 0) s_status = read_status(hdr);
+  __syncthreads();
+  return s_status == MOE_OK;
+}
+
+// bf16 copy; U 16-byte chunks per lane per task (a 256*U-element segment).
+template <int U>
+struct Bf16Task {
+  int64_t g;
+  int seg;
+  uint4 v[U];
+};
+
+template <int U>
+__device__ __forceinline__ void bf16_load(const DispatchParams &p, int64_t task, int tpr, int lane,
+                                          Bf16Task<U> &t) {
+  const int cpr = p.H / 8;
+  t.g = task / tpr;
+  t.seg = (int)(task - t.g * tpr);
+  const uint16_t *src = p.x + t.g * p.H;
+  const int c0 = t.seg * 32 * U + lane;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int c = c0 + u * 32;
+    t.v[u] = c < cpr ? ld_stream16(src + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <int U>
+__device__ __forceinline__ void bf16_store(const DispatchParams &p, int lane, const Bf16Task<U> &t,
+                                           const Routes &r) {
+  const int cpr = p.H / 8;
+  const unsigned okmask = check_routes(p, r, lane, t.seg == 0);
+  const int c0 = t.seg * 32 * U + lane;
+  for (int k = 0; k < p.K; ++k) {
+    const int e = __shfl_sync(kFull, r.e, k);
+    const int s = __shfl_sync(kFull, r.s, k);
+    if (!((okmask >> k) & 1u)) continue;
+    uint16_t *dst = static_cast<uint16_t *>(p.expert_x) + ((int64_t)e * p.cap + s) * p.H;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u * 32;
+      if (c < cpr) *reinterpret_cast<uint4 *>(dst + (int64_t)c * 8) = t.v[u];
+    }
+  }
+}
+
+template <int U>
 __global__ void __launch_bounds__(kDispatchThreads)
 dispatch_bf16_kernel(DispatchParams p) {
-  __shared__ int32_t s_status;
-  if (threadIdx.x == 0) s_status = read_status(p.hdr);
-  __syncthreads();
-  if (s_status != MOE_OK) return;
-
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * kDispatchThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kDispatchThreads) >> 5;
   const int cpr = p.H / 8;                               // 16-byte chunks per row
-  constexpr int cpt = 32 * kBf16ChunksPerLane;           // chunks per task
-  const int tpr = (cpr + cpt - 1) / cpt;                 // tasks per row
+  const int tpr = (cpr + 32 * U - 1) / (32 * U);         // tasks per row
   const int64_t ntasks = (int64_t)p.N * tpr;
 
-  for (int64_t task = warp0; task < ntasks; task += nwarps) {
-    const int64_t g = task / tpr;
-    const int seg = (int)(task - g * tpr);
-    int e_l, s_l;
-    const unsigned okmask = load_routes(p, g, lane, seg == 0, e_l, s_l);
-
-    const uint16_t *src = p.x + g * p.H;
-    const int c0 = seg * cpt + lane;
-    uint4 v[kBf16ChunksPerLane];
-#pragma unroll
-    for (int u = 0; u < kBf16ChunksPerLane; ++u) {
-      const int c = c0 + u * 32;
-      v[u] = c < cpr ? ld_stream16(src + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
-    }
-    for (int k = 0; k < p.K; ++k) {
-      const int e = __shfl_sync(kFull, e_l, k);
-      const int s = __shfl_sync(kFull, s_l, k);
-      if (!((okmask >> k) & 1u)) continue;
-      uint16_t *dst = static_cast<uint16_t *>(p.expert_x) + ((int64_t)e * p.cap + s) * p.H;
-#pragma unroll
-      for (int u = 0; u < kBf16ChunksPerLane; ++u) {
-        const int c = c0 + u * 32;
-        if (c < cpr) *reinterpret_cast<uint4 *>(dst + (int64_t)c * 8) = v[u];
-      }
-    }
+  // The first task's read of x needs nothing from the plan: issue it before
+  // waiting for the plan to finish.
+  Bf16Task<U> t;
+  const bool have = warp0 < ntasks;
+  if (have) bf16_load<U>(p, warp0, tpr, lane, t);
+  if (!wait_plan_ok(p.hdr)) return;
+  if (have) bf16_store<U>(p, lane, t, load_routes(p, t.g, lane));
+  for (int64_t task = warp0 + nwarps; task < ntasks; task += nwarps) {
+    const Routes r = load_routes(p, task / tpr, lane);    // in flight with the row loads
+    bf16_load<U>(p, task, tpr, lane, t);
+    bf16_store<U>(p, lane, t, r);
   }
 }
 
@@ -102,125 +151,172 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-__global__ void __launch_bounds__(kDispatchThreads)
-dispatch_fp8_kernel(DispatchParams p) {
-  __shared__ int32_t s_status;
-  if (threadIdx.x == 0) s_status = read_status(p.hdr);
-  __syncthreads();
-  if (s_status != MOE_OK) return;
+__device__ __forceinline__ float nudge(float q, int ulps) {
+  return __int_as_float(__float_as_int(q) + ulps);
+}
 
-  const int lane = threadIdx.x & 31;
+// e4m3(RN(a / s)), e4m3(RN(b / s)) given r = RN(1 / s) finite (see the file
+// comment for why the fast path is exact).
+__device__ __forceinline__ uint32_t quant_pair(float a, float b, float s, float r) {
+  const float qa = __fmul_rn(a, r), qb = __fmul_rn(b, r);
+  const uint32_t lo = e4m3x2(nudge(qa, -4), nudge(qb, -4));
+  const uint32_t hi = e4m3x2(nudge(qa, 4), nudge(qb, 4));
+  if (lo == hi) return lo;
+  return e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+}
+
+// fp8 quantisation; P pairs of 128-element blocks per task.
+template <int P>
+struct Fp8Task {
+  int64_t g;
+  int seg;
+  uint2 q[P];
+  float my_scale;   // lane L < 2P holds the scale of block seg*2P + L
+};
+
+// Load and quantise one task (needs nothing from the plan).
+template <int P>
+__device__ __forceinline__ void fp8_quantise(const DispatchParams &p, int64_t task, int tpr,
+                                             int lane, Fp8Task<P> &t) {
   const int half = lane >> 4;     // which block of the 256-element pair
   const int sub = lane & 15;      // 8 elements (16 bytes in, 8 bytes out) per lane
-  const int64_t warp0 = ((int64_t)blockIdx.x * kDispatchThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * kDispatchThreads) >> 5;
-  const int nb = p.H / 128;                                  // blocks per row
-  constexpr int bpt = 2 * kFp8PairsPerTask;                  // blocks per task (16)
-  const int tpr = (nb + bpt - 1) / bpt;
-  const int64_t ntasks = (int64_t)p.N * tpr;
-
-  for (int64_t task = warp0; task < ntasks; task += nwarps) {
-    const int64_t g = task / tpr;
-    const int seg = (int)(task - g * tpr);
-    int e_l, s_l;
-    const unsigned okmask = load_routes(p, g, lane, seg == 0, e_l, s_l);
-
-    const uint16_t *src = p.x + g * p.H;
-    uint4 v[kFp8PairsPerTask];
+  const int nb = p.H / 128;
+  constexpr int bpt = 2 * P;
+  t.g = task / tpr;
+  t.seg = (int)(task - t.g * tpr);
+  const uint16_t *src = p.x + t.g * p.H;
+  uint4 v[P];
 #pragma unroll
-    for (int it = 0; it < kFp8PairsPerTask; ++it) {
-      const int blk = seg * bpt + it * 2 + half;
-      v[it] = blk < nb ? ld_stream16(src + (int64_t)blk * 128 + sub * 8) : make_uint4(0, 0, 0, 0);
+  for (int it = 0; it < P; ++it) {
+    const int blk = t.seg * bpt + it * 2 + half;
+    v[it] = blk < nb ? ld_stream16(src + (int64_t)blk * 128 + sub * 8) : make_uint4(0, 0, 0, 0);
+  }
+  t.my_scale = 0.0f;
+#pragma unroll
+  for (int it = 0; it < P; ++it) {
+    const uint32_t w[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = bf16_lo(w[i]);
+      f[2 * i + 1] = bf16_hi(w[i]);
     }
-
-    uint2 q[kFp8PairsPerTask];
-    float my_scale = 0.0f;   // lane L < 16 ends up with the scale of block seg*16 + L
+    float amax = 0.0f;
 #pragma unroll
-    for (int it = 0; it < kFp8PairsPerTask; ++it) {
-      const uint32_t w[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
-      float f[8];
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        f[2 * i] = bf16_lo(w[i]);
-        f[2 * i + 1] = bf16_hi(w[i]);
-      }
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-      for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
-      const float scale = __fdiv_rn(amax, 448.0f);
-      uint32_t lo = 0, hi = 0;
-      if (amax != 0.0f) {
+    for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+    const float scale = __fdiv_rn(amax, 448.0f);
+    uint32_t lo = 0, hi = 0;
+    if (amax != 0.0f) {
+      const float r = __frcp_rn(scale);
+      if (r <= 3.0e38f) {   // finite reciprocal: fast exact path
+        lo = quant_pair(f[0], f[1], scale, r) | (quant_pair(f[2], f[3], scale, r) << 16);
+        hi = quant_pair(f[4], f[5], scale, r) | (quant_pair(f[6], f[7], scale, r) << 16);
+      } else {
         lo = e4m3x2(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale)) |
              (e4m3x2(__fdiv_rn(f[2], scale), __fdiv_rn(f[3], scale)) << 16);
         hi = e4m3x2(__fdiv_rn(f[4], scale), __fdiv_rn(f[5], scale)) |
              (e4m3x2(__fdiv_rn(f[6], scale), __fdiv_rn(f[7], scale)) << 16);
       }
-      q[it] = make_uint2(lo, hi);
-      const float s_even = __shfl_sync(kFull, scale, 0);
-      const float s_odd = __shfl_sync(kFull, scale, 16);
-      if (lane == it * 2) my_scale = s_even;
-      if (lane == it * 2 + 1) my_scale = s_odd;
     }
+    t.q[it] = make_uint2(lo, hi);
+    const float s_even = __shfl_sync(kFull, scale, 0);
+    const float s_odd = __shfl_sync(kFull, scale, 16);
+    if (lane == it * 2) t.my_scale = s_even;
+    if (lane == it * 2 + 1) t.my_scale = s_odd;
+  }
+}
 
-    const int nscale = min(bpt, nb - seg * bpt);
-    for (int k = 0; k < p.K; ++k) {
-      const int e = __shfl_sync(kFull, e_l, k);
-      const int s = __shfl_sync(kFull, s_l, k);
-      if (!((okmask >> k) & 1u)) continue;
-      const int64_t row = (int64_t)e * p.cap + s;
-      uint8_t *dst = static_cast<uint8_t *>(p.expert_x) + row * p.H;
+// Write one quantised task to every (expert, slot) of its token.
+template <int P>
+__device__ __forceinline__ void fp8_store(const DispatchParams &p, int lane, const Fp8Task<P> &t,
+                                          const Routes &r) {
+  const int half = lane >> 4;
+  const int sub = lane & 15;
+  const int nb = p.H / 128;
+  constexpr int bpt = 2 * P;
+  const unsigned okmask = check_routes(p, r, lane, t.seg == 0);
+  const int nscale = min(bpt, nb - t.seg * bpt);
+  for (int k = 0; k < p.K; ++k) {
+    const int e = __shfl_sync(kFull, r.e, k);
+    const int s = __shfl_sync(kFull, r.s, k);
+    if (!((okmask >> k) & 1u)) continue;
+    const int64_t row = (int64_t)e * p.cap + s;
+    uint8_t *dst = static_cast<uint8_t *>(p.expert_x) + row * p.H;
 #pragma unroll
-      for (int it = 0; it < kFp8PairsPerTask; ++it) {
-        const int blk = seg * bpt + it * 2 + half;
-        if (blk < nb) *reinterpret_cast<uint2 *>(dst + (int64_t)blk * 128 + sub * 8) = q[it];
-      }
-      if (lane < nscale) p.expert_x_scale[row * nb + seg * bpt + lane] = my_scale;
+    for (int it = 0; it < P; ++it) {
+      const int blk = t.seg * bpt + it * 2 + half;
+      if (blk < nb) *reinterpret_cast<uint2 *>(dst + (int64_t)blk * 128 + sub * 8) = t.q[it];
     }
+    if (lane < nscale) p.expert_x_scale[row * nb + t.seg * bpt + lane] = t.my_scale;
+  }
+}
+
+template <int P>
+__global__ void __launch_bounds__(kDispatchThreads)
+dispatch_fp8_kernel(DispatchParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * kDispatchThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kDispatchThreads) >> 5;
+  const int nb = p.H / 128;                                  // blocks per row
+  const int tpr = (nb + 2 * P - 1) / (2 * P);
+  const int64_t ntasks = (int64_t)p.N * tpr;
+
+  // Loading and quantising the first task needs nothing from the plan: do it
+  // before waiting for the plan to finish.
+  Fp8Task<P> t;
+  const bool have = warp0 < ntasks;
+  if (have) fp8_quantise<P>(p, warp0, tpr, lane, t);
+  if (!wait_plan_ok(p.hdr)) return;
+  if (have) fp8_store<P>(p, lane, t, load_routes(p, t.g, lane));
+  for (int64_t task = warp0 + nwarps; task < ntasks; task += nwarps) {
+    const Routes r = load_routes(p, task / tpr, lane);    // in flight during the quantisation
+    fp8_quantise<P>(p, task, tpr, lane, t);
+    fp8_store<P>(p, lane, t, r);
   }
 }
 
 namespace {
-int occupancy_cache[2][64];
 
-template <typename Kern>
-int blocks_per_sm(Kern kern, int which) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  int v = occupancy_cache[which][dev];
-  if (v == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kDispatchThreads, 0) != cudaSuccess ||
-        v < 1)
-      v = 1;
-    occupancy_cache[which][dev] = v;
-  }
-  return v;
+// One persistent-grid launch of `kern` over `warp_tasks` equal tasks, allowed
+// to start while the plan that precedes it in the stream is still running.
+cudaError_t launch_tasks(void (*kern)(DispatchParams), int64_t warp_tasks, const DispatchParams &p,
+                         cudaStream_t stream) {
+  const int grid = persistent_grid((const void *)kern, kDispatchThreads, warp_tasks);
+  return launch_after_previous(kern, grid, kDispatchThreads, p, stream);
 }
 
-int grid_for(int64_t warp_tasks, int per_sm) {
-  const int64_t want = (warp_tasks + (kDispatchThreads / 32) - 1) / (kDispatchThreads / 32);
-  const int64_t cap = (int64_t)device_sm_count() * per_sm;
-  int64_t g = want < cap ? want : cap;
-  return (int)(g < 1 ? 1 : g);
+// Segment size: the largest of 4, 2, 1 units that divides the row evenly
+// (4 when nothing does; the last task of a row is then partial).
+int pick_units(int units_per_row) {
+  for (int u : {4, 2, 1})
+    if (units_per_row % u == 0) return u;
+  return 4;
 }
+
 }  // namespace
 
 cudaError_t launch_dispatch_bf16(const DispatchParams &p, cudaStream_t stream) {
   const int cpr = p.H / 8;
-  const int64_t tasks = (int64_t)p.N * ((cpr + 32 * kBf16ChunksPerLane - 1) / (32 * kBf16ChunksPerLane));
-  const int grid = grid_for(tasks, blocks_per_sm(dispatch_bf16_kernel, 0));
-  dispatch_bf16_kernel<<<grid, kDispatchThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const int U = (cpr % 32 == 0) ? pick_units(cpr / 32) : 4;
+  const int64_t tasks = (int64_t)p.N * ((cpr + 32 * U - 1) / (32 * U));
+  switch (U) {
+    case 1: return launch_tasks(dispatch_bf16_kernel<1>, tasks, p, stream);
+    case 2: return launch_tasks(dispatch_bf16_kernel<2>, tasks, p, stream);
+    default: return launch_tasks(dispatch_bf16_kernel<4>, tasks, p, stream);
+  }
 }
 
 cudaError_t launch_dispatch_fp8(const DispatchParams &p, cudaStream_t stream) {
   const int nb = p.H / 128;
-  const int64_t tasks = (int64_t)p.N * ((nb + 2 * kFp8PairsPerTask - 1) / (2 * kFp8PairsPerTask));
-  const int grid = grid_for(tasks, blocks_per_sm(dispatch_fp8_kernel, 1));
-  dispatch_fp8_kernel<<<grid, kDispatchThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const int P = (nb % 2 == 0) ? pick_units(nb / 2) : 4;
+  const int64_t tasks = (int64_t)p.N * ((nb + 2 * P - 1) / (2 * P));
+  switch (P) {
+    case 1: return launch_tasks(dispatch_fp8_kernel<1>, tasks, p, stream);
+    case 2: return launch_tasks(dispatch_fp8_kernel<2>, tasks, p, stream);
+    default: return launch_tasks(dispatch_fp8_kernel<4>, tasks, p, stream);
+  }
 }
 
 }  // namespace moe

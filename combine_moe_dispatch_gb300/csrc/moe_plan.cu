@@ -46,6 +46,7 @@ plan_kernel(PlanParams p) {
   const int warp = tid >> 5;
   const int lane = tid & 31;
   WsHeader *hdr = p.hdr;
+  pdl_allow_dependents();
 
   if (tid == 0) {
     s_tile = atomicAdd(&hdr->ticket, 1u);
@@ -182,12 +183,299 @@ plan_kernel(PlanParams p) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Single-cluster plan.  When every rank-aligned chunk fits one warp and all
+// chunks fit 16 CTAs of 16 warps, the whole plan runs in one thread-block
+// cluster and the cross-tile step goes through distributed shared memory:
+//   1. warp w of CTA c ranks chunk 16c + w stably: for each 32-entry batch,
+//      the lanes holding the same expert are found with one ballot per bit
+//      of the expert id, on top of a warp-private per-expert counter;
+//   2. an exclusive scan over the CTA's 16 warps gives each warp's base in
+//      the CTA and the CTA histogram h_c;
+//   3. every CTA stores h_c (and its error bits) into row c of every peer's
+//      shared table (after a split cluster barrier, arrived at entry, shows
+//      that every peer has started), then one cluster barrier makes the table
+//      complete in every CTA: base_c = sum of rows < c, totals = sum of all
+//      rows, read locally.  No CTA reads a peer's memory, so none has to
+//      outlive that barrier for the others;
+//   4. slot = base_c + warp base + rank in warp.  Chunk j = 0 of rank r
+//      writes offsets[.][r]; the last CTA writes the counts, offsets[.][R]
+//      and the status word.
+// The barrier is the hardware cluster barrier over co-scheduled CTAs; the
+// kernel has no flags, counters or spin-waits in global memory.
+// ---------------------------------------------------------------------------
+
+// Lanes of this warp whose key equals this lane's key (keys < 2^bits, or -1
+// for "no key", which matches only other -1 lanes).  Every lane executes
+// every ballot (no lane leaves early), as the full-warp ballots require.
+__device__ __forceinline__ unsigned peers_with_same_key(int key, int bits) {
+  const unsigned none = __ballot_sync(0xFFFFFFFFu, key < 0);
+  unsigned m = ~none;
+  for (int b = 0; b < bits; ++b) {
+    const int bit = (key >> b) & 1;
+    const unsigned set = __ballot_sync(0xFFFFFFFFu, bit);
+    m &= bit ? set : ~set;
+  }
+  return key < 0 ? none : m;
+}
+
+__global__ void __launch_bounds__(kClusterWarps * 32)
+plan_cluster_kernel(PlanParams p) {
+  extern __shared__ int32_t smem[];
+  const int E = p.E;
+  int32_t *wc = smem;                             // [16][E] warp counters -> warp bases
+  int32_t *s_tab = smem + kClusterWarps * E;      // [ncta][E] CTA histograms, row c from CTA c
+  int32_t *s_base = s_tab + kClusterMaxCtas * E;  // [E] exclusive prefix of this CTA
+  __shared__ int32_t s_err[kClusterMaxCtas];      // error bits, entry c from CTA c
+  __shared__ int32_t s_cta_err, s_final;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int nthreads = kClusterWarps * 32;
+  const uint32_t cta = cluster_cta_rank();
+  const uint32_t ncta = gridDim.x;
+  pdl_allow_dependents();
+  // Peers' shared memory may be written only once every CTA of the cluster
+  // has started: arrive now, wait just before the first remote store.
+  cluster_arrive_relaxed();
+
+  // 1. this warp's chunk; its routing loads go out before anything else
+  const int chunk = (int)cta * kClusterWarps + warp;
+  const bool has_chunk = chunk < p.num_chunks;
+  int r = 0, j = 0, n_ent = 0;
+  int64_t ent0 = 0;
+  if (has_chunk) {
+    r = chunk / p.chunks_per_rank;
+    j = chunk % p.chunks_per_rank;
+    const int64_t g0 = (int64_t)r * p.T + (int64_t)j * p.chunk_tokens;
+    n_ent = min(p.chunk_tokens, p.T - j * p.chunk_tokens) * p.K;
+    ent0 = g0 * p.K;
+  }
+  int e_in[kClusterMaxBatches];
+#pragma unroll
+  for (int b = 0; b < kClusterMaxBatches; ++b) {
+    const int pl = b * 32 + lane;
+    e_in[b] = (b < p.batches && pl < n_ent) ? __ldg(p.topk_idx + ent0 + pl) : -1;
+  }
+  for (int i = tid; i < kClusterWarps * E; i += nthreads) wc[i] = 0;
+  if (tid == 0) s_cta_err = 0;
+  int32_t my_err = 0;
+  __syncthreads();
+
+  int bits = 1;
+  while ((1 << bits) < E) ++bits;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int lrank[kClusterMaxBatches];
+  int lexp[kClusterMaxBatches];
+#pragma unroll
+  for (int b = 0; b < kClusterMaxBatches; ++b) {
+    lrank[b] = 0;
+    lexp[b] = -1;
+    if (b >= p.batches) continue;                       // warp-uniform
+    const int pl = b * 32 + lane;
+    const bool valid = pl < n_ent;
+    const int e = e_in[b];
+    const bool ok = valid && e >= 0 && e < E;
+    if (valid && !ok) my_err |= (int32_t)kErrBadExpert;
+    const unsigned same = peers_with_same_key(ok ? e : -1, bits);
+    const int before = __popc(same & lt_mask);
+    const int wbase = ok ? wc[warp * E + e] : 0;
+    __syncwarp();
+    if (ok && before == 0) wc[warp * E + e] = wbase + __popc(same);
+    __syncwarp();
+    lrank[b] = wbase + before;
+    lexp[b] = ok ? e : -1;
+  }
+  my_err = __reduce_or_sync(0xFFFFFFFFu, my_err);
+  if (lane == 0 && my_err) atomicOr(&s_cta_err, my_err);
+  __syncthreads();
+  cluster_wait();
+
+  // 2. scan over the CTA's warps (all 16 counters loaded before any store)
+  for (int e = tid; e < E; e += nthreads) {
+    int c[kClusterWarps];
+#pragma unroll
+    for (int w = 0; w < kClusterWarps; ++w) c[w] = wc[w * E + e];
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kClusterWarps; ++w) {
+      wc[w * E + e] = run;
+      run += c[w];
+    }
+    // 3a. push the CTA histogram into row `cta` of every CTA's table
+    for (uint32_t q = 0; q < ncta; ++q) st_dsmem(s_tab + (int)cta * E + e, q, run);
+  }
+  if (tid == 0)
+    for (uint32_t q = 0; q < ncta; ++q) st_dsmem(s_err + cta, q, s_cta_err);
+
+  // 3b. one cluster barrier: every table is complete and visible locally
+  cluster_barrier();
+  const bool last = cta == ncta - 1;
+  int32_t err = 0;
+  for (int e = tid; e < E; e += nthreads) {
+    int b = 0, tot = 0;
+    for (uint32_t c = 0; c < ncta; ++c) {
+      const int h = s_tab[(int)c * E + e];
+      b += (c < cta) ? h : 0;
+      tot += h;
+    }
+    s_base[e] = b;
+    if (last) {
+      p.expert_num_tokens[e] = tot;
+      p.expert_rank_offsets[(int64_t)e * (p.R + 1) + p.R] = tot;
+      if (tot > p.cap) err |= (int32_t)kErrCapacity;
+    }
+  }
+  if (last && tid < (int)ncta) err |= s_err[tid];
+  __syncthreads();
+
+  // 4. slots, return addresses, rank offsets
+#pragma unroll
+  for (int b = 0; b < kClusterMaxBatches; ++b) {
+    if (b >= p.batches) continue;
+    const int pl = b * 32 + lane;
+    if (pl >= n_ent) continue;
+    const int e = lexp[b];
+    if (e < 0) {
+      p.slot_of[ent0 + pl] = -1;
+      continue;
+    }
+    const int slot = s_base[e] + wc[warp * E + e] + lrank[b];
+    p.slot_of[ent0 + pl] = slot;
+    if (slot < p.cap) p.src_of[(int64_t)e * p.cap + slot] = (int32_t)(ent0 + pl);
+  }
+  for (int w = 0; w < kClusterWarps; ++w) {              // chunks that start a rank
+    const int c = (int)cta * kClusterWarps + w;
+    if (c >= p.num_chunks || c % p.chunks_per_rank != 0) continue;
+    const int rr = c / p.chunks_per_rank;
+    for (int e = tid; e < E; e += nthreads)
+      p.expert_rank_offsets[(int64_t)e * (p.R + 1) + rr] = s_base[e] + wc[w * E + e];
+  }
+  if (last) {
+    err = __reduce_or_sync(0xFFFFFFFFu, err);
+    if (tid == 0) s_final = 0;
+    __syncthreads();
+    if (lane == 0 && err) atomicOr(&s_final, err);
+    __syncthreads();
+    if (tid == 0)
+      p.hdr->status = (s_final & kErrBadExpert) ? MOE_ERR_BAD_EXPERT
+                      : (s_final & kErrCapacity) ? MOE_ERR_CAPACITY : MOE_OK;
+  }
+}
+
 __global__ void set_debug_kernel(WsHeader *hdr, uint32_t flags, uint64_t timeout_ns) {
   hdr->debug_flags = flags;
   hdr->timeout_ns = timeout_ns;
 }
 
-cudaError_t launch_plan(const PlanParams &p, cudaStream_t stream) {
+namespace {
+
+// Chunking for the single-cluster path: the fewest entries per warp such
+// that all rank-aligned chunks fit 8 CTAs of 16 warps (each CTA then reads
+// at most 7 peer histograms), else 16 CTAs.
+bool cluster_geometry(PlanParams &p) {
+  if (p.E > kClusterMaxExperts) return false;
+  for (int max_ctas : {kClusterMaxCtas / 2, kClusterMaxCtas})
+  for (int b = 1; b <= kClusterMaxBatches; ++b) {
+    int tw = (32 * b) / p.K;
+    if (tw < 1) continue;
+    if (tw > p.T) tw = p.T;
+    const int cpr = (p.T + tw - 1) / tw;
+    const int64_t nc = (int64_t)p.R * cpr;
+    if (nc <= (int64_t)max_ctas * kClusterWarps) {
+      p.chunk_tokens = tw;
+      p.chunks_per_rank = cpr;
+      p.num_chunks = (int)nc;
+      p.batches = (tw * p.K + 31) / 32;
+      return true;
+    }
+  }
+  return false;
+}
+
+struct ClusterFit {
+  int ctas = 0;
+  size_t smem = 0;
+  int ok = -1;   // -1 unknown, 0 no, 1 yes
+};
+ClusterFit cluster_fit_cache[64];
+
+// Can a cluster of `ctas` blocks with `smem` bytes each be scheduled?
+cudaError_t cluster_fits(int ctas, size_t smem, bool *fits) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  ClusterFit &c = cluster_fit_cache[(dev >= 0 && dev < 64) ? dev : 0];
+  if (c.ok >= 0 && c.ctas == ctas && c.smem == smem) {
+    *fits = c.ok == 1;
+    return cudaSuccess;
+  }
+  if (ctas > 8) {
+    e = cudaFuncSetAttribute(plan_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(plan_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ctas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kClusterWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, plan_cluster_kernel, &cfg);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  c.ctas = ctas;
+  c.smem = smem;
+  c.ok = n > 0 ? 1 : 0;
+  *fits = n > 0;
+  return cudaSuccess;
+}
+
+cudaError_t launch_plan_cluster(const PlanParams &p, int ctas, size_t smem, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ctas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kClusterWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_cluster_kernel, p);
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const PlanParams &p_in, cudaStream_t stream) {
+  PlanParams p = p_in;
+  if (cluster_geometry(p)) {
+    const int ctas = (p.num_chunks + kClusterWarps - 1) / kClusterWarps;
+    const size_t csmem = (size_t)(kClusterWarps + kClusterMaxCtas + 1) * p.E * sizeof(int32_t);
+    bool fits = false;
+    cudaError_t e = cluster_fits(ctas, csmem, &fits);
+    if (e != cudaSuccess) return e;
+    if (fits) {
+      e = launch_plan_cluster(p, ctas, csmem, stream);
+      if (e != cudaSuccess) return e;
+      return cudaGetLastError();
+    }
+  }
   const size_t smem = (size_t)(kPlanWarps + 2) * p.E * sizeof(int32_t);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -3,9 +3,9 @@ allowed to run out; nothing here faults, traps or hangs the GPU.
 
 * expert ids out of range -> BAD_EXPERT, dispatch and combine write nothing;
 * more rows than the capacity -> CAPACITY with exact counts/offsets/slots;
-* the test hook withholds one tile's counts, so the other tiles' bounded
-  waits give up after 50 ms and the plan reports TIMEOUT; the next plan on
-  the same workspace is correct again;
+* the test hook withholds one tile's counts in the multi-tile plan, so the
+  other tiles' bounded waits give up after 50 ms and the plan reports
+  TIMEOUT; the next plan on the same workspace is correct again;
 * misaligned arguments are rejected before anything is enqueued;
 * plan + dispatch + combine captured in a CUDA graph and replayed."""
 import numpy as np
@@ -56,7 +56,9 @@ def test_capacity_overflow():
 
 
 def test_timeout_hook_and_recovery():
-    R, T, H, E, K = 4, 256, 128, 32, 8      # 8 plan tiles
+    # 20000 tokens x 8 experts is beyond one cluster, so the plan runs as 157
+    # tiles that wait on each other (the hook only affects those waits)
+    R, T, H, E, K = 1, 20000, 128, 32, 8
     idx, x, w = _case(3, R, T, H, E, K)
     shape = moe.make_shape(R, T, H, E, K, R * T)
     buf = moe.Buffers(shape, expert_y=False)

@@ -54,6 +54,51 @@ def test_small_shapes(name, R, T, H, E, K, payloads):
     assert res["not_bit_exact"] == 0, f"expected bit-exact combine, {res}"
 
 
+def _fp8_edge_rows(H=256):
+    """Rows that stress the e4m3 rounding: the hand-worked fixture rows, rows
+    whose quotients x/scale are exact E4M3 midpoints (scale a power of two),
+    one bf16 step either side of a midpoint, and scales so small that the
+    reciprocal overflows."""
+    import oracle_pins
+    rows = []
+    for name in ("fp8_block.txt", "fp8_division.txt"):
+        g = oracle_pins.read_kv(name)[0]
+        r = np.zeros(H, np.uint16)
+        v = [int(t, 0) for t in g["x"].split()]
+        for i, b in zip(v[0::2], v[1::2]):
+            r[i] = b
+        rows.append(r)
+    tab = oracle_pins.e4m3_table()[:0x7F]
+    mids = ((tab[:-1] + tab[1:]) / 2).astype(np.float64)
+    rng = np.random.default_rng(17)
+    for k in (-20, -3, 0, 5, 30):
+        s = 2.0 ** k
+        for sign in (1.0, -1.0):
+            m = rng.choice(mids, H)
+            vals = sign * m * s
+            vals[::128] = 448.0 * s                           # every block: scale = 2^k
+            rows.append(inputs.to_bf16_bits(vals.astype(np.float32)))
+            b = inputs.to_bf16_bits(vals.astype(np.float32)).astype(np.int32)
+            step = rng.choice([-1, 1], H)
+            step[::128] = 0
+            rows.append((b + step).astype(np.uint16))          # one bf16 ulp off the midpoint
+    for amax in (2.0 ** -130, 3.0 * 2.0 ** -128, 1e-38):      # reciprocal of the scale overflows
+        vals = rng.standard_normal(H) * amax / 4
+        vals[0] = amax
+        rows.append(inputs.to_bf16_bits(vals.astype(np.float32)))
+    return np.stack(rows)
+
+
+def test_fp8_rounding_edge_rows():
+    x = _fp8_edge_rows()
+    N = x.shape[0]
+    R, T, H, E, K = 1, N, x.shape[1], 5, 2
+    rng = np.random.default_rng(3)
+    idx = np.argsort(rng.random((N, E)), axis=1)[:, :K].astype(np.int32)
+    w = inputs.weights(N, K, 3)
+    gpu_check.run_case(R, T, H, E, K, N, idx, x, w, ("fp8",))
+
+
 def test_duplicate_experts_per_token():
     idx, x, w = _rand_case(5, 2, 64, 256, 4, 4, distinct=False)
     gpu_check.run_case(2, 64, 256, 4, 4, 2 * 64 * 4, idx, x, w, ("bf16", "fp8"))
@@ -88,6 +133,27 @@ def test_repeated_calls_reuse_workspace():
         st, cnt, off, slot, src = oracle.plan(R, T, E, K, R * T, idx)
         assert np.array_equal(buf.slot_of.cpu().numpy(), slot)
         assert np.array_equal(buf.expert_rank_offsets.cpu().numpy(), off)
+
+
+def test_both_plan_paths_share_one_workspace():
+    """The single-cluster plan (small shapes) and the multi-tile plan (here
+    20000 tokens, beyond one cluster) alternate on one workspace."""
+    import combine_moe_dispatch_gb300 as moe
+    import oracle
+    shapes = [(4, 300, 32, 4), (1, 20000, 32, 8), (8, 128, 256, 8), (1, 20000, 32, 8)]
+    ws = torch.zeros(max(moe.workspace_size(moe.make_shape(R, T, 256, E, K, R * T))
+                         for R, T, E, K in shapes), dtype=torch.uint8, device="cuda")
+    for i, (R, T, E, K) in enumerate(shapes):
+        shape = moe.make_shape(R, T, 256, E, K, R * T)
+        idx, _, _ = _rand_case(50 + i, R, T, 8, E, K)
+        b = moe.Buffers(shape, expert_x=False, expert_y=False)
+        moe.plan(shape, gpu_check.dev(idx), b.expert_num_tokens, b.expert_rank_offsets, b.slot_of,
+                 b.src_of, ws)
+        assert moe.read_status(ws) == moe.Status.OK
+        st, cnt, off, slot, src = oracle.plan(R, T, E, K, R * T, idx)
+        assert np.array_equal(b.slot_of.cpu().numpy(), slot)
+        assert np.array_equal(b.expert_rank_offsets.cpu().numpy(), off)
+        assert np.array_equal(b.expert_num_tokens.cpu().numpy(), cnt)
 
 
 @pytest.mark.parametrize("name", ["tiny", "mixtral", "dsv3_decode", "dsv3_prefill", "kimi_decode"])
