@@ -110,6 +110,7 @@ constexpr int kClusterMaxCtas = 16;
 constexpr int kClusterWarps = 16;
 constexpr int kClusterMaxBatches = 8;
 constexpr int kClusterMaxExperts = 1024;
+constexpr size_t kClusterMaxSmem = 200 * 1024;   // dynamic shared memory per CTA, at most
 
 struct DispatchParams {
   const uint16_t *x;

@@ -198,9 +198,14 @@ plan_kernel(PlanParams p) {
 //      complete in every CTA: base_c = sum of rows < c, totals = sum of all
 //      rows, read locally.  No CTA reads a peer's memory, so none has to
 //      outlive that barrier for the others;
-//   4. slot = base_c + warp base + rank in warp.  Chunk j = 0 of rank r
-//      writes offsets[.][r]; the last CTA writes the counts, offsets[.][R]
-//      and the status word.
+//   4. slot = base_c + warp base + rank in warp.  The CTA's return addresses
+//      are staged in shared memory in (expert, slot) order and written out
+//      as contiguous runs.  Each CTA owns a block of rows (experts) of the
+//      offsets matrix: the CTA where rank r starts pushed its in-CTA prefix
+//      for rank r into the row owner's shared memory before the barrier,
+//      and each owner writes its rows and counts as one contiguous run
+//      (stores from many CTAs into the same few sectors of that small
+//      matrix serialise).  The last CTA writes the status word.
 // The barrier is the hardware cluster barrier over co-scheduled CTAs; the
 // kernel has no flags, counters or spin-waits in global memory.
 // ---------------------------------------------------------------------------
@@ -219,6 +224,42 @@ __device__ __forceinline__ unsigned peers_with_same_key(int key, int bits) {
   return key < 0 ? none : m;
 }
 
+// Exclusive scan of in[0..n) into out[0..n) by the whole block (n <= 2 *
+// blockDim.x); returns the total.  Starts and ends with __syncthreads.
+__device__ __forceinline__ int block_exclusive_scan(const int32_t *in, int32_t *out, int n) {
+  __shared__ int32_t s_warp[32];
+  __shared__ int32_t s_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __syncthreads();
+  const int a = 2 * tid < n ? in[2 * tid] : 0;
+  const int b = 2 * tid + 1 < n ? in[2 * tid + 1] : 0;
+  int incl = a + b;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, w, off);
+      if (lane >= off) w += v;
+    }
+    if (lane < nw) s_warp[lane] = w;            // inclusive over warps
+    if (lane == nw - 1) s_total = w;
+  }
+  __syncthreads();
+  const int excl = incl - a - b + (warp > 0 ? s_warp[warp - 1] : 0);
+  if (2 * tid < n) out[2 * tid] = excl;
+  if (2 * tid + 1 < n) out[2 * tid + 1] = excl + a;
+  __syncthreads();
+  return s_total;
+}
+
 __global__ void __launch_bounds__(kClusterWarps * 32)
 plan_cluster_kernel(PlanParams p) {
   extern __shared__ int32_t smem[];
@@ -226,6 +267,11 @@ plan_cluster_kernel(PlanParams p) {
   int32_t *wc = smem;                             // [16][E] warp counters -> warp bases
   int32_t *s_tab = smem + kClusterWarps * E;      // [ncta][E] CTA histograms, row c from CTA c
   int32_t *s_base = s_tab + kClusterMaxCtas * E;  // [E] exclusive prefix of this CTA
+  int32_t *s_eoff = s_base + E;                   // [E] this CTA's entries before expert e
+  int32_t *s_stage = s_eoff + E;                  // [2][16*32*8] (entry id, expert) in slot order
+  int32_t *s_offs = s_stage + 2 * kClusterWarps * 32 * kClusterMaxBatches;
+                                                  // [R][rows] rank-start prefixes of this CTA's rows
+  const int rows = (E + (int)gridDim.x - 1) / (int)gridDim.x;   // offsets rows (experts) per CTA
   __shared__ int32_t s_err[kClusterMaxCtas];      // error bits, entry c from CTA c
   __shared__ int32_t s_cta_err, s_final;
 
@@ -293,6 +339,8 @@ plan_cluster_kernel(PlanParams p) {
   cluster_wait();
 
   // 2. scan over the CTA's warps (all 16 counters loaded before any store)
+  const int first_rank_warp =
+      (p.chunks_per_rank - ((int)cta * kClusterWarps) % p.chunks_per_rank) % p.chunks_per_rank;
   for (int e = tid; e < E; e += nthreads) {
     int c[kClusterWarps];
 #pragma unroll
@@ -300,11 +348,19 @@ plan_cluster_kernel(PlanParams p) {
     int run = 0;
 #pragma unroll
     for (int w = 0; w < kClusterWarps; ++w) {
+      const int cw = c[w];
+      c[w] = run;                                  // c[] now holds the exclusive prefixes
       wc[w * E + e] = run;
-      run += c[w];
+      run += cw;
     }
-    // 3a. push the CTA histogram into row `cta` of every CTA's table
+    // 3a. push the CTA histogram into row `cta` of every CTA's table, and
+    //     the in-CTA prefix of every chunk that starts a rank to the last CTA
     for (uint32_t q = 0; q < ncta; ++q) st_dsmem(s_tab + (int)cta * E + e, q, run);
+    for (int w = first_rank_warp; w < kClusterWarps; w += p.chunks_per_rank) {
+      const int ch = (int)cta * kClusterWarps + w;
+      if (ch >= p.num_chunks) break;
+      st_dsmem(s_offs + (ch / p.chunks_per_rank) * rows + e % rows, e / rows, wc[w * E + e]);
+    }
   }
   if (tid == 0)
     for (uint32_t q = 0; q < ncta; ++q) st_dsmem(s_err + cta, q, s_cta_err);
@@ -321,16 +377,15 @@ plan_cluster_kernel(PlanParams p) {
       tot += h;
     }
     s_base[e] = b;
-    if (last) {
-      p.expert_num_tokens[e] = tot;
-      p.expert_rank_offsets[(int64_t)e * (p.R + 1) + p.R] = tot;
-      if (tot > p.cap) err |= (int32_t)kErrCapacity;
-    }
+    if (last && tot > p.cap) err |= (int32_t)kErrCapacity;
   }
   if (last && tid < (int)ncta) err |= s_err[tid];
-  __syncthreads();
+  const int n_cta = block_exclusive_scan(s_tab + (int)cta * E, s_eoff, E);
 
-  // 4. slots, return addresses, rank offsets
+  // 4. slots; return addresses staged in (expert, slot) order so that the
+  //    src_of rows go out as contiguous runs
+  int32_t *stage_v = s_stage;
+  int32_t *stage_e = s_stage + kClusterWarps * 32 * kClusterMaxBatches;
 #pragma unroll
   for (int b = 0; b < kClusterMaxBatches; ++b) {
     if (b >= p.batches) continue;
@@ -341,16 +396,41 @@ plan_cluster_kernel(PlanParams p) {
       p.slot_of[ent0 + pl] = -1;
       continue;
     }
-    const int slot = s_base[e] + wc[warp * E + e] + lrank[b];
-    p.slot_of[ent0 + pl] = slot;
-    if (slot < p.cap) p.src_of[(int64_t)e * p.cap + slot] = (int32_t)(ent0 + pl);
+    const int local = wc[warp * E + e] + lrank[b];       // rank among this CTA's entries of e
+    p.slot_of[ent0 + pl] = s_base[e] + local;
+    stage_v[s_eoff[e] + local] = (int32_t)(ent0 + pl);
+    stage_e[s_eoff[e] + local] = e;
   }
-  for (int w = 0; w < kClusterWarps; ++w) {              // chunks that start a rank
-    const int c = (int)cta * kClusterWarps + w;
-    if (c >= p.num_chunks || c % p.chunks_per_rank != 0) continue;
-    const int rr = c / p.chunks_per_rank;
-    for (int e = tid; e < E; e += nthreads)
-      p.expert_rank_offsets[(int64_t)e * (p.R + 1) + rr] = s_base[e] + wc[w * E + e];
+  __syncthreads();
+  for (int i = tid; i < n_cta; i += nthreads) {
+    const int e = stage_e[i];
+    const int slot = s_base[e] + (i - s_eoff[e]);
+    if (slot < p.cap) p.src_of[(int64_t)e * p.cap + slot] = stage_v[i];
+  }
+  // offsets[e][r] = (histograms of the CTAs before the one where rank r
+  // starts) + (in-CTA prefix pushed by that CTA).  This CTA writes rows
+  // [e0, e1) of the matrix, one contiguous run, and their counts.
+  __syncthreads();                                   // s_base / s_tab are reused below
+  {
+    const int e0 = (int)cta * rows, e1 = min(E, e0 + rows);
+    for (int e = e0 + tid; e < e1; e += nthreads) {
+      int run = 0;
+      for (uint32_t c = 0; c < ncta; ++c) {
+        const int h = s_tab[(int)c * E + e];
+        s_tab[(int)c * E + e] = run;                 // exclusive over CTAs (rows e0..e1 only)
+        run += h;
+      }
+      p.expert_num_tokens[e] = run;
+      s_base[e] = run;                               // the total (this CTA's slots are done)
+    }
+    __syncthreads();
+    const int R1 = p.R + 1;
+    for (int i = tid; i < (e1 - e0) * R1; i += nthreads) {
+      const int e = e0 + i / R1, rr = i % R1;
+      const int cr = (rr * p.chunks_per_rank) / kClusterWarps;   // CTA where rank rr starts
+      p.expert_rank_offsets[(int64_t)e0 * R1 + i] =
+          rr == p.R ? s_base[e] : s_tab[cr * E + e] + s_offs[rr * rows + (e - e0)];
+    }
   }
   if (last) {
     err = __reduce_or_sync(0xFFFFFFFFu, err);
@@ -371,12 +451,12 @@ __global__ void set_debug_kernel(WsHeader *hdr, uint32_t flags, uint64_t timeout
 
 namespace {
 
-// Chunking for the single-cluster path: the fewest entries per warp such
-// that all rank-aligned chunks fit 8 CTAs of 16 warps (each CTA then reads
-// at most 7 peer histograms), else 16 CTAs.
+// Chunking for the single-cluster path: the fewest entries per warp (so the
+// most CTAs, which share the scattered stores) such that all rank-aligned
+// chunks fit 16 CTAs of 16 warps.
 bool cluster_geometry(PlanParams &p) {
   if (p.E > kClusterMaxExperts) return false;
-  for (int max_ctas : {kClusterMaxCtas / 2, kClusterMaxCtas})
+  for (int max_ctas : {kClusterMaxCtas})
   for (int b = 1; b <= kClusterMaxBatches; ++b) {
     int tw = (32 * b) / p.K;
     if (tw < 1) continue;
@@ -466,9 +546,11 @@ cudaError_t launch_plan(const PlanParams &p_in, cudaStream_t stream) {
   PlanParams p = p_in;
   if (cluster_geometry(p)) {
     const int ctas = (p.num_chunks + kClusterWarps - 1) / kClusterWarps;
-    const size_t csmem = (size_t)(kClusterWarps + kClusterMaxCtas + 1) * p.E * sizeof(int32_t);
+    const size_t csmem = ((size_t)(kClusterWarps + kClusterMaxCtas + 2) * p.E +
+                          (size_t)p.R * ((p.E + ctas - 1) / ctas) +
+                          2 * kClusterWarps * 32 * kClusterMaxBatches) * sizeof(int32_t);
     bool fits = false;
-    cudaError_t e = cluster_fits(ctas, csmem, &fits);
+    cudaError_t e = csmem <= kClusterMaxSmem ? cluster_fits(ctas, csmem, &fits) : cudaSuccess;
     if (e != cudaSuccess) return e;
     if (fits) {
       e = launch_plan_cluster(p, ctas, csmem, stream);
