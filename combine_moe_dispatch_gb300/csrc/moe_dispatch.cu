@@ -11,8 +11,10 @@
 //
 // How: work is cut by token, never by expert, so a skewed routing costs the
 // same as a uniform one.  The kernel may start while moe_plan is still
-// running (programmatic dependent launch): each warp loads (and, for fp8,
-// quantises) its first task, and only then waits for the plan's slots.  A warp takes one (token, segment) task at a time
+// running (programmatic dependent launch): each warp loads its first task
+// and only then waits for the plan's slots.  Tasks are software-pipelined:
+// the next task's row and routing loads are in flight while this task's
+// stores are issued (and, for fp8, while it is quantised).  A warp takes one (token, segment) task at a time
 // from a grid sized to fill every SM; segments are chosen to divide the row
 // evenly (1024 elements for H = 7168 or 4096), so all tasks are equal.  Its
 // lanes read the segment once with 16-byte loads (all loads issued before
@@ -132,14 +134,25 @@ dispatch_bf16_kernel(DispatchParams p) {
   // The first task's read of x needs nothing from the plan: issue it before
   // waiting for the plan to finish.
   Bf16Task<U> t;
-  const bool have = warp0 < ntasks;
-  if (have) bf16_load<U>(p, warp0, tpr, lane, t);
+  if (warp0 < ntasks) bf16_load<U>(p, warp0, tpr, lane, t);
   if (!wait_plan_ok(p.hdr)) return;
-  if (have) bf16_store<U>(p, lane, t, load_routes(p, t.g, lane));
-  for (int64_t task = warp0 + nwarps; task < ntasks; task += nwarps) {
-    const Routes r = load_routes(p, task / tpr, lane);    // in flight with the row loads
-    bf16_load<U>(p, task, tpr, lane, t);
+  if (warp0 >= ntasks) return;
+  Routes r = load_routes(p, t.g, lane);
+  // Software pipeline: the next task's loads go out before this task's stores.
+  for (int64_t task = warp0; task < ntasks; task += nwarps) {
+    const int64_t next = task + nwarps;
+    const bool more = next < ntasks;
+    Bf16Task<U> tn;
+    Routes rn;
+    if (more) {
+      bf16_load<U>(p, next, tpr, lane, tn);
+      rn = load_routes(p, tn.g, lane);
+    }
     bf16_store<U>(p, lane, t, r);
+    if (more) {
+      t = tn;
+      r = rn;
+    }
   }
 }
 
@@ -167,34 +180,45 @@ __device__ __forceinline__ uint32_t quant_pair(float a, float b, float s, float 
 
 // fp8 quantisation; P pairs of 128-element blocks per task.
 template <int P>
-struct Fp8Task {
+struct Fp8Raw {      // one task's input, as loaded
+  int64_t g;
+  int seg;
+  uint4 v[P];
+};
+
+template <int P>
+struct Fp8Task {     // one task's output
   int64_t g;
   int seg;
   uint2 q[P];
   float my_scale;   // lane L < 2P holds the scale of block seg*2P + L
 };
 
-// Load and quantise one task (needs nothing from the plan).
 template <int P>
-__device__ __forceinline__ void fp8_quantise(const DispatchParams &p, int64_t task, int tpr,
-                                             int lane, Fp8Task<P> &t) {
-  const int half = lane >> 4;     // which block of the 256-element pair
-  const int sub = lane & 15;      // 8 elements (16 bytes in, 8 bytes out) per lane
+__device__ __forceinline__ void fp8_load(const DispatchParams &p, int64_t task, int tpr, int lane,
+                                         Fp8Raw<P> &a) {
+  const int half = lane >> 4;
+  const int sub = lane & 15;
   const int nb = p.H / 128;
-  constexpr int bpt = 2 * P;
-  t.g = task / tpr;
-  t.seg = (int)(task - t.g * tpr);
-  const uint16_t *src = p.x + t.g * p.H;
-  uint4 v[P];
+  a.g = task / tpr;
+  a.seg = (int)(task - a.g * tpr);
+  const uint16_t *src = p.x + a.g * p.H;
 #pragma unroll
   for (int it = 0; it < P; ++it) {
-    const int blk = t.seg * bpt + it * 2 + half;
-    v[it] = blk < nb ? ld_stream16(src + (int64_t)blk * 128 + sub * 8) : make_uint4(0, 0, 0, 0);
+    const int blk = a.seg * 2 * P + it * 2 + half;
+    a.v[it] = blk < nb ? ld_stream16(src + (int64_t)blk * 128 + sub * 8) : make_uint4(0, 0, 0, 0);
   }
+}
+
+// Quantise one loaded task (needs nothing from the plan).
+template <int P>
+__device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Task<P> &t) {
+  t.g = a.g;
+  t.seg = a.seg;
   t.my_scale = 0.0f;
 #pragma unroll
   for (int it = 0; it < P; ++it) {
-    const uint32_t w[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
+    const uint32_t w[4] = {a.v[it].x, a.v[it].y, a.v[it].z, a.v[it].w};
     float f[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -263,17 +287,30 @@ dispatch_fp8_kernel(DispatchParams p) {
   const int tpr = (nb + 2 * P - 1) / (2 * P);
   const int64_t ntasks = (int64_t)p.N * tpr;
 
-  // Loading and quantising the first task needs nothing from the plan: do it
-  // before waiting for the plan to finish.
-  Fp8Task<P> t;
-  const bool have = warp0 < ntasks;
-  if (have) fp8_quantise<P>(p, warp0, tpr, lane, t);
+  // The first task's read of x needs nothing from the plan: issue it before
+  // waiting for the plan to finish.  Then software-pipeline the tasks: the
+  // next task's x and routing loads are issued before this task's stores,
+  // and it is quantised while those stores drain.
+  Fp8Raw<P> a;
+  if (warp0 < ntasks) fp8_load<P>(p, warp0, tpr, lane, a);
   if (!wait_plan_ok(p.hdr)) return;
-  if (have) fp8_store<P>(p, lane, t, load_routes(p, t.g, lane));
-  for (int64_t task = warp0 + nwarps; task < ntasks; task += nwarps) {
-    const Routes r = load_routes(p, task / tpr, lane);    // in flight during the quantisation
-    fp8_quantise<P>(p, task, tpr, lane, t);
+  if (warp0 >= ntasks) return;
+  Routes r = load_routes(p, a.g, lane);
+  Fp8Task<P> t;
+  fp8_quantise<P>(a, lane, t);
+  for (int64_t task = warp0; task < ntasks; task += nwarps) {
+    const int64_t next = task + nwarps;
+    const bool more = next < ntasks;
+    Routes rn;
+    if (more) {
+      fp8_load<P>(p, next, tpr, lane, a);
+      rn = load_routes(p, next / tpr, lane);
+    }
     fp8_store<P>(p, lane, t, r);
+    if (more) {
+      fp8_quantise<P>(a, lane, t);
+      r = rn;
+    }
   }
 }
 
@@ -289,17 +326,20 @@ cudaError_t launch_tasks(void (*kern)(DispatchParams), int64_t warp_tasks, const
 
 // Segment size: the largest of 4, 2, 1 units that divides the row evenly
 // (4 when nothing does; the last task of a row is then partial).
+#ifndef MOE_MAX_UNITS
+#define MOE_MAX_UNITS 4
+#endif
 int pick_units(int units_per_row) {
   for (int u : {4, 2, 1})
-    if (units_per_row % u == 0) return u;
-  return 4;
+    if (u <= MOE_MAX_UNITS && units_per_row % u == 0) return u;
+  return MOE_MAX_UNITS;
 }
 
 }  // namespace
 
 cudaError_t launch_dispatch_bf16(const DispatchParams &p, cudaStream_t stream) {
   const int cpr = p.H / 8;
-  const int U = (cpr % 32 == 0) ? pick_units(cpr / 32) : 4;
+  const int U = (cpr % 32 == 0) ? pick_units(cpr / 32) : MOE_MAX_UNITS;
   const int64_t tasks = (int64_t)p.N * ((cpr + 32 * U - 1) / (32 * U));
   switch (U) {
     case 1: return launch_tasks(dispatch_bf16_kernel<1>, tasks, p, stream);
@@ -310,7 +350,7 @@ cudaError_t launch_dispatch_bf16(const DispatchParams &p, cudaStream_t stream) {
 
 cudaError_t launch_dispatch_fp8(const DispatchParams &p, cudaStream_t stream) {
   const int nb = p.H / 128;
-  const int P = (nb % 2 == 0) ? pick_units(nb / 2) : 4;
+  const int P = (nb % 2 == 0) ? pick_units(nb / 2) : MOE_MAX_UNITS;
   const int64_t tasks = (int64_t)p.N * ((nb + 2 * P - 1) / (2 * P));
   switch (P) {
     case 1: return launch_tasks(dispatch_fp8_kernel<1>, tasks, p, stream);

@@ -171,3 +171,28 @@ def test_workload_full_size(name):
                              expert_y="device" if big else "host", combine_tokens=sample)
     print(name, res)
     torch.cuda.empty_cache()
+
+
+def test_fp8_scales_offset_by_4_bytes():
+    """A scale array 4 bytes past a 16-byte boundary: the scales must still
+    land exactly (bulk copies need 16-byte alignment, so they are not used)."""
+    import combine_moe_dispatch_gb300 as moe
+    import oracle
+    R, T, H, E, K = 2, 96, 512, 8, 2
+    idx, x, w = _rand_case(77, R, T, H, E, K)
+    cap = R * T
+    shape = moe.make_shape(R, T, H, E, K, cap, moe.PAYLOAD_FP8_E4M3)
+    b = moe.Buffers(shape, expert_x=True, expert_y=False)
+    raw = torch.full((E * cap * (H // 128) + 4,), -5.0, dtype=torch.float32, device="cuda")
+    sc = raw[1:1 + E * cap * (H // 128)]
+    assert sc.data_ptr() % 16 == 4
+    idx_d = gpu_check.dev(idx)
+    b.plan(idx_d)
+    moe.dispatch(shape, gpu_check.dev(x), idx_d, b.slot_of, b.expert_x, sc, b.workspace)
+    st, cnt, off, slot, src = oracle.plan(R, T, E, K, cap, idx)
+    q_o, sc_o = oracle.dispatch_fp8(x, idx, slot, E, cap)
+    got = sc.view(E, cap, H // 128).cpu().numpy()
+    for e in range(E):
+        assert np.array_equal(got[e, :cnt[e]].view(np.uint32), sc_o[e, :cnt[e]].view(np.uint32))
+        assert (got[e, cnt[e]:] == -5.0).all()
+    assert np.array_equal(b.expert_x.cpu().numpy()[0, :cnt[0]], q_o[0, :cnt[0]])
