@@ -29,8 +29,10 @@
 // (two roundings of 2^-24 each, plus half an ulp).  Rounding to E4M3 is
 // monotone, so if q~ moved 4 ulps down and 4 ulps up rounds to the same
 // byte, that byte is e4m3(RN(x / scale)); otherwise (a quotient next to an
-// E4M3 midpoint, or a zero) the lane divides with IEEE __fdiv_rn.  The
-// result is bit-identical to dividing every element.
+// E4M3 midpoint, or a zero) the lane divides its 8 elements with IEEE
+// __fdiv_rn, behind a warp-wide vote so that the division is a real branch
+// taken only when needed.  The result is bit-identical to dividing every
+// element.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -168,14 +170,16 @@ __device__ __forceinline__ float nudge(float q, int ulps) {
   return __int_as_float(__float_as_int(q) + ulps);
 }
 
-// e4m3(RN(a / s)), e4m3(RN(b / s)) given r = RN(1 / s) finite (see the file
-// comment for why the fast path is exact).
-__device__ __forceinline__ uint32_t quant_pair(float a, float b, float s, float r) {
+// Candidate bytes for e4m3(RN(a / s)), e4m3(RN(b / s)) from r = RN(1 / s):
+// returns true, with the bytes in *out, when q~ = RN(a * r) and its 4-ulp
+// neighbours round to the same bytes (see the file comment); false when the
+// pair needs the exact division.
+__device__ __forceinline__ bool quant_pair_fast(float a, float b, float r, uint32_t *out) {
   const float qa = __fmul_rn(a, r), qb = __fmul_rn(b, r);
   const uint32_t lo = e4m3x2(nudge(qa, -4), nudge(qb, -4));
   const uint32_t hi = e4m3x2(nudge(qa, 4), nudge(qb, 4));
-  if (lo == hi) return lo;
-  return e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+  *out = lo;
+  return lo == hi;
 }
 
 // fp8 quantisation; P pairs of 128-element blocks per task.
@@ -231,19 +235,27 @@ __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Ta
 #pragma unroll
     for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
     const float scale = __fdiv_rn(amax, 448.0f);
-    uint32_t lo = 0, hi = 0;
-    if (amax != 0.0f) {
-      const float r = __frcp_rn(scale);
-      if (r <= 3.0e38f) {   // finite reciprocal: fast exact path
-        lo = quant_pair(f[0], f[1], scale, r) | (quant_pair(f[2], f[3], scale, r) << 16);
-        hi = quant_pair(f[4], f[5], scale, r) | (quant_pair(f[6], f[7], scale, r) << 16);
-      } else {
-        lo = e4m3x2(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale)) |
-             (e4m3x2(__fdiv_rn(f[2], scale), __fdiv_rn(f[3], scale)) << 16);
-        hi = e4m3x2(__fdiv_rn(f[4], scale), __fdiv_rn(f[5], scale)) |
-             (e4m3x2(__fdiv_rn(f[6], scale), __fdiv_rn(f[7], scale)) << 16);
+    // All lanes take the same path here (no divergent branch around the
+    // warp-wide vote): an all-zero block gives q = 0; otherwise the
+    // multiply-by-reciprocal candidates, and the exact division only for the
+    // rare pairs whose candidate is not certain (or when 1/scale overflows).
+    const bool zero = amax == 0.0f;
+    const float r = zero ? 1.0f : __frcp_rn(scale);
+    const bool r_ok = r <= 3.0e38f;
+    uint32_t b4[4];
+    bool sure = true;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sure &= quant_pair_fast(f[2 * i], f[2 * i + 1], r, &b4[i]);
+    const bool slow = !zero && !(r_ok && sure);
+    if (__any_sync(kFull, slow)) {
+      if (slow) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          b4[i] = e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
       }
     }
+    uint32_t lo = b4[0] | (b4[1] << 16), hi = b4[2] | (b4[3] << 16);
+    if (zero) lo = hi = 0u;
     t.q[it] = make_uint2(lo, hi);
     const float s_even = __shfl_sync(kFull, scale, 0);
     const float s_odd = __shfl_sync(kFull, scale, 16);
