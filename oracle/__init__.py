@@ -63,6 +63,8 @@ class Oracle:
         P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         lib.oracle_plan.argtypes = [I, I, I, I, I, P, P, P, P, P]
         lib.oracle_plan.restype = I
+        lib.oracle_plan_masked.argtypes = [I, I, I, I, I, P, P, P, P, P, P]
+        lib.oracle_plan_masked.restype = I
         lib.oracle_dispatch_bf16.argtypes = [I, I, I, I, I, P, P, P, P]
         lib.oracle_dispatch_bf16.restype = None
         lib.oracle_quant_row_e4m3.argtypes = [I, P, P, P]
@@ -115,6 +117,19 @@ class Oracle:
         src = np.full((E, cap), -1, np.int32)
         st = self.lib.oracle_plan(R, T, E, K, cap, _ptr(idx), _ptr(cnt), _ptr(off),
                                   _ptr(slot), _ptr(src))
+        return st, cnt, off, slot, src
+
+    def plan_masked(self, R: int, T: int, E: int, K: int, cap: int, topk_idx, num_tokens=None):
+        """As ``plan`` for ragged ranks (``num_tokens[R]``, None = all T) and
+        masked entries (expert id -1)."""
+        idx = _c(topk_idx, np.int32).reshape(R * T, K)
+        nt = None if num_tokens is None else _c(num_tokens, np.int32)
+        cnt = np.full(E, -1, np.int32)
+        off = np.full((E, R + 1), -1, np.int32)
+        slot = np.full((R * T, K), -7, np.int32)
+        src = np.full((E, cap), -1, np.int32)
+        st = self.lib.oracle_plan_masked(R, T, E, K, cap, _ptr(idx), None if nt is None else _ptr(nt),
+                                         _ptr(cnt), _ptr(off), _ptr(slot), _ptr(src))
         return st, cnt, off, slot, src
 
     def dispatch_bf16(self, x_bits, topk_idx, slot_of, E: int, cap: int, out=None):
@@ -179,7 +194,7 @@ def default() -> Oracle:
 
 def __getattr__(name):
     # Module-level shortcuts: oracle.plan(...), oracle.combine(...), ...
-    if name in ("bf16_to_f32", "f32_to_bf16", "e4m3_to_f32", "f32_to_e4m3", "plan",
+    if name in ("bf16_to_f32", "f32_to_bf16", "e4m3_to_f32", "f32_to_e4m3", "plan", "plan_masked",
                 "dispatch_bf16", "quant_row_e4m3", "dispatch_fp8", "combine"):
         return getattr(default(), name)
     raise AttributeError(name)

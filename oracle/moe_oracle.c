@@ -160,6 +160,76 @@ int oracle_plan(int R, int T, int E, int K, int cap, const int32_t *topk_idx,
   return status;
 }
 
+/* "Lower latency and higher throughput with multi-node DeepSeek deployment",
+ * CUDA Graph: data-parallel groups run different batch sizes, and the
+ * all-to-all kernels let them do so without padding every group to the
+ * largest batch.  "Efficient and portable mixture-of-experts communication",
+ * Portable Kernels: the number of tokens a group sends is bounded by a fixed
+ * maximum per group (here T).
+ *
+ * Readings taken: rank r holds num_tokens[r] valid tokens (clamped to
+ * [0, T]); an expert id of -1 marks an entry that is not routed.  Only
+ * routed entries are counted and get slots, in the same stable (rank, token,
+ * k) order; the others get slot_of = -1. */
+static int routed_entry(int T, int K, const int32_t *num_tokens, const int32_t *topk_idx,
+                        int64_t g, int k) {
+  int64_t r = g / T, t = g % T;
+  if (num_tokens) {
+    int64_t nt = num_tokens[r];
+    if (nt < 0) nt = 0;
+    if (nt > T) nt = T;
+    if (t >= nt) return 0;
+  }
+  return topk_idx[g * K + k] != -1;
+}
+
+int oracle_plan_masked(int R, int T, int E, int K, int cap, const int32_t *topk_idx,
+                       const int32_t *num_tokens, int32_t *expert_num_tokens,
+                       int32_t *expert_rank_offsets, int32_t *slot_of, int32_t *src_of) {
+  if (R <= 0 || T < 0 || E <= 0 || K <= 0 || cap <= 0) return ORACLE_BAD_SHAPE;
+  const int64_t N = (int64_t)R * T;
+
+  for (int64_t g = 0; g < N; ++g)
+    for (int k = 0; k < K; ++k)
+      if (routed_entry(T, K, num_tokens, topk_idx, g, k) &&
+          (topk_idx[g * K + k] < 0 || topk_idx[g * K + k] >= E))
+        return ORACLE_BAD_EXPERT;
+
+  for (int e = 0; e < E; ++e) expert_num_tokens[e] = 0;
+  for (int64_t g = 0; g < N; ++g)
+    for (int k = 0; k < K; ++k)
+      if (routed_entry(T, K, num_tokens, topk_idx, g, k))
+        expert_num_tokens[topk_idx[g * K + k]] += 1;
+
+  for (int e = 0; e < E; ++e)
+    for (int r = 0; r <= R; ++r) expert_rank_offsets[(int64_t)e * (R + 1) + r] = 0;
+  for (int r = 0; r <= R; ++r)
+    for (int64_t g = 0; g < (int64_t)r * T; ++g)
+      for (int k = 0; k < K; ++k)
+        if (routed_entry(T, K, num_tokens, topk_idx, g, k))
+          expert_rank_offsets[(int64_t)topk_idx[g * K + k] * (R + 1) + r] += 1;
+
+  int32_t *fill = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+  if (!fill) abort();
+  int status = ORACLE_OK;
+  for (int64_t g = 0; g < N; ++g) {
+    for (int k = 0; k < K; ++k) {
+      if (!routed_entry(T, K, num_tokens, topk_idx, g, k)) {
+        slot_of[g * K + k] = -1;
+        continue;
+      }
+      int e = topk_idx[g * K + k];
+      int s = fill[e];
+      fill[e] += 1;
+      slot_of[g * K + k] = s;
+      if (s < cap) src_of[(int64_t)e * cap + s] = (int32_t)(g * K + k);
+      else status = ORACLE_CAPACITY;
+    }
+  }
+  free(fill);
+  return status;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Dispatch.                                                                 */
 /* ------------------------------------------------------------------------ */

@@ -85,6 +85,16 @@ int oracle_plan(int R, int T, int E, int K, int cap, const int32_t *topk_idx,
                 int32_t *expert_num_tokens, int32_t *expert_rank_offsets,
                 int32_t *slot_of, int32_t *src_of);
 
+/* Plan with ragged ranks and masked routing.  Entry (g, k) of token
+ * g = r*T + t is routed iff t < clamp(num_tokens[r], 0, T) (num_tokens NULL:
+ * every token) and topk_idx[g,k] != -1; entries of tokens beyond num_tokens
+ * are ignored whatever they hold.  Counts, offsets and slots are those of
+ * oracle_plan over the routed entries only; unrouted entries get
+ * slot_of = -1.  A routed id outside [0, E) gives ORACLE_BAD_EXPERT. */
+int oracle_plan_masked(int R, int T, int E, int K, int cap, const int32_t *topk_idx,
+                       const int32_t *num_tokens, int32_t *expert_num_tokens,
+                       int32_t *expert_rank_offsets, int32_t *slot_of, int32_t *src_of);
+
 /* ---- dispatch ------------------------------------------------------------ */
 /* bf16 payload: expert_x[e][slot_of[g,k]][:] = x[g][:] bit for bit. */
 void oracle_dispatch_bf16(int N, int H, int E, int K, int cap,

@@ -239,6 +239,75 @@ def check_plan_empty(o):
     assert st == 0 and (cnt == 0).all() and (off == 0).all() and (src == -1).all()
 
 
+def _routed_mask(R, T, K, topk_idx, num_tokens):
+    idx = np.asarray(topk_idx, np.int64).reshape(R * T, K)
+    t = np.arange(R * T) % T
+    r = np.arange(R * T) // T
+    nt = np.full(R, T) if num_tokens is None else np.clip(np.asarray(num_tokens), 0, T)
+    return (t < nt[r])[:, None] & (idx != -1)
+
+
+def plan_masked_by_sort(R, T, E, K, topk_idx, num_tokens):
+    """Masked plan from numpy: the routed entries' positions, then a stable
+    argsort of their experts."""
+    routed = _routed_mask(R, T, K, topk_idx, num_tokens).ravel()
+    flat = np.asarray(topk_idx, np.int64).ravel()
+    pos = np.nonzero(routed)[0]
+    ex = flat[pos]
+    order = np.argsort(ex, kind="stable")
+    cnt = np.bincount(ex, minlength=E).astype(np.int32)
+    start = np.concatenate([[0], np.cumsum(cnt)[:-1]]).astype(np.int64)
+    slot = np.full(flat.size, -1, np.int64)
+    slot[pos[order]] = np.arange(pos.size) - start[ex[order]]
+    off = np.zeros((E, R + 1), np.int32)
+    for e in range(E):
+        off[e] = np.searchsorted(np.sort(pos[ex == e]), np.arange(R + 1) * T * K)
+    src_rows = [pos[order][start[e]:start[e] + cnt[e]] for e in range(E)]
+    return cnt, off, slot.reshape(-1, K).astype(np.int32), src_rows
+
+
+def check_plan_masked(o):
+    rng = np.random.default_rng(71)
+    shapes = [(1, 2, 2, 2), (2, 1, 2, 2), (3, 1, 3, 1), (2, 2, 2, 1)]
+    for R, T, E, K in shapes:                      # exhaustive over ids in {-1..E-1}
+        N = R * T
+        for combo in itertools.product(range(-1, E), repeat=N * K):
+            idx = np.array(combo, np.int32).reshape(N, K)
+            nt = rng.integers(-1, T + 2, R).astype(np.int32)   # includes out-of-range counts
+            for num_tokens in (None, nt):
+                st, cnt, off, slot, src = o.plan_masked(R, T, E, K, N * K, idx, num_tokens)
+                rc, ro, rs, rows = plan_masked_by_sort(R, T, E, K, idx, num_tokens)
+                assert st == 0, f"status {st}"
+                assert np.array_equal(cnt, rc) and np.array_equal(off, ro), "masked counts/offsets"
+                assert np.array_equal(slot, rs), "masked slots"
+                for e in range(E):
+                    assert np.array_equal(src[e, :cnt[e]], rows[e]), "masked src_of"
+    for R, T, E, K in [(4, 50, 16, 4), (8, 33, 256, 8)]:   # random, larger
+        idx = np.argsort(rng.random((R * T, E)), axis=1)[:, :K].astype(np.int32)
+        idx[rng.random(idx.shape) < 0.2] = -1
+        nt = rng.integers(0, T + 1, R).astype(np.int32)
+        st, cnt, off, slot, src = o.plan_masked(R, T, E, K, R * T, idx, nt)
+        rc, ro, rs, rows = plan_masked_by_sort(R, T, E, K, idx, nt)
+        assert st == 0 and np.array_equal(cnt, rc) and np.array_equal(off, ro)
+        assert np.array_equal(slot, rs)
+        assert cnt.sum() == _routed_mask(R, T, K, idx, nt).sum(), "counts = routed entries"
+    # ids of padding tokens are ignored, routed out-of-range ids are errors
+    idx = np.array([[0, 1], [5, 9]], np.int32)
+    assert o.plan_masked(1, 2, 2, 2, 4, idx, np.array([1], np.int32))[0] == 0
+    assert o.plan_masked(1, 2, 2, 2, 4, idx, np.array([2], np.int32))[0] == 1
+    # hand-worked fixture
+    g = read_kv("plan_masked.txt")[0]
+    R, T, E, K, cap = (int(g[k]) for k in ("R", "T", "E", "K", "cap"))
+    idx = np.array(_ints(g["topk_idx"]), np.int32).reshape(R * T, K)
+    st, cnt, off, slot, src = o.plan_masked(R, T, E, K, cap, idx,
+                                            np.array(_ints(g["num_tokens"]), np.int32))
+    assert st == int(g["status"])
+    assert cnt.tolist() == _ints(g["expert_num_tokens"]), "fixture counts"
+    assert off.ravel().tolist() == _ints(g["expert_rank_offsets"]), "fixture offsets"
+    assert slot.ravel().tolist() == _ints(g["slot_of"]), "fixture slots"
+    assert src.ravel().tolist() == _ints(g["src_of"]), "fixture src_of"
+
+
 def check_plan_errors(o):
     idx = np.array([[0, 1], [2, 3]], np.int32)
     for bad in (-1, 4, 1 << 20):
@@ -437,7 +506,8 @@ def check_combine_bound(o):
 
 ALL_CHECKS = [
     check_bf16, check_e4m3_decode, check_e4m3_encode,
-    check_plan_exhaustive, check_plan_random, check_plan_empty, check_plan_errors,
+    check_plan_exhaustive, check_plan_random, check_plan_empty, check_plan_masked,
+    check_plan_errors,
     check_plan_golden,
     check_dispatch_bf16, check_fp8_golden, check_fp8_properties, check_dispatch_fp8,
     check_combine_golden, check_combine_identity, check_combine_bound,

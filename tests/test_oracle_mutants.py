@@ -12,7 +12,8 @@ import pytest
 import oracle
 import oracle_pins
 
-# (name, text in moe_oracle.c, replacement).  Each text occurs exactly once.
+# (name, text in moe_oracle.c, replacement).  Every occurrence of the text is
+# replaced (the same mistake made consistently).
 MUTANTS = [
     ("bf16_ties_away", "(lower == 0x8000u && (upper & 1u))", "(lower == 0x8000u)"),
     ("bf16_truncate", "upper += 1u;", "upper += 0u;"),
@@ -31,6 +32,9 @@ MUTANTS = [
      "src_of[(int64_t)e * cap + s] = (int32_t)(g * K);"),
     ("plan_no_capacity_status", "else status = ORACLE_CAPACITY;", "else status = ORACLE_OK;"),
     ("plan_wrong_error_code", "return ORACLE_BAD_EXPERT;", "return ORACLE_CAPACITY;"),
+    ("masked_rank0_count", "int64_t nt = num_tokens[r];", "int64_t nt = num_tokens[0];"),
+    ("masked_counts_padding", "    if (t >= nt) return 0;", "    if (t > nt) return 0;"),
+    ("masked_routes_minus_one", "  return topk_idx[g * K + k] != -1;", "  return topk_idx[g * K + k] != -2;"),
     ("dispatch_bf16_swap_pairs", "dst[h] = x[g * H + h];", "dst[h] = x[g * H + (h ^ 1)];"),
     ("quant_scale_447", "float s = amax / 448.0f;", "float s = amax / 447.0f;"),
     ("quant_amax_drops_last", "for (int i = b * 128; i < (b + 1) * 128; ++i) {\n      float a",
@@ -65,7 +69,7 @@ def test_real_oracle_passes_every_pin():
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_mutant_is_caught(tmp_path, name, old, new):
     src = open(oracle.SRC).read()
-    assert src.count(old) == 1, f"mutation anchor for {name} must occur exactly once"
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
     mdir = tmp_path / name
     mdir.mkdir()
     shutil.copy(oracle.HDR, mdir / "moe_oracle.h")
