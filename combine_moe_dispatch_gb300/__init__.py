@@ -78,6 +78,7 @@ SIGNATURES = {
     "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "moe_workspace_set_debug": ([_P, _U32, _U64, _P], ctypes.c_int),
     "moe_plan_noalloc": ([_SP, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "moe_plan_masked": ([_SP, _P, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
 }
 
 _lib = None
@@ -150,6 +151,16 @@ def plan(shape: Shape, topk_idx, expert_num_tokens, expert_rank_offsets, slot_of
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream))
     return _check(st, "moe_plan", check)
+
+
+def plan_masked(shape: Shape, topk_idx, num_tokens, expert_num_tokens, expert_rank_offsets,
+                slot_of, src_of, workspace, stream=None, check=True) -> Status:
+    st = load_library().moe_plan_masked(ctypes.byref(shape), _ptr(topk_idx), _ptr(num_tokens),
+                                        _ptr(expert_num_tokens), _ptr(expert_rank_offsets),
+                                        _ptr(slot_of), _ptr(src_of), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(stream))
+    return _check(st, "moe_plan_masked", check)
 
 
 def dispatch(shape: Shape, x, topk_idx, slot_of, expert_x, expert_x_scale, workspace,
@@ -229,6 +240,11 @@ class Buffers:
     def plan(self, topk_idx, stream=None, check=True):
         return plan(self.shape, topk_idx, self.expert_num_tokens, self.expert_rank_offsets,
                     self.slot_of, self.src_of, self.workspace, stream, check)
+
+    def plan_masked(self, topk_idx, num_tokens=None, stream=None, check=True):
+        return plan_masked(self.shape, topk_idx, num_tokens, self.expert_num_tokens,
+                           self.expert_rank_offsets, self.slot_of, self.src_of, self.workspace,
+                           stream, check)
 
     def dispatch(self, x, topk_idx, stream=None, check=True):
         return dispatch(self.shape, x, topk_idx, self.slot_of, self.expert_x, self.expert_x_scale,

@@ -98,9 +98,31 @@ moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, void *str
   return from_cuda(cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream));
 }
 
+static moe_status plan_common(const moe_shape *shape, const int32_t *topk_idx,
+                              const int32_t *num_tokens, int masked, int32_t *expert_num_tokens,
+                              int32_t *expert_rank_offsets, int32_t *slot_of, int32_t *src_of,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
 moe_status moe_plan(const moe_shape *shape, const int32_t *topk_idx, int32_t *expert_num_tokens,
                     int32_t *expert_rank_offsets, int32_t *slot_of, int32_t *src_of,
                     void *workspace, size_t workspace_bytes, void *stream) {
+  return plan_common(shape, topk_idx, nullptr, 0, expert_num_tokens, expert_rank_offsets, slot_of,
+                     src_of, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_plan_masked(const moe_shape *shape, const int32_t *topk_idx,
+                           const int32_t *num_tokens, int32_t *expert_num_tokens,
+                           int32_t *expert_rank_offsets, int32_t *slot_of, int32_t *src_of,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+  if (num_tokens && ((uintptr_t)num_tokens & 3u)) return MOE_ERR_ALIGNMENT;
+  return plan_common(shape, topk_idx, num_tokens, 1, expert_num_tokens, expert_rank_offsets,
+                     slot_of, src_of, workspace, workspace_bytes, stream);
+}
+
+static moe_status plan_common(const moe_shape *shape, const int32_t *topk_idx,
+                              const int32_t *num_tokens, int masked, int32_t *expert_num_tokens,
+                              int32_t *expert_rank_offsets, int32_t *slot_of, int32_t *src_of,
+                              void *workspace, size_t workspace_bytes, void *stream) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   const bool empty = shape->tokens_per_rank == 0;   // topk_idx, slot_of may then be NULL
@@ -125,6 +147,8 @@ moe_status moe_plan(const moe_shape *shape, const int32_t *topk_idx, int32_t *ex
   char *base = static_cast<char *>(workspace);
   PlanParams p;
   p.topk_idx = topk_idx;
+  p.num_tokens = num_tokens;
+  p.masked = masked;
   p.expert_num_tokens = expert_num_tokens;
   p.expert_rank_offsets = expert_rank_offsets;
   p.slot_of = slot_of;

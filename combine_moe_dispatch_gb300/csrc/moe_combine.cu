@@ -70,9 +70,12 @@ combine_kernel(CombineParams p) {
       s_l = __ldg(p.slot_of + g * p.K + lane);
       w_l = __ldg(p.topk_weights + g * p.K + lane);
     }
+    // slot -1: an entry the plan did not route (skipped; a token with no
+    // routed entry gets y = +0).  Other out-of-range entries are reported.
+    const bool routed = lane < p.K && s_l != -1;
     const bool e_ok = e_l >= 0 && e_l < p.E;
-    const bool ok = lane < p.K && e_ok && s_l >= 0 && s_l < p.cap;
-    if (seg == 0 && lane < p.K && !ok)
+    const bool ok = routed && e_ok && s_l >= 0 && s_l < p.cap;
+    if (seg == 0 && routed && !ok)
       report_status(p.hdr, e_ok ? MOE_ERR_CAPACITY : MOE_ERR_BAD_EXPERT);
     const unsigned okmask = __ballot_sync(kFullMask, ok);
 

@@ -88,6 +88,8 @@ inline WsLayout ws_layout(const moe_shape &s) {
 // ---------------------------------------------------------------------------
 struct PlanParams {
   const int32_t *topk_idx;
+  const int32_t *num_tokens;   // [R] valid tokens per rank, or null (all T)
+  int masked;                  // 1: expert id -1 marks an entry that is not routed
   int32_t *expert_num_tokens;
   int32_t *expert_rank_offsets;
   int32_t *slot_of;
@@ -131,6 +133,15 @@ struct CombineParams {
   WsHeader *hdr;
   int N, H, E, K, cap;
 };
+
+// Valid tokens of rank r: clamp(num_tokens[r], 0, T), or T without num_tokens.
+#ifdef __CUDACC__
+__device__ __forceinline__ int rank_tokens(const PlanParams &p, int r) {
+  if (!p.num_tokens) return p.T;
+  const int nt = __ldg(p.num_tokens + r);
+  return nt < 0 ? 0 : (nt > p.T ? p.T : nt);
+}
+#endif
 
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_plan(const PlanParams &p, cudaStream_t stream);

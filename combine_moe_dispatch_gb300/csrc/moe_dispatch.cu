@@ -61,12 +61,15 @@ __device__ __forceinline__ Routes load_routes(const DispatchParams &p, int64_t g
   return r;
 }
 
-// Mask of the valid k; out-of-range entries are reported once per token.
+// Mask of the routed, valid k.  slot -1 marks an entry the plan did not
+// route (masked id, or a token beyond its rank's count): skipped silently.
+// Other out-of-range entries are skipped and reported once per token.
 __device__ __forceinline__ unsigned check_routes(const DispatchParams &p, const Routes &r, int lane,
                                                  bool report) {
+  const bool routed = lane < p.K && r.s != -1;
   const bool e_ok = r.e >= 0 && r.e < p.E;
-  const bool ok = lane < p.K && e_ok && r.s >= 0 && r.s < p.cap;
-  if (report && lane < p.K && !ok)
+  const bool ok = routed && e_ok && r.s >= 0 && r.s < p.cap;
+  if (report && routed && !ok)
     report_status(p.hdr, e_ok ? MOE_ERR_CAPACITY : MOE_ERR_BAD_EXPERT);
   return __ballot_sync(kFull, ok);
 }

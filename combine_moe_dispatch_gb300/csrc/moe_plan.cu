@@ -75,6 +75,7 @@ plan_kernel(PlanParams p) {
     const int n_ent = tok * p.K;
     const int64_t ent0 = g0 * p.K;
     const int epw = ((n_ent + kPlanWarps * 32 - 1) / (kPlanWarps * 32)) * 32;  // entries per warp
+    const int routed_ent = max(0, min(tok, rank_tokens(p, r) - j * p.tile_tokens)) * p.K;
     const unsigned lt_mask = (1u << lane) - 1u;
 
     // 1. stable ranks inside the warp's share of the tile
@@ -84,9 +85,10 @@ plan_kernel(PlanParams p) {
     for (int b = 0; b < kPlanBatchesPerWarp; ++b) {
       const int pl = warp * epw + b * 32 + lane;
       const bool valid = (b * 32 < epw) && pl < n_ent;
-      int e = valid ? __ldg(p.topk_idx + ent0 + pl) : -1;
-      const bool ok = valid && e >= 0 && e < E;
-      if (valid && !ok) atomicOr(&s_err, kErrBadExpert);
+      int e = (valid && pl < routed_ent) ? __ldg(p.topk_idx + ent0 + pl) : -1;
+      const bool routed = valid && pl < routed_ent && !(p.masked && e == -1);
+      const bool ok = routed && e >= 0 && e < E;
+      if (routed && !ok) atomicOr(&s_err, kErrBadExpert);
       const int key = ok ? e : -1;
       const unsigned same = __match_any_sync(0xFFFFFFFFu, key);
       const int before = __popc(same & lt_mask);
@@ -298,11 +300,14 @@ plan_cluster_kernel(PlanParams p) {
     n_ent = min(p.chunk_tokens, p.T - j * p.chunk_tokens) * p.K;
     ent0 = g0 * p.K;
   }
+  // entries of tokens beyond the rank's valid count are not routed
+  const int routed_ent = has_chunk
+      ? max(0, min(n_ent / p.K, rank_tokens(p, r) - j * p.chunk_tokens)) * p.K : 0;
   int e_in[kClusterMaxBatches];
 #pragma unroll
   for (int b = 0; b < kClusterMaxBatches; ++b) {
     const int pl = b * 32 + lane;
-    e_in[b] = (b < p.batches && pl < n_ent) ? __ldg(p.topk_idx + ent0 + pl) : -1;
+    e_in[b] = (b < p.batches && pl < routed_ent) ? __ldg(p.topk_idx + ent0 + pl) : -1;
   }
   for (int i = tid; i < kClusterWarps * E; i += nthreads) wc[i] = 0;
   if (tid == 0) s_cta_err = 0;
@@ -320,10 +325,10 @@ plan_cluster_kernel(PlanParams p) {
     lexp[b] = -1;
     if (b >= p.batches) continue;                       // warp-uniform
     const int pl = b * 32 + lane;
-    const bool valid = pl < n_ent;
     const int e = e_in[b];
-    const bool ok = valid && e >= 0 && e < E;
-    if (valid && !ok) my_err |= (int32_t)kErrBadExpert;
+    const bool routed = pl < routed_ent && !(p.masked && e == -1);
+    const bool ok = routed && e >= 0 && e < E;
+    if (routed && !ok) my_err |= (int32_t)kErrBadExpert;
     const unsigned same = peers_with_same_key(ok ? e : -1, bits);
     const int before = __popc(same & lt_mask);
     const int wbase = ok ? wc[warp * E + e] : 0;

@@ -116,6 +116,26 @@ moe_status moe_plan(const moe_shape *shape, const int32_t *topk_idx,
                     int32_t *slot_of, int32_t *src_of,
                     void *workspace, size_t workspace_bytes, void *stream);
 
+/* Plan for ragged ranks and masked routing.
+ *
+ * Follows "Lower latency and higher throughput with multi-node DeepSeek
+ * deployment", CUDA Graph (data-parallel groups run different batch sizes,
+ * without padding every group to the largest) and "Efficient and portable
+ * mixture-of-experts communication", Portable Kernels (a fixed maximum
+ * number of tokens per group, here T).
+ *
+ * As moe_plan, except that entry (g, k) of token g = r*T + t is routed only
+ * if t < clamp(num_tokens[r], 0, T) and topk_idx[g,k] != -1.  Unrouted
+ * entries are not counted, get slot_of = -1, and are skipped by moe_dispatch
+ * and moe_combine; ids of tokens beyond num_tokens[r] are never read.  A
+ * token with no routed entry combines to y = +0.
+ * In:   num_tokens [R] int32 device array (4-byte aligned), or NULL for all T.
+ * Errors: as moe_plan (a routed id outside [0, E) is BAD_EXPERT). */
+moe_status moe_plan_masked(const moe_shape *shape, const int32_t *topk_idx,
+                           const int32_t *num_tokens, int32_t *expert_num_tokens,
+                           int32_t *expert_rank_offsets, int32_t *slot_of, int32_t *src_of,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
 /* Dispatch: write each token's row to every (expert, slot) it is routed to.
  *
  * Follows "Efficient and portable mixture-of-experts communication", Dispatch
@@ -137,7 +157,8 @@ moe_status moe_plan(const moe_shape *shape, const int32_t *topk_idx,
  * Work: the workspace moe_plan used; the call writes nothing if its status
  *       word is set.  Requires moe_plan on the same topk_idx, ordered before
  *       this call.  An entry whose expert or slot is out of range is skipped
- *       and sets the status word (BAD_EXPERT / CAPACITY).
+ *       and sets the status word (BAD_EXPERT / CAPACITY); an entry with
+ *       slot_of = -1 (not routed, see moe_plan_masked) is skipped silently.
  * Host errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA. */
 moe_status moe_dispatch(const moe_shape *shape, const void *x,
                         const int32_t *topk_idx, const int32_t *slot_of,
@@ -158,7 +179,8 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x,
  *       topk_idx, slot_of [N, K] int32; topk_weights [N, K] fp32
  * Out:  y            [N, H] bf16, 16-byte aligned
  * Work: the workspace moe_plan used; nothing is written if its status word
- *       is set; entries out of range are skipped and set it.
+ *       is set; entries out of range are skipped and set it; entries with
+ *       slot_of = -1 (not routed) are skipped silently.
  * Host errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA. */
 moe_status moe_combine(const moe_shape *shape, const void *expert_y,
                        const int32_t *topk_idx, const int32_t *slot_of,

@@ -67,14 +67,24 @@ class Result(dict):
 
 def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
              payloads=("bf16", "fp8"), expert_y="host", combine_tokens=None, seed=0,
-             expect_status=None) -> Result:
+             expect_status=None, masked=False, num_tokens=None) -> Result:
     """Run plan/dispatch/combine on the GPU and compare with the oracle.
     ``expert_y``: "host" (seeded numpy, full [E,cap,H]) or "device" (seeded
     torch generator on the GPU, for shapes too large for the host).
     ``combine_tokens``: token ids the oracle recomputes (None = all)."""
     N = R * T
     res = Result(mismatch={}, max_ulp=0, not_bit_exact=0)
-    st_o, cnt, off, slot_o, src_o = oracle.plan(R, T, E, K, cap, idx)
+    if masked:
+        st_o, cnt, off, slot_o, src_o = oracle.plan_masked(R, T, E, K, cap, idx, num_tokens)
+        nt_d = None if num_tokens is None else dev(np.asarray(num_tokens, np.int32))
+    else:
+        st_o, cnt, off, slot_o, src_o = oracle.plan(R, T, E, K, cap, idx)
+
+    def do_plan(buf):
+        if masked:
+            buf.plan_masked(idx_d, nt_d)
+        else:
+            buf.plan(idx_d)
     if expect_status is None:
         expect_status = {oracle.OK: moe.Status.OK, oracle.CAPACITY: moe.Status.CAPACITY,
                          oracle.BAD_EXPERT: moe.Status.BAD_EXPERT}[st_o]
@@ -93,7 +103,7 @@ def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
         if buf.expert_x_scale is not None:
             buf.expert_x_scale.fill_(SENTINEL_SCALE)
         buf.src_of.fill_(-1)
-        buf.plan(idx_d)
+        do_plan(buf)
         st = moe.read_status(buf.workspace)
         assert st == expect_status, f"plan status {st!r}, expected {expect_status!r}"
         if expect_status == moe.Status.BAD_EXPERT:
@@ -118,21 +128,23 @@ def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
         assert torch.equal(touched, populated_mask(cnt, cap)), "rows written outside [0, count)"
         if N == 0:
             continue
-        got = buf.expert_x[e_t, s_t]
+        sel = (slot_o.reshape(-1) >= 0)
+        sel_d = dev(sel)
+        got = buf.expert_x[e_t[sel_d], s_t[sel_d]]
         if payload == "bf16":
             got = host_u16(got)
-            exp = np.repeat(x, K, axis=0)
+            exp = np.repeat(x, K, axis=0)[sel]
             assert np.array_equal(got, exp), "bf16 dispatch rows"
             bf16_buf = buf
         else:
             q_o, sc_o = oracle.dispatch_fp8(x, np.zeros((N, 1), np.int32),
                                             np.arange(N, dtype=np.int32)[:, None], 1, N)
             got_q = got.cpu().numpy()
-            exp_q = np.repeat(q_o[0], K, axis=0)
+            exp_q = np.repeat(q_o[0], K, axis=0)[sel]
             bad = np.nonzero((got_q != exp_q).any(axis=1))[0]
             assert bad.size == 0, f"fp8 bytes differ in {bad.size} rows (first entry {bad[:4]})"
-            got_s = buf.expert_x_scale[e_t, s_t].cpu().numpy()
-            exp_s = np.repeat(sc_o[0], K, axis=0)
+            got_s = buf.expert_x_scale[e_t[sel_d], s_t[sel_d]].cpu().numpy()
+            exp_s = np.repeat(sc_o[0], K, axis=0)[sel]
             assert np.array_equal(got_s.view(np.uint32), exp_s.view(np.uint32)), "fp8 scales"
             pop = populated_mask(cnt, cap)
             assert bool((buf.expert_x_scale[~pop] == SENTINEL_SCALE).all()), "scales beyond count"
@@ -143,7 +155,7 @@ def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
     if bf16_buf is None:
         shape = moe.make_shape(R, T, H, E, K, cap, moe.PAYLOAD_BF16)
         bf16_buf = moe.Buffers(shape, expert_y=False, expert_x=False)
-        bf16_buf.plan(idx_d)
+        do_plan(bf16_buf)
         assert moe.read_status(bf16_buf.workspace) == moe.Status.OK
     if expert_y == "host":
         ey = inputs.expert_outputs(E, cap, H, seed)
@@ -160,11 +172,14 @@ def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
     if expert_y == "host":
         y_o = oracle.combine(ey, idx, slot_o, w)[G]
     else:
-        rows = host_u16(ey_d[dev(idx[G].astype(np.int64)).view(-1),
-                             dev(slot_o[G].astype(np.int64)).view(-1)])
+        routed = slot_o[G] >= 0
+        e_g = np.where(routed, idx[G], 0).astype(np.int64)
+        s_g = np.where(routed, slot_o[G], 0).astype(np.int64)
+        rows = host_u16(ey_d[dev(e_g).view(-1), dev(s_g).view(-1)])
         nG = len(G)
         y_o = oracle.combine(rows.reshape(1, nG * K, H), np.zeros((nG, K), np.int32),
-                             np.arange(nG * K, dtype=np.int32).reshape(nG, K), w[G])
+                             np.where(routed, np.arange(nG * K).reshape(nG, K), -1).astype(np.int32),
+                             w[G])
     yg = y[G]
     assert not np.isnan((yg.astype(np.uint32) << 16).view(np.float32)).any(), \
         "NaN in y: a row beyond an expert's count was read"

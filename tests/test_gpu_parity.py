@@ -196,3 +196,53 @@ def test_fp8_scales_offset_by_4_bytes():
         assert np.array_equal(got[e, :cnt[e]].view(np.uint32), sc_o[e, :cnt[e]].view(np.uint32))
         assert (got[e, cnt[e]:] == -5.0).all()
     assert np.array_equal(b.expert_x.cpu().numpy()[0, :cnt[0]], q_o[0, :cnt[0]])
+
+
+MASKED = [
+    # name, R, T, H, E, K  (the last two take the multi-tile plan)
+    ("masked_cluster", 4, 100, 256, 16, 4),
+    ("masked_dsv3_like", 8, 128, 512, 256, 8),
+    ("masked_many_tiles", 1, 20000, 128, 32, 8),
+    ("masked_e2048", 2, 128, 256, 2048, 8),
+]
+
+
+@pytest.mark.parametrize("name,R,T,H,E,K", MASKED, ids=[c[0] for c in MASKED])
+def test_masked_ragged_routing(name, R, T, H, E, K):
+    """moe_plan_masked: ragged ranks (num_tokens, including 0, T and values
+    outside [0, T]) and masked entries (id -1) through plan, dispatch (both
+    payloads) and combine, against the oracle's masked plan."""
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    idx, x, w = _rand_case(zlib.crc32(name.encode()) + 1, R, T, H, E, K)
+    idx[rng.random(idx.shape) < 0.15] = -1
+    nt = rng.integers(0, T + 1, R).astype(np.int32)
+    nt[0] = T
+    if R > 2:
+        nt[1], nt[2] = 0, T + 7
+    # ids of tokens beyond num_tokens are never read: fill them with garbage
+    t = np.arange(R * T) % T
+    pad = t >= np.clip(nt, 0, T)[np.arange(R * T) // T]
+    idx[pad] = 1 << 20
+    res = gpu_check.run_case(R, T, H, E, K, R * T, idx, x, w, ("bf16", "fp8"),
+                             masked=True, num_tokens=nt)
+    assert res["not_bit_exact"] == 0
+
+
+def test_masked_without_num_tokens():
+    idx, x, w = _rand_case(3, 2, 64, 256, 8, 2)
+    idx[::3, 1] = -1
+    idx[5] = -1                                        # a token with no routed entry: y = +0
+    res = gpu_check.run_case(2, 64, 256, 8, 2, 128, idx, x, w, ("bf16",), masked=True)
+    assert res["not_bit_exact"] == 0
+
+
+def test_masked_full_size_dsv3_decode():
+    wl = WORKLOADS["dsv3_decode"]
+    d = inputs.make(wl, 0)
+    rng = np.random.default_rng(11)
+    idx = d["topk_idx"].copy()
+    idx[rng.random(idx.shape) < 0.1] = -1
+    nt = rng.integers(wl.T // 2, wl.T + 1, wl.R).astype(np.int32)
+    gpu_check.run_case(wl.R, wl.T, wl.H, wl.E, wl.K, wl.cap, idx, d["x"], d["topk_weights"],
+                       ("bf16", "fp8"), expert_y="device", masked=True, num_tokens=nt)
+    torch.cuda.empty_cache()
