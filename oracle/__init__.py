@@ -73,6 +73,8 @@ class Oracle:
         lib.oracle_dispatch_fp8.restype = None
         lib.oracle_combine.argtypes = [I, I, I, I, I, P, P, P, P, P]
         lib.oracle_combine.restype = None
+        lib.oracle_combine_shared.argtypes = [I, I, I, I, I, P, P, P, P, P, P]
+        lib.oracle_combine_shared.restype = None
         for name in ("oracle_bf16_to_f32_n", "oracle_f32_to_bf16_n",
                      "oracle_e4m3_to_f32_n", "oracle_f32_to_e4m3_n"):
             getattr(lib, name).argtypes = [I64, P, P]
@@ -178,6 +180,20 @@ class Oracle:
         return y
 
 
+    def combine_shared(self, expert_y_bits, topk_idx, slot_of, topk_weights, shared_bits):
+        ey = _c(expert_y_bits, np.uint16)
+        E, cap, H = ey.shape
+        idx = _c(topk_idx, np.int32)
+        N, K = idx.shape
+        slot = _c(slot_of, np.int32)
+        w = _c(topk_weights, np.float32)
+        sh = _c(shared_bits, np.uint16)
+        y = np.empty((N, H), np.uint16)
+        self.lib.oracle_combine_shared(N, H, E, K, cap, _ptr(ey), _ptr(idx), _ptr(slot), _ptr(w),
+                                       _ptr(sh), _ptr(y))
+        return y
+
+
 _default = None
 
 
@@ -195,6 +211,6 @@ def default() -> Oracle:
 def __getattr__(name):
     # Module-level shortcuts: oracle.plan(...), oracle.combine(...), ...
     if name in ("bf16_to_f32", "f32_to_bf16", "e4m3_to_f32", "f32_to_e4m3", "plan", "plan_masked",
-                "dispatch_bf16", "quant_row_e4m3", "dispatch_fp8", "combine"):
+                "dispatch_bf16", "quant_row_e4m3", "dispatch_fp8", "combine", "combine_shared"):
         return getattr(default(), name)
     raise AttributeError(name)

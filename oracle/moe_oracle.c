@@ -331,3 +331,28 @@ void oracle_combine(int N, int H, int E, int K, int cap,
     }
   }
 }
+
+/* "Lower latency and higher throughput with multi-node DeepSeek
+ * deployment", Expert Parallelism and Compute/Communication Overlap: each
+ * token also goes through a shared expert, whose output is added to the
+ * routed experts' weighted sum (and can be computed while dispatch is in
+ * flight).  Reading taken: the shared output (bf16) seeds the fp32
+ * accumulator, the routed terms follow in ascending k, one final rounding. */
+void oracle_combine_shared(int N, int H, int E, int K, int cap,
+                           const uint16_t *expert_y, const int32_t *topk_idx,
+                           const int32_t *slot_of, const float *topk_weights,
+                           const uint16_t *shared, uint16_t *y) {
+  for (int64_t g = 0; g < N; ++g) {
+    for (int h = 0; h < H; ++h) {
+      float acc = oracle_bf16_to_f32(shared[g * H + h]);
+      for (int k = 0; k < K; ++k) {
+        int e = topk_idx[g * K + k];
+        int s = slot_of[g * K + k];
+        if (e < 0 || e >= E || s < 0 || s >= cap) continue;
+        float v = oracle_bf16_to_f32(expert_y[((int64_t)e * cap + s) * H + h]);
+        acc = fmaf(topk_weights[g * K + k], v, acc);
+      }
+      y[g * H + h] = oracle_f32_to_bf16(acc); /* shared + routed, one rounding */
+    }
+  }
+}

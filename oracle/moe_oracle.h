@@ -121,6 +121,15 @@ void oracle_combine(int N, int H, int E, int K, int cap,
                     const int32_t *slot_of, const float *topk_weights,
                     uint16_t *y);
 
+/* Combine fused with the shared expert: as oracle_combine, but the fp32
+ * accumulator starts at the shared expert's output for the token:
+ * y[g][h] = bf16( fma chain over k of w*expert_y, starting from
+ *                 float(shared[g][h]) ). */
+void oracle_combine_shared(int N, int H, int E, int K, int cap,
+                           const uint16_t *expert_y, const int32_t *topk_idx,
+                           const int32_t *slot_of, const float *topk_weights,
+                           const uint16_t *shared, uint16_t *y);
+
 #ifdef __cplusplus
 }
 #endif

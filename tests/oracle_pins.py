@@ -504,11 +504,44 @@ def check_combine_bound(o):
         assert (np.abs(yf - S) <= bound).all(), "combine outside the fp32 error bound"
 
 
+def check_combine_shared(o):
+    """Hand-worked cases; a zero shared output reduces to combine exactly
+    (+0 + x = x for every non-NaN x); the fp64 error bound with the shared
+    term; and the shared output alone when no entry is routed."""
+    for c in read_kv("combine_shared.txt"):
+        w = np.array(_ints(c["w"]), np.uint32).view(np.float32)
+        v = np.array(_ints(c["v"]), np.uint16)
+        K, H = w.size, 8
+        ey = np.repeat(v[:, None, None], H, axis=2).astype(np.uint16)
+        sh = np.full((1, H), int(c["shared"], 0), np.uint16)
+        y = o.combine_shared(ey, np.arange(K, dtype=np.int32)[None, :], np.zeros((1, K), np.int32),
+                             w[None, :], sh)
+        assert (y == int(c["y"], 0)).all(), f"combine_shared case {c['case']}: {hex(y[0, 0])}"
+    rng = np.random.default_rng(41)
+    R, T, E, K, H = 2, 20, 9, 4, 64
+    N, idx, w, slot, cnt = _combine_case(o, rng, R, T, E, K, H)
+    ey = torch_bf16_bits(rng.standard_normal((E, N, H)).astype(np.float32))
+    zero = np.zeros((N, H), np.uint16)
+    assert np.array_equal(o.combine_shared(ey, idx, slot, w, zero), o.combine(ey, idx, slot, w))
+    sh = torch_bf16_bits(rng.standard_normal((N, H)).astype(np.float32))
+    y = o.combine_shared(ey, idx, slot, w, sh)
+    eyf = torch.from_numpy(ey.view(np.int16)).view(torch.bfloat16).double().numpy()
+    shf = torch.from_numpy(sh.view(np.int16)).view(torch.bfloat16).double().numpy()
+    terms = w.astype(np.float64)[:, :, None] * eyf[idx, slot]
+    S = shf + terms.sum(axis=1)
+    A = np.abs(shf) + np.abs(terms).sum(axis=1)
+    yf = torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).double().numpy()
+    half_ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(S), 2.0**-126))) - 8)
+    assert (np.abs(yf - S) <= half_ulp + (K + 1) * 2.0**-24 * A * 1.01 + 2.0**-133).all()
+    none = np.full((N, K), -1, np.int32)
+    assert np.array_equal(o.combine_shared(ey, none, none, w, sh), sh), "no routed entry: y = shared"
+
+
 ALL_CHECKS = [
     check_bf16, check_e4m3_decode, check_e4m3_encode,
     check_plan_exhaustive, check_plan_random, check_plan_empty, check_plan_masked,
     check_plan_errors,
     check_plan_golden,
     check_dispatch_bf16, check_fp8_golden, check_fp8_properties, check_dispatch_fp8,
-    check_combine_golden, check_combine_identity, check_combine_bound,
+    check_combine_golden, check_combine_identity, check_combine_bound, check_combine_shared,
 ]

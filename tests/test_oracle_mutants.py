@@ -50,6 +50,11 @@ MUTANTS = [
     ("combine_k_descending", "float acc = 0.0f;\n      for (int k = 0; k < K; ++k) {",
      "float acc = 0.0f;\n      for (int k = K - 1; k >= 0; --k) {"),
     ("combine_acc_negzero", "float acc = 0.0f;", "float acc = -0.0f;"),
+    ("shared_ignored", "float acc = oracle_bf16_to_f32(shared[g * H + h]);", "float acc = 0.0f;"),
+    ("shared_after_rounding",
+     "      y[g * H + h] = oracle_f32_to_bf16(acc); /* shared + routed, one rounding */",
+     "      y[g * H + h] = oracle_f32_to_bf16(oracle_bf16_to_f32(oracle_f32_to_bf16(acc - "
+     "oracle_bf16_to_f32(shared[g * H + h]))) + oracle_bf16_to_f32(shared[g * H + h]));"),
 ]
 
 
