@@ -79,6 +79,7 @@ SIGNATURES = {
     "moe_workspace_set_debug": ([_P, _U32, _U64, _P], ctypes.c_int),
     "moe_plan_noalloc": ([_SP, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_plan_masked": ([_SP, _P, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
+    "moe_combine_shared": ([_SP, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
 }
 
 _lib = None
@@ -189,6 +190,14 @@ def plan_noalloc(shape: Shape, topk_idx, expert_num_tokens, expert_rank_offsets,
                                          _ptr(slot_of), _ptr(src_of), _ptr(status_out),
                                          _stream(stream))
     return _check(st, "moe_plan_noalloc", check)
+
+
+def combine_shared(shape: Shape, expert_y, topk_idx, slot_of, topk_weights, shared_y, y, workspace,
+                   stream=None, check=True) -> Status:
+    st = load_library().moe_combine_shared(ctypes.byref(shape), _ptr(expert_y), _ptr(topk_idx),
+                                           _ptr(slot_of), _ptr(topk_weights), _ptr(shared_y),
+                                           _ptr(y), _ptr(workspace), _stream(stream))
+    return _check(st, "moe_combine_shared", check)
 
 
 def read_status(workspace, stream=None) -> Status:

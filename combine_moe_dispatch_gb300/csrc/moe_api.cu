@@ -198,9 +198,34 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *to
   return from_cuda(fp8 ? launch_dispatch_fp8(p, s) : launch_dispatch_bf16(p, s));
 }
 
+static moe_status combine_common(const moe_shape *shape, const void *expert_y,
+                                 const int32_t *topk_idx, const int32_t *slot_of,
+                                 const float *topk_weights, const void *shared, void *y,
+                                 void *workspace, void *stream);
+
 moe_status moe_combine(const moe_shape *shape, const void *expert_y, const int32_t *topk_idx,
                        const int32_t *slot_of, const float *topk_weights, void *y,
                        void *workspace, void *stream) {
+  return combine_common(shape, expert_y, topk_idx, slot_of, topk_weights, nullptr, y, workspace,
+                        stream);
+}
+
+moe_status moe_combine_shared(const moe_shape *shape, const void *expert_y,
+                              const int32_t *topk_idx, const int32_t *slot_of,
+                              const float *topk_weights, const void *shared_y, void *y,
+                              void *workspace, void *stream) {
+  if (shape && shape->tokens_per_rank > 0) {
+    if (!shared_y) return MOE_ERR_INVALID_ARG;
+    if ((uintptr_t)shared_y % 16 != 0) return MOE_ERR_ALIGNMENT;
+  }
+  return combine_common(shape, expert_y, topk_idx, slot_of, topk_weights, shared_y, y, workspace,
+                        stream);
+}
+
+static moe_status combine_common(const moe_shape *shape, const void *expert_y,
+                                 const int32_t *topk_idx, const int32_t *slot_of,
+                                 const float *topk_weights, const void *shared, void *y,
+                                 void *workspace, void *stream) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   if (shape->tokens_per_rank == 0) return MOE_OK;   // empty batch: nothing to read or write
@@ -211,6 +236,7 @@ moe_status moe_combine(const moe_shape *shape, const void *expert_y, const int32
     return MOE_ERR_ALIGNMENT;
   CombineParams p;
   p.expert_y = static_cast<const uint16_t *>(expert_y);
+  p.shared = static_cast<const uint16_t *>(shared);
   p.topk_idx = topk_idx;
   p.slot_of = slot_of;
   p.topk_weights = topk_weights;

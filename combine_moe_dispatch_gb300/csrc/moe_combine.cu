@@ -6,7 +6,10 @@
 //   y[g][h] = bf16_rn( acc ),  acc = 0; for k = 0..K-1:
 //             acc = fma(w[g,k], float(expert_y[idx[g,k]][slot_of[g,k]][h]), acc)
 // i.e. the receiver-side weighted sum of the 16-bit expert outputs, one fp32
-// accumulator per element, fixed k order, one final rounding.
+// accumulator per element, fixed k order, one final rounding.  With a
+// shared-expert output ("Lower latency and higher throughput with
+// multi-node DeepSeek deployment", Expert Parallelism) the accumulator
+// starts from it instead of +0, which saves a separate read-add-write pass.
 //
 // How: a warp takes one (token, segment) task at a time; lanes 0..K-1 hold
 // the token's K (expert, slot, weight) and broadcast them by shuffle.  For a
@@ -81,10 +84,26 @@ combine_kernel(CombineParams p) {
 
     const int c0 = seg * cpt + lane;
     float acc[U][8];
+    if (p.shared) {                       // the shared expert's output seeds the accumulator
+      const uint16_t *srow = p.shared + g * p.H;
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * 32;
+        const uint4 v = c < cpr ? __ldcs(reinterpret_cast<const uint4 *>(srow + (int64_t)c * 8))
+                                : make_uint4(0, 0, 0, 0);
+        const uint32_t a[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+        for (int i = 0; i < 4; ++i) {
+          acc[u][2 * i] = __uint_as_float(a[i] << 16);
+          acc[u][2 * i + 1] = __uint_as_float(a[i] & 0xFFFF0000u);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+    }
 
     for (int kb = 0; kb < p.K; kb += KG) {
       uint4 v[KG][U];

@@ -126,6 +126,7 @@ struct DispatchParams {
 
 struct CombineParams {
   const uint16_t *expert_y;
+  const uint16_t *shared;      // [N, H] bf16 shared-expert output, or null
   const int32_t *topk_idx;
   const int32_t *slot_of;
   const float *topk_weights;

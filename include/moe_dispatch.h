@@ -187,6 +187,23 @@ moe_status moe_combine(const moe_shape *shape, const void *expert_y,
                        const float *topk_weights, void *y,
                        void *workspace, void *stream);
 
+/* Combine fused with the shared expert:
+ * y[g] = bf16( shared_y[g] + sum over k of w[g,k] * expert_y[idx[g,k]][slot_of[g,k]] ).
+ *
+ * Follows "Lower latency and higher throughput with multi-node DeepSeek
+ * deployment", Expert Parallelism and Compute/Communication Overlap (every
+ * token also passes through a shared expert whose output is added to the
+ * routed sum).  Arithmetic: the fp32 accumulator starts at the bf16 shared
+ * value, then one fused multiply-add per k in ascending k, one final
+ * round-to-nearest-even -- one pass instead of a combine plus an add.
+ * In:   shared_y [N, H] bf16, 16-byte aligned (may be the same array as y);
+ *       everything else as moe_combine.
+ * Errors: as moe_combine. */
+moe_status moe_combine_shared(const moe_shape *shape, const void *expert_y,
+                              const int32_t *topk_idx, const int32_t *slot_of,
+                              const float *topk_weights, const void *shared_y, void *y,
+                              void *workspace, void *stream);
+
 /* Synchronise `stream` and read the workspace status word into *out (MOE_OK
  * or a device error).  The only call that waits for the device; meant for
  * tests and error handling, not for the hot path.

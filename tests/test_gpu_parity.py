@@ -246,3 +246,36 @@ def test_masked_full_size_dsv3_decode():
     gpu_check.run_case(wl.R, wl.T, wl.H, wl.E, wl.K, wl.cap, idx, d["x"], d["topk_weights"],
                        ("bf16", "fp8"), expert_y="device", masked=True, num_tokens=nt)
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("R,T,H,E,K", [(2, 64, 256, 8, 2), (3, 50, 392, 37, 5), (8, 128, 7168, 256, 8)])
+def test_combine_shared(R, T, H, E, K):
+    """moe_combine_shared against the oracle, bit for bit, including tokens
+    with no routed entry (y = shared) and in place (y = shared_y)."""
+    import combine_moe_dispatch_gb300 as moe
+    import oracle
+    idx, x, w = _rand_case(R * T + K, R, T, H, E, K)
+    idx[::7] = -1
+    N, cap = R * T, R * T
+    shape = moe.make_shape(R, T, H, E, K, cap)
+    b = moe.Buffers(shape, expert_x=False, expert_y=False)
+    idx_d = gpu_check.dev(idx)
+    b.plan_masked(idx_d)
+    st, cnt, off, slot, src = oracle.plan_masked(R, T, E, K, cap, idx)
+    ey = inputs.expert_outputs_device(E, cap, H, 5)
+    ey[~gpu_check.populated_mask(cnt, cap)] = float("nan")
+    sh = inputs.hidden_states(N, H, 9)
+    sh_d = gpu_check.dev(sh)
+    moe.combine_shared(shape, ey, idx_d, b.slot_of, gpu_check.dev(w), sh_d, b.y, b.workspace)
+    routed = slot >= 0
+    e_g = np.where(routed, idx, 0).astype(np.int64)
+    s_g = np.where(routed, slot, 0).astype(np.int64)
+    rows = gpu_check.host_u16(ey[gpu_check.dev(e_g).view(-1), gpu_check.dev(s_g).view(-1)])
+    y_o = oracle.combine_shared(rows.reshape(1, N * K, H), np.zeros((N, K), np.int32),
+                                np.where(routed, np.arange(N * K).reshape(N, K), -1).astype(np.int32),
+                                w, sh)
+    assert np.array_equal(gpu_check.host_u16(b.y), y_o)
+    # in place: the shared output buffer receives y
+    moe.combine_shared(shape, ey, idx_d, b.slot_of, gpu_check.dev(w), sh_d, sh_d, b.workspace)
+    assert np.array_equal(gpu_check.host_u16(sh_d), y_o)
+    assert moe.read_status(b.workspace) == moe.Status.OK
