@@ -75,6 +75,8 @@ class Oracle:
         lib.oracle_combine.restype = None
         lib.oracle_combine_shared.argtypes = [I, I, I, I, I, P, P, P, P, P, P]
         lib.oracle_combine_shared.restype = None
+        lib.oracle_router_topk.argtypes = [I, I, I, P, P, P]
+        lib.oracle_router_topk.restype = None
         for name in ("oracle_bf16_to_f32_n", "oracle_f32_to_bf16_n",
                      "oracle_e4m3_to_f32_n", "oracle_f32_to_e4m3_n"):
             getattr(lib, name).argtypes = [I64, P, P]
@@ -194,6 +196,15 @@ class Oracle:
         return y
 
 
+    def router_topk(self, logits, K: int):
+        lg = _c(logits, np.float32)
+        N, E = lg.shape
+        idx = np.empty((N, K), np.int32)
+        w = np.empty((N, K), np.float32)
+        self.lib.oracle_router_topk(N, E, K, _ptr(lg), _ptr(idx), _ptr(w))
+        return idx, w
+
+
 _default = None
 
 
@@ -211,6 +222,6 @@ def default() -> Oracle:
 def __getattr__(name):
     # Module-level shortcuts: oracle.plan(...), oracle.combine(...), ...
     if name in ("bf16_to_f32", "f32_to_bf16", "e4m3_to_f32", "f32_to_e4m3", "plan", "plan_masked",
-                "dispatch_bf16", "quant_row_e4m3", "dispatch_fp8", "combine", "combine_shared"):
+                "dispatch_bf16", "quant_row_e4m3", "dispatch_fp8", "combine", "combine_shared", "router_topk"):
         return getattr(default(), name)
     raise AttributeError(name)

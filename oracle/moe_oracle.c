@@ -356,3 +356,48 @@ void oracle_combine_shared(int N, int H, int E, int K, int cap,
     }
   }
 }
+
+/* "Efficient and portable mixture-of-experts communication", Introduction:
+ * the router is a small linear layer producing a probability distribution
+ * over experts; the experts with the K highest scores are chosen and the
+ * output is their average weighted by the router's probabilities.  "Lower
+ * latency and higher throughput with multi-node DeepSeek deployment", MoE
+ * Router: a sort that tracks the indices of the sorted elements; the sparse
+ * kernels consume the top-K indices and scores directly.
+ *
+ * Readings taken: order by logit, descending, ties by lower expert index;
+ * weights = softmax over the K chosen logits (the renormalised top-K of the
+ * full softmax), exp(l_k - l_max) / sum, in fp64, rounded once to fp32. */
+static const float *router_row;
+
+static int router_cmp(const void *a, const void *b) {
+  const int ia = *(const int *)a, ib = *(const int *)b;
+  const float la = router_row[ia], lb = router_row[ib];
+  if (la > lb) return -1;
+  if (la < lb) return 1;
+  return (ia > ib) - (ia < ib);
+}
+
+void oracle_router_topk(int N, int E, int K, const float *logits, int32_t *topk_idx,
+                        float *topk_weights) {
+  int *order = (int *)malloc((size_t)E * sizeof(int));
+  double *z = (double *)malloc((size_t)K * sizeof(double));
+  if (!order || !z) abort();
+  for (int64_t g = 0; g < N; ++g) {
+    router_row = logits + g * E;
+    for (int e = 0; e < E; ++e) order[e] = e;
+    qsort(order, (size_t)E, sizeof(int), router_cmp);
+    const double m = (double)router_row[order[0]];
+    double sum = 0.0;
+    for (int k = 0; k < K; ++k) {
+      z[k] = exp((double)router_row[order[k]] - m);
+      sum += z[k];
+    }
+    for (int k = 0; k < K; ++k) {
+      topk_idx[g * K + k] = order[k];
+      topk_weights[g * K + k] = (float)(z[k] / sum);
+    }
+  }
+  free(order);
+  free(z);
+}

@@ -130,6 +130,12 @@ void oracle_combine_shared(int N, int H, int E, int K, int cap,
                            const int32_t *slot_of, const float *topk_weights,
                            const uint16_t *shared, uint16_t *y);
 
+/* Router: for each of N tokens, the K largest of its E logits (ties: lower
+ * expert index first), in that order, and their softmax weights computed in
+ * fp64 from the largest logit and rounded once to fp32.  K <= E. */
+void oracle_router_topk(int N, int E, int K, const float *logits, int32_t *topk_idx,
+                        float *topk_weights);
+
 #ifdef __cplusplus
 }
 #endif

@@ -537,6 +537,33 @@ def check_combine_shared(o):
     assert np.array_equal(o.combine_shared(ey, none, none, w, sh), sh), "no routed entry: y = shared"
 
 
+def check_router(o):
+    """Hand-worked cases; indices against numpy's lexsort (descending logit,
+    then ascending index); weights within 1 fp32 ulp of a numpy fp64 softmax
+    over the chosen logits (the two fp64 exps may differ in the last bit);
+    weights sum to 1 and do not increase."""
+    for c in read_kv("router.txt"):
+        E, K = int(c["E"]), int(c["K"])
+        lg = np.array(_ints(c["logits"]), np.uint32).view(np.float32).reshape(1, E)
+        idx, w = o.router_topk(lg, K)
+        assert idx[0].tolist() == _ints(c["topk_idx"]), f"router case {c['case']}: {idx}"
+        assert w.view(np.uint32)[0].tolist() == _ints(c["topk_weights"]), f"router case {c['case']}: {w}"
+    rng = np.random.default_rng(61)
+    for N, E, K in [(200, 8, 2), (100, 256, 8), (50, 384, 8), (30, 7, 7), (64, 64, 1)]:
+        lg = rng.standard_normal((N, E)).astype(np.float32) * 3
+        lg[: N // 2] = np.round(lg[: N // 2])               # many ties
+        idx, w = o.router_topk(lg, K)
+        ref = np.stack([np.lexsort((np.arange(E), -lg[g]))[:K] for g in range(N)]).astype(np.int32)
+        assert np.array_equal(idx, ref), "router indices"
+        sel = np.take_along_axis(lg, ref, axis=1).astype(np.float64)
+        z = np.exp(sel - sel[:, :1])
+        wr = (z / z.sum(axis=1, keepdims=True)).astype(np.float32)
+        d = np.abs(w.view(np.int32).astype(np.int64) - wr.view(np.int32).astype(np.int64))
+        assert d.max() <= 1, "router weights vs fp64 softmax"
+        assert (np.abs(w.astype(np.float64).sum(axis=1) - 1) <= K * 2.0**-24).all()
+        assert (np.diff(w, axis=1) <= 0).all(), "weights follow the logit order"
+
+
 ALL_CHECKS = [
     check_bf16, check_e4m3_decode, check_e4m3_encode,
     check_plan_exhaustive, check_plan_random, check_plan_empty, check_plan_masked,
@@ -544,4 +571,5 @@ ALL_CHECKS = [
     check_plan_golden,
     check_dispatch_bf16, check_fp8_golden, check_fp8_properties, check_dispatch_fp8,
     check_combine_golden, check_combine_identity, check_combine_bound, check_combine_shared,
+    check_router,
 ]

@@ -51,6 +51,10 @@ MUTANTS = [
      "float acc = 0.0f;\n      for (int k = K - 1; k >= 0; --k) {"),
     ("combine_acc_negzero", "float acc = 0.0f;", "float acc = -0.0f;"),
     ("shared_ignored", "float acc = oracle_bf16_to_f32(shared[g * H + h]);", "float acc = 0.0f;"),
+    ("router_ties_higher_index", "  return (ia > ib) - (ia < ib);", "  return (ia < ib) - (ia > ib);"),
+    ("router_ascending", "  if (la > lb) return -1;\n  if (la < lb) return 1;", "  if (la > lb) return 1;\n  if (la < lb) return -1;"),
+    ("router_no_max_shift", "      z[k] = exp((double)router_row[order[k]] - m);", "      z[k] = exp((double)router_row[order[k]]);"),
+    ("router_float_softmax", "      topk_weights[g * K + k] = (float)(z[k] / sum);", "      topk_weights[g * K + k] = (float)z[k] / (float)sum + 1e-7f;"),
     ("shared_after_rounding",
      "      y[g * H + h] = oracle_f32_to_bf16(acc); /* shared + routed, one rounding */",
      "      y[g * H + h] = oracle_f32_to_bf16(oracle_bf16_to_f32(oracle_f32_to_bf16(acc - "
