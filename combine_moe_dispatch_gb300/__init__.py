@@ -80,6 +80,7 @@ SIGNATURES = {
     "moe_plan_noalloc": ([_SP, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_plan_masked": ([_SP, _P, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
     "moe_combine_shared": ([_SP, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "moe_router_topk": ([_SP, _P, _P, _P, _P], ctypes.c_int),
 }
 
 _lib = None
@@ -198,6 +199,12 @@ def combine_shared(shape: Shape, expert_y, topk_idx, slot_of, topk_weights, shar
                                            _ptr(slot_of), _ptr(topk_weights), _ptr(shared_y),
                                            _ptr(y), _ptr(workspace), _stream(stream))
     return _check(st, "moe_combine_shared", check)
+
+
+def router_topk(shape: Shape, logits, topk_idx, topk_weights, stream=None, check=True) -> Status:
+    st = load_library().moe_router_topk(ctypes.byref(shape), _ptr(logits), _ptr(topk_idx),
+                                        _ptr(topk_weights), _stream(stream))
+    return _check(st, "moe_router_topk", check)
 
 
 def read_status(workspace, stream=None) -> Status:

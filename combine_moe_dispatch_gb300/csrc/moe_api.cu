@@ -250,6 +250,26 @@ static moe_status combine_common(const moe_shape *shape, const void *expert_y,
   return from_cuda(launch_combine(p, (cudaStream_t)stream));
 }
 
+moe_status moe_router_topk(const moe_shape *shape, const float *logits, int32_t *topk_idx,
+                           float *topk_weights, void *stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (shape->top_k > shape->num_experts || shape->num_experts > kRouterMaxExperts)
+    return MOE_ERR_UNSUPPORTED;
+  if (shape->tokens_per_rank == 0) return MOE_OK;   // empty batch
+  if (!logits || !topk_idx || !topk_weights) return MOE_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(topk_weights, 4))
+    return MOE_ERR_ALIGNMENT;
+  RouterParams p;
+  p.logits = logits;
+  p.topk_idx = topk_idx;
+  p.topk_weights = topk_weights;
+  p.N = (int64_t)shape->num_ranks * shape->tokens_per_rank;
+  p.E = shape->num_experts;
+  p.K = shape->top_k;
+  return from_cuda(launch_router(p, (cudaStream_t)stream));
+}
+
 moe_status moe_read_status(const void *workspace, void *stream, moe_status *out) {
   if (!workspace || !out) return MOE_ERR_INVALID_ARG;
   int32_t v = 0;

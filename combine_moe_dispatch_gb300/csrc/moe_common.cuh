@@ -21,6 +21,7 @@ constexpr int kPlanTileEntries = 1024;                          // entries (g,k)
 constexpr int kPlanBatchesPerWarp = kPlanTileEntries / (32 * kPlanWarps);  // 2
 constexpr int kMaxExperts = 2048;
 constexpr int kMaxTopK = 32;
+constexpr int kRouterMaxExperts = 1024;   // logits held in registers, 32 per lane at most
 
 struct PlanGeometry {
   int tile_tokens;     // TT: tokens per tile
@@ -135,6 +136,14 @@ struct CombineParams {
   int N, H, E, K, cap;
 };
 
+struct RouterParams {
+  const float *logits;     // [N, E]
+  int32_t *topk_idx;       // [N, K]
+  float *topk_weights;     // [N, K]
+  int64_t N;
+  int E, K;
+};
+
 // Valid tokens of rank r: clamp(num_tokens[r], 0, T), or T without num_tokens.
 #ifdef __CUDACC__
 __device__ __forceinline__ int rank_tokens(const PlanParams &p, int r) {
@@ -149,6 +158,7 @@ cudaError_t launch_plan(const PlanParams &p, cudaStream_t stream);
 cudaError_t launch_dispatch_bf16(const DispatchParams &p, cudaStream_t stream);
 cudaError_t launch_dispatch_fp8(const DispatchParams &p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+cudaError_t launch_router(const RouterParams &p, cudaStream_t stream);
 cudaError_t launch_set_debug(WsHeader *hdr, uint32_t flags, uint64_t timeout_ns,
                              cudaStream_t stream);
 

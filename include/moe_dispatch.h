@@ -204,6 +204,25 @@ moe_status moe_combine_shared(const moe_shape *shape, const void *expert_y,
                               const float *topk_weights, const void *shared_y, void *y,
                               void *workspace, void *stream);
 
+/* Router: top-K experts and their weights from router logits, ready for
+ * moe_plan.
+ *
+ * Follows "Efficient and portable mixture-of-experts communication",
+ * Introduction (the router produces a probability distribution over the
+ * experts; the K highest-scoring experts are chosen and their outputs are
+ * averaged with weights from that distribution) and "Lower latency and
+ * higher throughput with multi-node DeepSeek deployment", MoE Router (a
+ * sort that tracks indices; sparse kernels consume the top-K indices and
+ * scores directly).  Per token: the K largest logits in descending order,
+ * ties to the lower expert index; weights = softmax over those K logits,
+ * exp(l_k - l_max) / sum computed in fp64, rounded once to fp32.
+ * In:   logits [N, E] fp32 (4-byte aligned).
+ * Out:  topk_idx [N, K] int32, topk_weights [N, K] fp32.
+ * Limits: K <= E <= 1024 (else UNSUPPORTED).  NaN logits: unspecified.
+ * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, CUDA.  No workspace. */
+moe_status moe_router_topk(const moe_shape *shape, const float *logits, int32_t *topk_idx,
+                           float *topk_weights, void *stream);
+
 /* Synchronise `stream` and read the workspace status word into *out (MOE_OK
  * or a device error).  The only call that waits for the device; meant for
  * tests and error handling, not for the hot path.

@@ -279,3 +279,30 @@ def test_combine_shared(R, T, H, E, K):
     moe.combine_shared(shape, ey, idx_d, b.slot_of, gpu_check.dev(w), sh_d, sh_d, b.workspace)
     assert np.array_equal(gpu_check.host_u16(sh_d), y_o)
     assert moe.read_status(b.workspace) == moe.Status.OK
+
+
+@pytest.mark.parametrize("N,E,K", [(64, 8, 2), (1024, 256, 8), (4096, 384, 8), (500, 1024, 32),
+                                   (33, 7, 7), (300, 64, 1)])
+def test_router_topk(N, E, K):
+    """moe_router_topk against the oracle: indices bit for bit (including
+    many exact ties), weights within 1 fp32 ulp (the two sides' fp64 exp may
+    differ in the last bit); then the router's output through moe_plan."""
+    import combine_moe_dispatch_gb300 as moe
+    import oracle
+    rng = np.random.default_rng(N + E + K)
+    lg = (rng.standard_normal((N, E)) * 3).astype(np.float32)
+    lg[: N // 3] = np.round(lg[: N // 3])
+    lg[N // 3: N // 2, : E // 2] = -np.inf
+    shape = moe.make_shape(1, N, 256, E, K, N)
+    idx_d = torch.empty((N, K), dtype=torch.int32, device="cuda")
+    w_d = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    moe.router_topk(shape, gpu_check.dev(lg), idx_d, w_d)
+    idx_o, w_o = oracle.router_topk(lg, K)
+    assert np.array_equal(idx_d.cpu().numpy(), idx_o)
+    d = np.abs(w_d.cpu().numpy().view(np.int32).astype(np.int64) - w_o.view(np.int32).astype(np.int64))
+    assert d.max() <= 1, f"router weights differ by {d.max()} ulp"
+    b = moe.Buffers(shape, expert_x=False, expert_y=False)
+    b.plan(idx_d)
+    st, cnt, off, slot, src = oracle.plan(1, N, E, K, N, idx_o)
+    assert moe.read_status(b.workspace) == moe.Status.OK
+    assert np.array_equal(b.slot_of.cpu().numpy(), slot)
