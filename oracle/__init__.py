@@ -77,6 +77,12 @@ class Oracle:
         lib.oracle_combine_shared.restype = None
         lib.oracle_router_topk.argtypes = [I, I, I, P, P, P]
         lib.oracle_router_topk.restype = None
+        lib.oracle_exp_f32.argtypes = [ctypes.c_float]
+        lib.oracle_exp_f32.restype = ctypes.c_float
+        lib.oracle_silu_f32.argtypes = [ctypes.c_float]
+        lib.oracle_silu_f32.restype = ctypes.c_float
+        lib.oracle_silu_mul_quant.argtypes = [I, I, I, P, P, P, P]
+        lib.oracle_silu_mul_quant.restype = None
         for name in ("oracle_bf16_to_f32_n", "oracle_f32_to_bf16_n",
                      "oracle_e4m3_to_f32_n", "oracle_f32_to_e4m3_n"):
             getattr(lib, name).argtypes = [I64, P, P]
@@ -205,6 +211,27 @@ class Oracle:
         return idx, w
 
 
+    def exp_f32(self, x) -> np.ndarray:
+        x = np.asarray(x, np.float32).ravel()
+        return np.array([self.lib.oracle_exp_f32(float(v)) for v in x], np.float32)
+
+    def silu_f32(self, x) -> np.ndarray:
+        x = np.asarray(x, np.float32).ravel()
+        return np.array([self.lib.oracle_silu_f32(float(v)) for v in x], np.float32)
+
+    def silu_mul_quant(self, expert_h_bits, expert_num_tokens, act_q=None, act_scale=None):
+        h = _c(expert_h_bits, np.uint16)
+        E, cap, I2 = h.shape
+        I = I2 // 2
+        cnt = _c(expert_num_tokens, np.int32)
+        if act_q is None:
+            act_q = np.zeros((E, cap, I), np.uint8)
+        if act_scale is None:
+            act_scale = np.zeros((E, cap, I // 128), np.float32)
+        self.lib.oracle_silu_mul_quant(E, cap, I, _ptr(h), _ptr(cnt), _ptr(act_q), _ptr(act_scale))
+        return act_q, act_scale
+
+
 _default = None
 
 
@@ -222,6 +249,7 @@ def default() -> Oracle:
 def __getattr__(name):
     # Module-level shortcuts: oracle.plan(...), oracle.combine(...), ...
     if name in ("bf16_to_f32", "f32_to_bf16", "e4m3_to_f32", "f32_to_e4m3", "plan", "plan_masked",
-                "dispatch_bf16", "quant_row_e4m3", "dispatch_fp8", "combine", "combine_shared", "router_topk"):
+                "dispatch_bf16", "quant_row_e4m3", "dispatch_fp8", "combine", "combine_shared", "router_topk", "exp_f32", "silu_f32",
+                "silu_mul_quant"):
         return getattr(default(), name)
     raise AttributeError(name)

@@ -401,3 +401,91 @@ void oracle_router_topk(int N, int E, int K, const float *logits, int32_t *topk_
   free(order);
   free(z);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Activation and re-quantisation between the expert GEMMs.                  */
+/* ------------------------------------------------------------------------ */
+
+/* e^x in binary32.  The pages fix no algorithm; for the quantised bytes to be
+ * reproducible bit for bit, this library fixes one, the classic Cody-Waite
+ * scheme (Cody & Waite, "Software Manual for the Elementary Functions"):
+ *   n = rint(x * log2(e)),  r = x - n*ln2_hi - n*ln2_lo   (ln2_hi has 16
+ *   significant bits, so n*ln2_hi is exact for |n| < 256),
+ *   e^r ~ sum_{k<=7} r^k / k!  (Horner with fmaf; truncation < 1e-8 on
+ *   |r| <= ln2/2),  e^x = e^r * 2^n  (2^n built exactly).
+ * Every step is one IEEE binary32 operation, so any implementation that
+ * executes the same steps gets the same bits. */
+float oracle_exp_f32(float x) {
+  if (x > 88.72f) return INFINITY;
+  if (x < -87.33f) return 0.0f;
+  const float ln2_hi = 0.693145751953125f;      /* 0x3F317200 */
+  const float ln2_lo = 1.42860677e-06f;         /* 0x35BFBE8E */
+  const float log2e = 1.44269502f;              /* 0x3FB8AA3B */
+  const float n = rintf(x * log2e);
+  float r = fmaf(-n, ln2_hi, x);
+  r = fmaf(-n, ln2_lo, r);
+  float p = 1.98412701e-04f;                     /* 1/7!  0x39500D01 */
+  p = fmaf(p, r, 1.38888892e-03f);               /* 1/6!  0x3AB60B61 */
+  p = fmaf(p, r, 8.33333377e-03f);               /* 1/5!  0x3C088889 */
+  p = fmaf(p, r, 4.16666679e-02f);               /* 1/4!  0x3D2AAAAB */
+  p = fmaf(p, r, 1.66666672e-01f);               /* 1/3!  0x3E2AAAAB */
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  int ni = (int)n;
+  if (ni > 127) {                                /* 2^128 is not a float */
+    p = p * 2.0f;
+    ni -= 1;
+  }
+  uint32_t bits = (uint32_t)(ni + 127) << 23;
+  float two_n;
+  memcpy(&two_n, &bits, sizeof two_n);
+  return p * two_n;
+}
+
+float oracle_silu_f32(float g) {
+  return g / (1.0f + oracle_exp_f32(-g));
+}
+
+/* "Lower latency and higher throughput with multi-node DeepSeek
+ * deployment", Quantization: the SiLU kernel works on activations split
+ * along the hidden dimension, quantises them with one scale per 128
+ * elements from the absolute maximum, and, to stay valid inside CUDA
+ * graphs, reads the per-expert token counts to decide which rows hold
+ * tokens instead of relying on the buffer sizes.  Reading taken: the first
+ * half of each expert_h row is the gate projection, the second the up
+ * projection; a = SiLU(gate) * up in binary32; quantisation as in
+ * oracle_quant_row_e4m3, applied to a. */
+void oracle_silu_mul_quant(int E, int cap, int I, const uint16_t *expert_h,
+                           const int32_t *expert_num_tokens, uint8_t *act_q,
+                           float *act_scale) {
+  float *a = (float *)malloc((size_t)I * sizeof(float));
+  if (!a) abort();
+  const int nb = I / 128;
+  for (int e = 0; e < E; ++e) {
+    int rows = expert_num_tokens[e];
+    if (rows < 0) rows = 0;
+    if (rows > cap) rows = cap;
+    for (int s = 0; s < rows; ++s) {
+      const int64_t row = (int64_t)e * cap + s;
+      const uint16_t *h = expert_h + row * 2 * I;
+      for (int i = 0; i < I; ++i) {
+        const float g = oracle_bf16_to_f32(h[i]);
+        const float u = oracle_bf16_to_f32(h[I + i]);
+        a[i] = oracle_silu_f32(g) * u;
+      }
+      for (int b = 0; b < nb; ++b) {
+        float amax = 0.0f;
+        for (int i = b * 128; i < (b + 1) * 128; ++i) {
+          const float v = fabsf(a[i]);
+          if (v > amax) amax = v;
+        }
+        const float sc = amax / 448.0f;
+        act_scale[row * nb + b] = sc;
+        for (int i = b * 128; i < (b + 1) * 128; ++i)
+          act_q[row * I + i] = (amax == 0.0f) ? 0x00 : oracle_f32_to_e4m3(a[i] / sc);
+      }
+    }
+  }
+  free(a);
+}

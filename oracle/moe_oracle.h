@@ -136,6 +136,23 @@ void oracle_combine_shared(int N, int H, int E, int K, int cap,
 void oracle_router_topk(int N, int E, int K, const float *logits, int32_t *topk_idx,
                         float *topk_weights);
 
+/* e^x in binary32 by the algorithm this library fixes for SiLU (Cody-Waite
+ * reduction with a two-part ln 2, degree-7 Taylor polynomial in Horner form
+ * with fused multiply-adds, exact scaling by 2^n): +inf above 88.72, 0 below
+ * -87.33. */
+float oracle_exp_f32(float x);
+/* SiLU(g) = g / (1 + e^-g) with oracle_exp_f32, in binary32. */
+float oracle_silu_f32(float g);
+
+/* Activation between the expert GEMMs: for expert e and row s <
+ * clamp(expert_num_tokens[e], 0, cap), a = SiLU(gate) * up with gate, up the
+ * two halves of expert_h[e][s] ([E, cap, 2I] bf16), then a 1x128 E4M3
+ * quantisation of a exactly like oracle_quant_row_e4m3 (on fp32 values).
+ * Writes act_q[E, cap, I] and act_scale[E, cap, I/128] for those rows only. */
+void oracle_silu_mul_quant(int E, int cap, int I, const uint16_t *expert_h,
+                           const int32_t *expert_num_tokens, uint8_t *act_q,
+                           float *act_scale);
+
 #ifdef __cplusplus
 }
 #endif

@@ -564,6 +564,72 @@ def check_router(o):
         assert (np.diff(w, axis=1) <= 0).all(), "weights follow the logit order"
 
 
+def _ulps(a, b):
+    a = np.asarray(a, np.float32).view(np.int32).astype(np.int64)
+    b = np.asarray(b, np.float32).view(np.int32).astype(np.int64)
+    a = np.where(a < 0, -(a & 0x7FFFFFFF), a)
+    b = np.where(b < 0, -(b & 0x7FFFFFFF), b)
+    return np.abs(a - b)
+
+
+def check_exp_silu(o):
+    """The fixed binary32 exp within 1 ulp of fp64 exp rounded to binary32,
+    exact at 0, saturating outside [-87.33, 88.72], monotone; SiLU within 4
+    ulp of the fp64 definition x / (1 + e^-x)."""
+    rng = np.random.default_rng(81)
+    x = np.concatenate([np.linspace(-87.3, 88.7, 20001), rng.uniform(-87.3, 88.7, 5000),
+                        rng.standard_normal(5000), [0.0, 1.0, -1.0, 0.5, 1e-8, -1e-8]]).astype(np.float32)
+    e = o.exp_f32(x)
+    assert _ulps(e, np.exp(x.astype(np.float64)).astype(np.float32)).max() <= 1, "exp within 1 ulp"
+    assert o.exp_f32([0.0])[0] == 1.0
+    assert np.isinf(o.exp_f32([88.75])[0]) and o.exp_f32([-87.4])[0] == 0.0
+    xs = np.sort(x)
+    assert (np.diff(o.exp_f32(xs)) >= 0).all(), "exp is monotone"
+    g = np.concatenate([rng.standard_normal(20000) * 4, np.linspace(-80, 80, 4001)]).astype(np.float32)
+    si = o.silu_f32(g)
+    gd = g.astype(np.float64)
+    ref = (gd / (1.0 + np.exp(-gd))).astype(np.float32)
+    assert _ulps(si, ref).max() <= 4, "silu within 4 ulp"
+    assert o.silu_f32([0.0])[0] == 0.0
+
+
+def check_silu_mul_quant(o):
+    """Rows below clamp(count, 0, cap) only; a = SiLU(gate) * up from the
+    first and second halves of each row; every dequantised value within half
+    an E4M3 step (plus the SiLU error) of the fp64 reference; zero blocks
+    give scale 0 and q = 0."""
+    rng = np.random.default_rng(91)
+    E, cap, I = 5, 6, 256
+    h = torch_bf16_bits((rng.standard_normal((E, cap, 2 * I)) * 2).astype(np.float32))
+    h[2, 0, :128] = 0                                  # zero gate block -> zero block
+    cnt = np.array([3, 0, 2, 9, -4], np.int32)         # beyond cap and negative clamp
+    q = np.full((E, cap, I), 0xA5, np.uint8)
+    sc = np.full((E, cap, I // 128), -3.0, np.float32)
+    o.silu_mul_quant(h, cnt, q, sc)
+    hf = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).double().numpy()
+    tab = e4m3_table()
+    for e in range(E):
+        rows = min(max(int(cnt[e]), 0), cap)
+        assert (q[e, rows:] == 0xA5).all() and (sc[e, rows:] == -3.0).all(), "rows beyond the count"
+        for s_ in range(rows):
+            gate, up = hf[e, s_, :I], hf[e, s_, I:]
+            a = gate / (1 + np.exp(-gate)) * up
+            for b in range(I // 128):
+                blk = a[b * 128:(b + 1) * 128]
+                amax = np.abs(blk).max()
+                if amax == 0:
+                    assert sc[e, s_, b] == 0 and (q[e, s_, b * 128:(b + 1) * 128] == 0).all()
+                    continue
+                s = float(sc[e, s_, b])
+                assert abs(s * 448 - amax) <= amax * 2.0**-20, "scale from the block maximum"
+                t = blk / s
+                step = np.where(np.abs(t) < 2.0**-6, 2.0**-9,
+                                2.0 ** (np.floor(np.log2(np.maximum(np.abs(t), 2.0**-6))) - 3))
+                deq = tab[q[e, s_, b * 128:(b + 1) * 128]]
+                assert (np.abs(deq - np.clip(t, -448, 448)) <= 0.5 * step + np.abs(t) * 2.0**-19).all()
+    assert (sc[2, 0, 0] == 0) and (q[2, 0, :128] == 0).all(), "zero gate -> zero block"
+
+
 ALL_CHECKS = [
     check_bf16, check_e4m3_decode, check_e4m3_encode,
     check_plan_exhaustive, check_plan_random, check_plan_empty, check_plan_masked,
@@ -571,5 +637,5 @@ ALL_CHECKS = [
     check_plan_golden,
     check_dispatch_bf16, check_fp8_golden, check_fp8_properties, check_dispatch_fp8,
     check_combine_golden, check_combine_identity, check_combine_bound, check_combine_shared,
-    check_router,
+    check_router, check_exp_silu, check_silu_mul_quant,
 ]

@@ -55,6 +55,13 @@ MUTANTS = [
     ("router_ascending", "  if (la > lb) return -1;\n  if (la < lb) return 1;", "  if (la > lb) return 1;\n  if (la < lb) return -1;"),
     ("router_no_max_shift", "      z[k] = exp((double)router_row[order[k]] - m);", "      z[k] = exp((double)router_row[order[k]]);"),
     ("router_float_softmax", "      topk_weights[g * K + k] = (float)(z[k] / sum);", "      topk_weights[g * K + k] = (float)z[k] / (float)sum + 1e-7f;"),
+    ("exp_no_ln2_lo", "  r = fmaf(-n, ln2_lo, r);", "  r = r;"),
+    ("exp_floor", "  const float n = rintf(x * log2e);", "  const float n = floorf(x * log2e);"),
+    ("exp_short_polynomial", "  float p = 1.98412701e-04f;", "  float p = 0.0f;"),
+    ("silu_sign", "  return g / (1.0f + oracle_exp_f32(-g));", "  return g / (1.0f + oracle_exp_f32(g));"),
+    ("silu_gate_up_swapped", "        const float g = oracle_bf16_to_f32(h[i]);\n        const float u = oracle_bf16_to_f32(h[I + i]);",
+     "        const float u = oracle_bf16_to_f32(h[i]);\n        const float g = oracle_bf16_to_f32(h[I + i]);"),
+    ("silu_count_off_by_one", "    for (int s = 0; s < rows; ++s) {", "    for (int s = 0; s + 1 < rows; ++s) {"),
     ("shared_after_rounding",
      "      y[g * H + h] = oracle_f32_to_bf16(acc); /* shared + routed, one rounding */",
      "      y[g * H + h] = oracle_f32_to_bf16(oracle_bf16_to_f32(oracle_f32_to_bf16(acc - "
