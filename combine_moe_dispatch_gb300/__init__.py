@@ -81,6 +81,7 @@ SIGNATURES = {
     "moe_plan_masked": ([_SP, _P, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
     "moe_combine_shared": ([_SP, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_router_topk": ([_SP, _P, _P, _P, _P], ctypes.c_int),
+    "moe_silu_mul_quant": ([_SP, ctypes.c_int32, _P, _P, _P, _P, _P, _P], ctypes.c_int),
 }
 
 _lib = None
@@ -205,6 +206,14 @@ def router_topk(shape: Shape, logits, topk_idx, topk_weights, stream=None, check
     st = load_library().moe_router_topk(ctypes.byref(shape), _ptr(logits), _ptr(topk_idx),
                                         _ptr(topk_weights), _stream(stream))
     return _check(st, "moe_router_topk", check)
+
+
+def silu_mul_quant(shape: Shape, intermediate: int, expert_h, expert_num_tokens, act_q, act_scale,
+                   workspace, stream=None, check=True) -> Status:
+    st = load_library().moe_silu_mul_quant(ctypes.byref(shape), intermediate, _ptr(expert_h),
+                                           _ptr(expert_num_tokens), _ptr(act_q), _ptr(act_scale),
+                                           _ptr(workspace), _stream(stream))
+    return _check(st, "moe_silu_mul_quant", check)
 
 
 def read_status(workspace, stream=None) -> Status:

@@ -270,6 +270,32 @@ moe_status moe_router_topk(const moe_shape *shape, const float *logits, int32_t 
   return from_cuda(launch_router(p, (cudaStream_t)stream));
 }
 
+moe_status moe_silu_mul_quant(const moe_shape *shape, int32_t intermediate, const void *expert_h,
+                              const int32_t *expert_num_tokens, void *act_q, float *act_scale,
+                              void *workspace, void *stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (intermediate <= 0) return MOE_ERR_INVALID_ARG;
+  if (intermediate % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)shape->num_experts * shape->capacity * 2 * intermediate >= ((int64_t)1 << 46))
+    return MOE_ERR_UNSUPPORTED;
+  if (!expert_h || !expert_num_tokens || !act_q || !act_scale) return MOE_ERR_INVALID_ARG;
+  if (!workspace) return MOE_ERR_WORKSPACE;
+  if (!aligned(expert_h, 16) || !aligned(act_q, 16) || !aligned(expert_num_tokens, 4) ||
+      !aligned(act_scale, 4) || !aligned(workspace, 16))
+    return MOE_ERR_ALIGNMENT;
+  ActParams p;
+  p.expert_h = static_cast<const uint16_t *>(expert_h);
+  p.expert_num_tokens = expert_num_tokens;
+  p.act_q = act_q;
+  p.act_scale = act_scale;
+  p.hdr = header(workspace);
+  p.E = shape->num_experts;
+  p.cap = shape->capacity;
+  p.I = intermediate;
+  return from_cuda(launch_silu_quant(p, (cudaStream_t)stream));
+}
+
 moe_status moe_read_status(const void *workspace, void *stream, moe_status *out) {
   if (!workspace || !out) return MOE_ERR_INVALID_ARG;
   int32_t v = 0;

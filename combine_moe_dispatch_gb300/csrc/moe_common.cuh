@@ -3,6 +3,7 @@
 // few PTX helpers (acquire/release flags, the global timer).
 #pragma once
 
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -136,6 +137,15 @@ struct CombineParams {
   int N, H, E, K, cap;
 };
 
+struct ActParams {
+  const uint16_t *expert_h;          // [E, cap, 2I] bf16: gate | up
+  const int32_t *expert_num_tokens;  // [E]
+  void *act_q;                       // [E, cap, I] e4m3
+  float *act_scale;                  // [E, cap, I/128]
+  WsHeader *hdr;
+  int E, cap, I;
+};
+
 struct RouterParams {
   const float *logits;     // [N, E]
   int32_t *topk_idx;       // [N, K]
@@ -159,6 +169,7 @@ cudaError_t launch_dispatch_bf16(const DispatchParams &p, cudaStream_t stream);
 cudaError_t launch_dispatch_fp8(const DispatchParams &p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 cudaError_t launch_router(const RouterParams &p, cudaStream_t stream);
+cudaError_t launch_silu_quant(const ActParams &p, cudaStream_t stream);
 cudaError_t launch_set_debug(WsHeader *hdr, uint32_t flags, uint64_t timeout_ns,
                              cudaStream_t stream);
 
@@ -275,6 +286,69 @@ __device__ __forceinline__ void pdl_allow_dependents() {
 }
 __device__ __forceinline__ void pdl_wait_for_previous() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// --- 1x128 E4M3 quantisation shared by dispatch and the activation kernel ---
+// bf16 halves of a 32-bit word -> float (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two floats -> two E4M3 bytes (first in the low byte), nearest even, saturating.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float nudge(float q, int ulps) {
+  return __int_as_float(__float_as_int(q) + ulps);
+}
+
+// Candidate bytes for e4m3(RN(a / s)), e4m3(RN(b / s)) from r = RN(1 / s):
+// returns true, with the bytes in *out, when q~ = RN(a * r) and its 4-ulp
+// neighbours round to the same bytes (see the file comment); false when the
+// pair needs the exact division.
+__device__ __forceinline__ bool quant_pair_fast(float a, float b, float r, uint32_t *out) {
+  const float qa = __fmul_rn(a, r), qb = __fmul_rn(b, r);
+  const uint32_t lo = e4m3x2(nudge(qa, -4), nudge(qb, -4));
+  const uint32_t hi = e4m3x2(nudge(qa, 4), nudge(qb, 4));
+  *out = lo;
+  return lo == hi;
+}
+
+// One lane's 8 values of a 128-element block held by a half-warp (lanes
+// 0-15 one block, 16-31 the next): the block scale amax/448 (to *scale) and
+// the 8 E4M3 bytes e4m3(RN(x / scale)), an all-zero block giving 0.  All 32
+// lanes must call it together.  Exact division, cheaply: with r = RN(1/scale),
+// q~ = RN(x * r) is within 3 binary32 ulps of RN(x / scale) (two roundings of
+// 2^-24 plus half an ulp); rounding to E4M3 is monotone, so if q~ moved 4
+// ulps down and up rounds to one byte, that byte is exact.  Otherwise (next
+// to an E4M3 midpoint, a zero element, or 1/scale overflowing) the lane
+// divides with IEEE __fdiv_rn, behind a warp-wide vote so the division is a
+// real branch.
+__device__ __forceinline__ uint2 quantise_block8(const float (&f)[8], float *scale_out) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+  const float scale = __fdiv_rn(amax, 448.0f);
+  const bool zero = amax == 0.0f;
+  const float r = zero ? 1.0f : __frcp_rn(scale);
+  const bool r_ok = r <= 3.0e38f;
+  uint32_t b4[4];
+  bool sure = true;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sure &= quant_pair_fast(f[2 * i], f[2 * i + 1], r, &b4[i]);
+  const bool slow = !zero && !(r_ok && sure);
+  if (__any_sync(0xFFFFFFFFu, slow)) {
+    if (slow) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        b4[i] = e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
+    }
+  }
+  *scale_out = scale;
+  if (zero) return make_uint2(0u, 0u);
+  return make_uint2(b4[0] | (b4[1] << 16), b4[2] | (b4[3] << 16));
 }
 
 // The status the dispatch and combine kernels see; read once per block.

@@ -161,30 +161,6 @@ dispatch_bf16_kernel(DispatchParams p) {
   }
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Two floats -> two E4M3 bytes (first in the low byte), nearest even, saturating.
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
-  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-}
-
-__device__ __forceinline__ float nudge(float q, int ulps) {
-  return __int_as_float(__float_as_int(q) + ulps);
-}
-
-// Candidate bytes for e4m3(RN(a / s)), e4m3(RN(b / s)) from r = RN(1 / s):
-// returns true, with the bytes in *out, when q~ = RN(a * r) and its 4-ulp
-// neighbours round to the same bytes (see the file comment); false when the
-// pair needs the exact division.
-__device__ __forceinline__ bool quant_pair_fast(float a, float b, float r, uint32_t *out) {
-  const float qa = __fmul_rn(a, r), qb = __fmul_rn(b, r);
-  const uint32_t lo = e4m3x2(nudge(qa, -4), nudge(qb, -4));
-  const uint32_t hi = e4m3x2(nudge(qa, 4), nudge(qb, 4));
-  *out = lo;
-  return lo == hi;
-}
-
 // fp8 quantisation; P pairs of 128-element blocks per task.
 template <int P>
 struct Fp8Raw {      // one task's input, as loaded
@@ -232,33 +208,9 @@ __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Ta
       f[2 * i] = bf16_lo(w[i]);
       f[2 * i + 1] = bf16_hi(w[i]);
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-    for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
-    const float scale = __fdiv_rn(amax, 448.0f);
-    // All lanes take the same path here (no divergent branch around the
-    // warp-wide vote): an all-zero block gives q = 0; otherwise the
-    // multiply-by-reciprocal candidates, and the exact division only for the
-    // rare pairs whose candidate is not certain (or when 1/scale overflows).
-    const bool zero = amax == 0.0f;
-    const float r = zero ? 1.0f : __frcp_rn(scale);
-    const bool r_ok = r <= 3.0e38f;
-    uint32_t b4[4];
-    bool sure = true;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sure &= quant_pair_fast(f[2 * i], f[2 * i + 1], r, &b4[i]);
-    const bool slow = !zero && !(r_ok && sure);
-    if (__any_sync(kFull, slow)) {
-      if (slow) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          b4[i] = e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
-      }
-    }
-    uint32_t lo = b4[0] | (b4[1] << 16), hi = b4[2] | (b4[3] << 16);
-    if (zero) lo = hi = 0u;
+    float scale;
+    const uint2 q = quantise_block8(f, &scale);
+    const uint32_t lo = q.x, hi = q.y;
     t.q[it] = make_uint2(lo, hi);
     const float s_even = __shfl_sync(kFull, scale, 0);
     const float s_odd = __shfl_sync(kFull, scale, 16);

@@ -6,7 +6,7 @@ both the CUDA path and the CPU oracle can consume exactly the same bytes.
 
 Recipe (numpy ``default_rng``; one independent child stream per quantity,
 spawned from ``SeedSequence(seed)`` in the order x, routing, logits,
-expert outputs):
+expert outputs, gate/up projections):
 
 * ``x``: N(0,1) in float32, rounded to bf16 by torch's CPU cast (round to
   nearest even).  Returned as ``uint16`` bit patterns.
@@ -22,6 +22,8 @@ expert outputs):
 * weights: softmax over the K chosen experts of N(0,1) logits, computed in
   float64 and stored as float32 (the router's probabilities).
 * expert outputs: N(0,1) rounded to bf16, like ``x``.
+* gate/up projections (the first expert GEMM's output, [E, cap, 2I]): the
+  gate half N(0, 2^2), the up half N(0,1), rounded to bf16.
 """
 from __future__ import annotations
 
@@ -29,7 +31,7 @@ import numpy as np
 
 from .configs import Workload
 
-_STREAMS = ("x", "routing", "logits", "expert_y")
+_STREAMS = ("x", "routing", "logits", "expert_y", "gate_up")
 
 
 def _rng(seed: int, what: str) -> np.random.Generator:
@@ -96,6 +98,23 @@ def expert_outputs_device(E: int, cap: int, H: int, seed: int = 0, device="cuda"
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     return torch.randn((E, cap, H), generator=gen, device=device, dtype=torch.bfloat16)
+
+
+def gate_up(E: int, cap: int, I: int, seed: int = 0) -> np.ndarray:
+    """expert_h[E, cap, 2I] as bf16 bits: gate half N(0, 4), up half N(0, 1)."""
+    z = _rng(seed, "gate_up").standard_normal((E, cap, 2 * I), dtype=np.float32)
+    z[..., :I] *= 2.0
+    return to_bf16_bits(z)
+
+
+def gate_up_device(E: int, cap: int, I: int, seed: int = 0, device="cuda"):
+    """As ``gate_up`` drawn on the device with a seeded torch generator."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    z = torch.randn((E, cap, 2 * I), generator=gen, device=device, dtype=torch.float32)
+    z[..., :I] *= 2.0
+    return z.to(torch.bfloat16)
 
 
 def make(wl: Workload, seed: int = 0) -> dict:

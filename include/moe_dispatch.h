@@ -223,6 +223,30 @@ moe_status moe_combine_shared(const moe_shape *shape, const void *expert_y,
 moe_status moe_router_topk(const moe_shape *shape, const float *logits, int32_t *topk_idx,
                            float *topk_weights, void *stream);
 
+/* Activation between the expert GEMMs, driven by the routing counts:
+ * for expert e and row s < clamp(expert_num_tokens[e], 0, cap),
+ *   a = SiLU(gate) * up   (gate, up = first and second half of expert_h[e][s]),
+ * then 1x128 E4M3 quantisation of a by the same rule as moe_dispatch.
+ *
+ * Follows "Lower latency and higher throughput with multi-node DeepSeek
+ * deployment", Quantization (the SiLU kernel quantises its output on the fly
+ * with one scale per 128 elements from the absolute maximum, and reads the
+ * per-expert token counts, not the buffer sizes, so that it stays valid in a
+ * CUDA graph).  SiLU(g) = g / (1 + e^-g) in binary32 with e^x by a fixed
+ * sequence of IEEE operations (Cody-Waite reduction, degree-7 Taylor
+ * polynomial with fused multiply-adds), so the bytes are reproducible.
+ * In:   expert_h [E, cap, 2*intermediate] bf16, 16-byte aligned;
+ *       expert_num_tokens [E] int32 (from moe_plan);
+ * Out:  act_q [E, cap, intermediate] E4M3 (16-byte aligned) and act_scale
+ *       [E, cap, intermediate/128] fp32, rows below the count only.
+ * Work: the workspace of the plan that produced the counts; nothing is
+ *       written if its status word is set.  Uses E and cap of `shape`.
+ * Errors: INVALID_ARG, UNSUPPORTED (intermediate % 128 != 0), ALIGNMENT,
+ *       WORKSPACE, CUDA. */
+moe_status moe_silu_mul_quant(const moe_shape *shape, int32_t intermediate, const void *expert_h,
+                              const int32_t *expert_num_tokens, void *act_q, float *act_scale,
+                              void *workspace, void *stream);
+
 /* Synchronise `stream` and read the workspace status word into *out (MOE_OK
  * or a device error).  The only call that waits for the device; meant for
  * tests and error handling, not for the hot path.

@@ -90,6 +90,12 @@ def test_host_rejections_enqueue_nothing(lib):
     assert lib.moe_combine(ctypes.byref(big_k), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None) \
         == Status.UNSUPPORTED
     assert lib.moe_plan(None, _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), 1 << 20, None) == Status.INVALID_ARG
+    # activation: intermediate size, null pointers, alignment, workspace
+    assert lib.moe_silu_mul_quant(sp, 200, _p(A), _p(A), _p(A), _p(A), _p(A), None) == Status.UNSUPPORTED
+    assert lib.moe_silu_mul_quant(sp, 0, _p(A), _p(A), _p(A), _p(A), _p(A), None) == Status.INVALID_ARG
+    assert lib.moe_silu_mul_quant(sp, 256, None, _p(A), _p(A), _p(A), _p(A), None) == Status.INVALID_ARG
+    assert lib.moe_silu_mul_quant(sp, 256, _p(A), _p(A), _p(A + 1), _p(A), _p(A), None) == Status.ALIGNMENT
+    assert lib.moe_silu_mul_quant(sp, 256, _p(A), _p(A), _p(A), _p(A), None, None) == Status.WORKSPACE
     out = ctypes.c_int(0)
     assert lib.moe_read_status(None, None, ctypes.byref(out)) == Status.INVALID_ARG
     assert lib.moe_workspace_init(None, 256, None) == Status.INVALID_ARG
