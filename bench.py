@@ -72,6 +72,26 @@ def call_bytes(wl) -> dict:
     }
 
 
+def next_row_bytes(wl, routed_masked: int, valid_tokens: int) -> dict:
+    """Algorithmic bytes of the calls beyond the step (the rows built after
+    it): the masked plan over a ragged batch, combine fused with the shared
+    expert, the activation between the expert GEMMs, and the router."""
+    N, H, E, K, R, I = wl.N, wl.H, wl.E, wl.K, wl.R, wl.inter
+    maps = N * K * 4
+    return {
+        # read num_tokens and the valid tokens' topk_idx; write slot_of (all
+        # entries, -1 where unrouted), src_of of routed entries, counts, offsets
+        "plan_masked": R * 4 + valid_tokens * K * 4 + maps + routed_masked * 4 + E * 4
+                       + E * (R + 1) * 4,
+        # combine plus the shared expert's output read
+        "combine_shared": N * K * H * 2 + 3 * maps + N * H * 2 + N * H * 2,
+        # every routed row: read gate|up (2I bf16), write I e4m3 and I/128 scales
+        "silu_mul_quant": E * 4 + N * K * (2 * I * 2 + I + (I // 128) * 4),
+        # read logits, write K ids and K weights per token
+        "router_topk": N * E * 4 + N * K * 8,
+    }
+
+
 def step_calls(wl) -> list:
     """Every row of the hot path: plan, both dispatch payloads (fp8 needs
     H % 128 == 0), combine."""
@@ -307,6 +327,116 @@ class BufferSet:
         return per
 
 
+def measure_next_rows(moe, torch, wl, d, device, stream, l2, peak, seed, warmup):
+    """Per-call device time of the rows built after the step, each over its
+    own rotating buffer sets (enough sets that one rotation touches >= 2x L2,
+    up to 256), as graphs of back-to-back launches.  The expert buffers of
+    the combine and activation calls use the tight capacity (the largest
+    per-expert count): the rows read and written are the same, the padding
+    that no call touches is not allocated."""
+    import numpy as np
+    N, H, E, K, R, T, I = wl.N, wl.H, wl.E, wl.K, wl.R, wl.T, wl.inter
+    idx = d["topk_idx"]
+    cap_t = int(np.bincount(idx.ravel(), minlength=E).max())
+    nt, idx_m = inputs.ragged_batch(R, T, idx, E, seed=seed)
+    valid = int(nt.sum())
+    t = np.arange(N) % T
+    routed_m = int(((idx_m >= 0) & (t < np.repeat(nt, T))[:, None]).sum())
+    nb = next_row_bytes(wl, routed_m, valid)
+    calls = ["plan_masked", "combine_shared", "router_topk"]
+    if I and I % 128 == 0:
+        calls.append("silu_mul_quant")
+    i32 = dict(dtype=torch.int32, device=device)
+    sh_full = moe.make_shape(R, T, H, E, K, wl.cap)
+    sh_t = moe.make_shape(R, T, H, E, K, cap_t)
+    idx_d = torch.from_numpy(idx).to(device)
+
+    def n_sets(c):
+        return int(max(2, min(256, -(-2 * l2 // nb[c]))))
+
+    def planned(shape):
+        b = moe.Buffers(shape, device=device, expert_x=False, expert_y=False)
+        b.plan(idx_d, stream)
+        return b
+
+    def make_set(c, i):
+        if c == "plan_masked":
+            ws = torch.zeros(moe.workspace_size(sh_full), dtype=torch.uint8, device=device)
+            return dict(idx=torch.from_numpy(idx_m).to(device), nt=torch.from_numpy(nt).to(device),
+                        cnt=torch.empty(E, **i32), off=torch.empty((E, R + 1), **i32),
+                        slot=torch.empty((N, K), **i32), src=torch.empty((E, wl.cap), **i32), ws=ws)
+        if c == "combine_shared":
+            b = planned(sh_t)
+            return dict(b=b, ey=inputs.expert_outputs_device(E, cap_t, H, seed + i, device=device),
+                        sh=inputs.expert_outputs_device(1, N, H, seed + 100 + i, device=device)[0],
+                        w=torch.from_numpy(d["topk_weights"]).to(device),
+                        y=torch.empty((N, H), dtype=torch.bfloat16, device=device))
+        if c == "silu_mul_quant":
+            b = planned(sh_t)
+            return dict(b=b, h=inputs.gate_up_device(E, cap_t, I, seed + i, device=device),
+                        q=torch.empty((E, cap_t, I), dtype=torch.uint8, device=device),
+                        sc=torch.empty((E, cap_t, I // 128), dtype=torch.float32, device=device))
+        lg = inputs.router_logits(N, E, seed + i)
+        return dict(lg=torch.from_numpy(lg).to(device), idx=torch.empty((N, K), **i32),
+                    w=torch.empty((N, K), dtype=torch.float32, device=device))
+
+    def do(c, st_, x):
+        if c == "plan_masked":
+            moe.plan_masked(sh_full, x["idx"], x["nt"], x["cnt"], x["off"], x["slot"], x["src"],
+                            x["ws"], st_)
+        elif c == "combine_shared":
+            moe.combine_shared(sh_t, x["ey"], idx_d, x["b"].slot_of, x["w"], x["sh"], x["y"],
+                               x["b"].workspace, st_)
+        elif c == "silu_mul_quant":
+            moe.silu_mul_quant(sh_t, I, x["h"], x["b"].expert_num_tokens, x["q"], x["sc"],
+                               x["b"].workspace, st_)
+        else:
+            moe.router_topk(sh_full, x["lg"], x["idx"], x["w"], st_)
+
+    def status_ok(x):
+        ws = x.get("ws", x["b"].workspace if "b" in x else None)
+        return ws is None or moe.read_status(ws, stream) == moe.Status.OK
+
+    out = {}
+    for c in calls:
+        ns = n_sets(c)
+        with torch.cuda.stream(stream):
+            sets = [make_set(c, i) for i in range(ns)]
+            for _ in range(warmup):
+                for x in sets:
+                    do(c, stream, x)
+        stream.synchronize()
+        assert all(status_ok(x) for x in sets), c
+        reps = max(1, 24 // ns)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                for x in sets:
+                    do(c, torch.cuda.current_stream(device), x)
+        ts = []
+        with torch.cuda.stream(stream):
+            for it in range(3 + 5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                b.synchronize()
+                if it >= 3:
+                    ts.append(a.elapsed_time(b) / (reps * ns))
+        assert all(status_ok(x) for x in sets), c
+        us = 1e3 * statistics.median(ts)
+        rot = ns * nb[c]
+        out[c] = {"us": us, "bytes": nb[c], "gbs": nb[c] / (us * 1e-6) / 1e9,
+                  "frac_of_peak": nb[c] / (us * 1e-6) / 1e9 / peak, "sets": ns,
+                  "rotation_bytes": rot, "rotation_exceeds_l2": rot > l2}
+        del g, sets
+        torch.cuda.synchronize()
+    out["_config"] = {"capacity_for_expert_buffers": cap_t, "intermediate": I,
+                      "ragged_valid_tokens": valid, "masked_routed_entries": routed_m,
+                      "timing": "graph of back-to-back launches over the rotating sets; median of 5 replays"}
+    return out
+
+
 def run_gpu(args, wl):
     import torch
     import combine_moe_dispatch_gb300 as moe
@@ -475,6 +605,10 @@ def run_gpu(args, wl):
 
     # roofline of the dominant kernel
     peak, peak_kind = read_peaks()
+    next_rows = None
+    if not args.no_next_rows:
+        next_rows = measure_next_rows(moe, torch, wl, d, device, stream, l2, peak, args.seed,
+                                      args.warmup)
     means = {c: statistics.median(v) for c, v in per_call.items()}
     dom = max((c for c in calls), key=means.get)
     achieved = cb[dom] / (means[dom] * 1e-3) / 1e9
@@ -523,6 +657,7 @@ def run_gpu(args, wl):
             "roofline": roofline,
             "calls": calls_out,
             "dispatch_incl_plan": disp,
+            "next_rows": next_rows,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
@@ -546,6 +681,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the per-call timing of the masked plan, combine with the shared "
+                         "expert, activation and router")
     ap.add_argument("--only", default=None,
                     help="profiling: time only this call (plus the plan it needs); no e2e")
     ap.add_argument("--tight-capacity", action="store_true",

@@ -1,7 +1,9 @@
 """Build libmoe_gb300.so in-tree with nvcc for sm_103a (GB300).
 
-Each ``csrc/*.cu`` compiles to an object file in parallel, then nvcc links
-the shared library next to this file.  The CUDA runtime is linked
+A host generator (``csrc/silu_table_gen.cpp``, built with the system C++
+compiler) first writes the activation kernel's SiLU table into the build
+folder; then each ``csrc/*.cu`` compiles to an object file in parallel, and
+nvcc links the shared library next to this file.  The CUDA runtime is linked
 statically, so the library needs only the driver at run time.
 
     python -m combine_moe_dispatch_gb300.buildlib [--verbose-ptxas] [--force]
@@ -23,7 +25,9 @@ LIB = os.path.join(PKG, "libmoe_gb300.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=default",
-                 "-I", INCLUDE, "-I", CSRC]
+                 "-I", INCLUDE, "-I", CSRC, "-I", BUILD_DIR]
+TABLE_GEN = os.path.join(CSRC, "silu_table_gen.cpp")
+TABLE = os.path.join(BUILD_DIR, "silu_table.inc")
 
 
 def _sources():
@@ -32,7 +36,21 @@ def _sources():
 
 def _inputs():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
-        sorted(glob.glob(os.path.join(INCLUDE, "*.h")))
+        sorted(glob.glob(os.path.join(INCLUDE, "*.h"))) + [TABLE_GEN]
+
+
+def generate_table(cxx: str = "g++") -> str:
+    """Compile and run the SiLU table generator (plain IEEE binary32: no
+    fused contraction, no fast-math)."""
+    exe = os.path.join(BUILD_DIR, "silu_table_gen")
+    cmd = [cxx, "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-o", exe, TABLE_GEN]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"{cxx} failed on {TABLE_GEN}:\n{r.stdout}\n{r.stderr}")
+    r = subprocess.run([exe, TABLE], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"silu_table_gen failed:\n{r.stdout}\n{r.stderr}")
+    return TABLE
 
 
 def up_to_date() -> bool:
@@ -46,6 +64,7 @@ def build(force: bool = False, verbose_ptxas: bool = False, nvcc: str = "nvcc") 
     if not force and not verbose_ptxas and up_to_date():
         return LIB
     os.makedirs(BUILD_DIR, exist_ok=True)
+    generate_table()
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
 
     def compile_one(src):

@@ -11,50 +11,79 @@
 // graph whatever the routing (the pages: kernels must read the per-expert
 // counts rather than plan their work from the buffer sizes).
 //
-// SiLU(g) = g / (1 + e^-g) with e^x computed by a fixed sequence of IEEE
-// binary32 operations (Cody-Waite reduction with a two-part ln 2, a degree-7
-// Taylor polynomial in Horner form with fused multiply-adds, exact scaling by
-// 2^n), so that the result, and therefore every quantised byte, is
-// reproducible bit for bit on any implementation of the same steps.
+// SiLU(g) = g / (1 + e^-g) in binary32, with e^x by a fixed sequence of IEEE
+// operations (Cody-Waite reduction with a two-part ln 2, a degree-7 Taylor
+// polynomial by Horner with fused multiply-adds, exact scaling by 2^n), so
+// every byte is reproducible.  The gate is bf16, so SiLU(g) is a function of
+// 16 bits, and the kernel looks it up instead of evaluating it:
+//  * 2^-25 <= |g| < 128: a table of the 8192 values, generated at build time
+//    by silu_table_gen.cpp with that sequence and staged in shared memory;
+//  * |g| < 2^-25: e^-g rounds to exactly 1, so SiLU(g) = g / 2 = g * 0.5;
+//  * |g| >= 128: for g > 0, e^-g is below 2^-25 (or 0), so 1 + e^-g == 1 and
+//    SiLU(g) = g; for g < 0, e^-g = +inf and g / inf = -0, which g * 0 also
+//    gives (with NaN for g = -inf, as the division does).
+// The product with up and the quantisation are evaluated as written.
 //
-// How: persistent grid; each block scans the clamped counts into a prefix in
-// shared memory, then warps take (row, segment) tasks over the populated rows
-// only and find a task's expert by binary search.  A task is 1024 elements
-// of a (8 blocks of 128): each half-warp loads 8 gate and 8 up values per
-// lane (16-byte loads), computes a in registers and quantises its block.
-#include <math.h>
-
+// How: persistent grid; each block stages the table (before waiting on the
+// previous kernel, which it does not depend on) and scans the clamped counts
+// into a prefix in shared memory; then each warp takes a contiguous range of
+// (row, segment) tasks over the populated rows only (its first task's expert
+// by binary search, the next ones by walking forward).  A task is 2P blocks
+// of 128 elements: each half-warp loads 8 gate and 8 up values per lane per
+// block pair (16-byte loads), and the loads of a warp's next task are issued
+// before the current one is computed.  Each block's scale
+// and reciprocal are computed once, by the lane that stores the scale, and
+// handed to the half-warp that quantises the block by shuffle.
 #include "moe_common.cuh"
 
 namespace moe {
 
 constexpr int kActThreads = 256;
 constexpr unsigned kWarpAll = 0xFFFFFFFFu;
+constexpr int kSiluTabEntries = 8192;   // sign x 32 binades x 128 mantissas
+constexpr int kSiluTabE0 = 102;         // biased exponent of 2^-25
 
-// e^x; +inf above 88.72 and 0 below -87.33 (the steps of the file comment).
-__device__ __forceinline__ float exp_fixed(float x) {
-  const float xc = fminf(fmaxf(x, -87.33f), 88.72f);
-  const float n = rintf(__fmul_rn(xc, 1.44269502f));          // log2(e)
-  float r = __fmaf_rn(-n, 0.693145751953125f, xc);           // ln2, high 16 bits
-  r = __fmaf_rn(-n, 1.42860677e-06f, r);                     // ln2, low part
-  float p = 1.98412701e-04f;                                 // 1/7!
-  p = __fmaf_rn(p, r, 1.38888892e-03f);                      // 1/6!
-  p = __fmaf_rn(p, r, 8.33333377e-03f);                      // 1/5!
-  p = __fmaf_rn(p, r, 4.16666679e-02f);                      // 1/4!
-  p = __fmaf_rn(p, r, 1.66666672e-01f);                      // 1/3!
-  p = __fmaf_rn(p, r, 0.5f);
-  p = __fmaf_rn(p, r, 1.0f);
-  p = __fmaf_rn(p, r, 1.0f);
-  int ni = (int)n;
-  const bool big = ni > 127;                                 // 2^128 is not a float
-  p = big ? __fmul_rn(p, 2.0f) : p;
-  ni = big ? ni - 1 : ni;
-  const float v = __fmul_rn(p, __int_as_float((ni + 127) << 23));
-  return x > 88.72f ? __int_as_float(0x7F800000) : (x < -87.33f ? 0.0f : v);
+__device__ __align__(16) const uint32_t g_silu_table[kSiluTabEntries] = {
+#include "silu_table.inc"
+};
+
+// SiLU(g) for the bf16 pattern h (in the low 16 bits), every case of the
+// file comment.
+__device__ __forceinline__ float silu_bf16(uint32_t h, const float *s_tab) {
+  const float g = __uint_as_float(h << 16);
+  const int t = (int)(h & 0x7FFFu) - (kSiluTabE0 << 7);
+  const bool in_tab = (unsigned)t < (unsigned)(kSiluTabEntries / 2);
+  const float tab = s_tab[(in_tab ? (uint32_t)t : 0u) | ((h >> 15) << 12)];
+  const float small = __fmul_rn(g, 0.5f);
+  const float large = g > 0.0f ? g : __fmul_rn(g, 0.0f);
+  return in_tab ? tab : (t < 0 ? small : large);
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, exp_fixed(-g))), u);
+// SiLU of the 8 bf16 gates in gw (two per word, low half first).  Both
+// halves of a word are indexed at once: with the sign bits cleared, adding
+// 0x4D00 to each half (no carry can cross) maps the table's magnitudes
+// [102 << 7, 134 << 7) to [0x8000, 0x9000), so a half is in the table iff
+// its top nibble is 1000b, and its low 12 bits are the index.  Lanes look
+// the table up unconditionally (the index is masked into range) and the
+// warp takes the exact selects only if some lane met a gate outside it.
+__device__ __forceinline__ void silu8(const uint32_t (&gw)[4], const float *s_tab, float (&sv)[8]) {
+  uint32_t outside = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t d = (gw[i] & 0x7FFF7FFFu) + 0x4D004D00u;
+    outside |= d ^ 0x80008000u;
+    const uint32_t i0 = (d & 0xFFFu) | ((gw[i] >> 3) & 0x1000u);
+    const uint32_t i1 = ((d >> 16) & 0xFFFu) | ((gw[i] >> 19) & 0x1000u);
+    sv[2 * i] = s_tab[i0];
+    sv[2 * i + 1] = s_tab[i1];
+  }
+  if (__any_sync(kWarpAll, (outside & 0xF000F000u) != 0)) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      sv[2 * i] = silu_bf16(gw[i] & 0xFFFFu, s_tab);
+      sv[2 * i + 1] = silu_bf16(gw[i] >> 16, s_tab);
+    }
+  }
 }
 
 // Exclusive prefix of clamp(count[e], 0, cap) over e into out[0..E], by the
@@ -91,14 +120,44 @@ __device__ void count_prefix(const int32_t *count, int E, int cap, int32_t *out)
   __syncthreads();
 }
 
+// The expert whose populated rows hold row number rg: the last e with
+// prefix[e] <= rg.
+__device__ __forceinline__ int populated_expert(const int32_t *s_prefix, int E, int rg) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_prefix[mid] <= rg) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+template <int P>
+__device__ __forceinline__ void load_task(const ActParams &p, int64_t row, int seg, int half, int sub,
+                                          int nb, uint4 (&gv)[P], uint4 (&uv)[P]) {
+  const uint16_t *gate = p.expert_h + row * 2 * p.I;
+  const uint16_t *up = gate + p.I;
+#pragma unroll
+  for (int it = 0; it < P; ++it) {
+    const int blk = seg * 2 * P + it * 2 + half;
+    const int64_t off = (int64_t)blk * 128 + sub * 8;
+    gv[it] = blk < nb ? __ldcs(reinterpret_cast<const uint4 *>(gate + off)) : make_uint4(0, 0, 0, 0);
+    uv[it] = blk < nb ? __ldcs(reinterpret_cast<const uint4 *>(up + off)) : make_uint4(0, 0, 0, 0);
+  }
+}
+
 template <int P>
 __global__ void __launch_bounds__(kActThreads)
 silu_quant_kernel(ActParams p) {
-  extern __shared__ int32_t s_prefix[];                     // [E + 1]
+  extern __shared__ __align__(16) unsigned char s_raw[];
+  float *s_tab = reinterpret_cast<float *>(s_raw);                                  // [8192]
+  int32_t *s_prefix = reinterpret_cast<int32_t *>(s_raw + kSiluTabEntries * 4);    // [E + 1]
   __shared__ int32_t s_status;
+  for (int i = threadIdx.x; i < kSiluTabEntries / 4; i += kActThreads)
+    reinterpret_cast<uint4 *>(s_tab)[i] = __ldg(reinterpret_cast<const uint4 *>(g_silu_table) + i);
   pdl_wait_for_previous();
   if (threadIdx.x == 0) s_status = read_status(p.hdr);
-  count_prefix(p.expert_num_tokens, p.E, p.cap, s_prefix);
+  count_prefix(p.expert_num_tokens, p.E, p.cap, s_prefix);   // ends with __syncthreads
   if (s_status != MOE_OK) return;
 
   const int lane = threadIdx.x & 31;
@@ -109,62 +168,92 @@ silu_quant_kernel(ActParams p) {
   const int nb = p.I / 128;
   constexpr int bpt = 2 * P;
   const int tpr = (nb + bpt - 1) / bpt;
+  // each warp takes a contiguous range of (populated row, segment) tasks, so
+  // the row and its expert advance incrementally from one task to the next
   const int64_t ntasks = (int64_t)s_prefix[p.E] * tpr;
+  const int64_t per_warp = (ntasks + nwarps - 1) / nwarps;
+  int64_t task = warp0 * per_warp;
+  const int64_t task_end = min(ntasks, task + per_warp);
+  if (task >= task_end) return;
 
-  for (int64_t task = warp0; task < ntasks; task += nwarps) {
-    const int rg = (int)(task / tpr);
-    const int seg = (int)(task - (int64_t)rg * tpr);
-    int lo = 0, hi = p.E;                                   // last e with prefix[e] <= rg
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_prefix[mid] <= rg) lo = mid;
-      else hi = mid;
+  int rg = (int)(task / tpr);
+  int seg = (int)(task - (int64_t)rg * tpr);
+  int e = populated_expert(s_prefix, p.E, rg);
+  int64_t row = (int64_t)e * p.cap + (rg - s_prefix[e]);
+  uint4 gv[P], uv[P];
+  load_task<P>(p, row, seg, half, sub, nb, gv, uv);
+  for (;;) {
+    // the next task's loads go out before this task's arithmetic
+    const bool more = task + 1 < task_end;
+    int nseg = seg + 1, nrg = rg;
+    if (nseg == tpr) {
+      nseg = 0;
+      ++nrg;
+      while (e + 1 < p.E && s_prefix[e + 1] <= nrg) ++e;   // experts without rows are skipped
     }
-    const int64_t row = (int64_t)lo * p.cap + (rg - s_prefix[lo]);
-    const uint16_t *gate = p.expert_h + row * 2 * p.I;
-    const uint16_t *up = gate + p.I;
-    uint4 gv[P], uv[P];
+    const int64_t nrow = (int64_t)e * p.cap + (nrg - s_prefix[e]);
+    uint4 gn[P], un[P];
+    if (more) {
+      load_task<P>(p, nrow, nseg, half, sub, nb, gn, un);
+    } else {
 #pragma unroll
-    for (int it = 0; it < P; ++it) {
-      const int blk = seg * bpt + it * 2 + half;
-      const int64_t off = (int64_t)blk * 128 + sub * 8;
-      gv[it] = blk < nb ? __ldcs(reinterpret_cast<const uint4 *>(gate + off)) : make_uint4(0, 0, 0, 0);
-      uv[it] = blk < nb ? __ldcs(reinterpret_cast<const uint4 *>(up + off)) : make_uint4(0, 0, 0, 0);
+      for (int it = 0; it < P; ++it) gn[it] = un[it] = make_uint4(0, 0, 0, 0);
     }
-    float my_scale = 0.0f;
-    uint8_t *qrow = static_cast<uint8_t *>(p.act_q) + row * p.I;
+
+    float a[P][8], am[P];
 #pragma unroll
     for (int it = 0; it < P; ++it) {
       const uint32_t gw[4] = {gv[it].x, gv[it].y, gv[it].z, gv[it].w};
       const uint32_t uw[4] = {uv[it].x, uv[it].y, uv[it].z, uv[it].w};
-      float a[8];
+      float sv[8];
+      silu8(gw, s_tab, sv);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        a[2 * i] = silu_mul(bf16_lo(gw[i]), bf16_lo(uw[i]));
-        a[2 * i + 1] = silu_mul(bf16_hi(gw[i]), bf16_hi(uw[i]));
+        a[it][2 * i] = __fmul_rn(sv[2 * i], bf16_lo(uw[i]));
+        a[it][2 * i + 1] = __fmul_rn(sv[2 * i + 1], bf16_hi(uw[i]));
       }
-      float scale;
-      const uint2 q = quantise_block8(a, &scale);
+      am[it] = half_warp_amax(a[it]);
+    }
+    // lane L < 2P owns block seg*2P + L: amax from half L & 1 of pair L >> 1
+    float mine = 0.0f;
+#pragma unroll
+    for (int it = 0; it < P; ++it) {
+      const float v = __shfl_sync(kWarpAll, am[it], (lane & 1) * 16);
+      if ((lane >> 1) == it) mine = v;
+    }
+    const float my_scale = __fdiv_rn(mine, 448.0f);
+    const float my_r = mine == 0.0f ? 1.0f : __frcp_rn(my_scale);
+    uint8_t *qrow = static_cast<uint8_t *>(p.act_q) + row * p.I;
+#pragma unroll
+    for (int it = 0; it < P; ++it) {
+      const float scale = __shfl_sync(kWarpAll, my_scale, it * 2 + half);
+      const float r = __shfl_sync(kWarpAll, my_r, it * 2 + half);
+      const uint2 q = quant_bytes8(a[it], scale, r, am[it] == 0.0f);
       const int blk = seg * bpt + it * 2 + half;
       if (blk < nb) *reinterpret_cast<uint2 *>(qrow + (int64_t)blk * 128 + sub * 8) = q;
-      const float s_even = __shfl_sync(kWarpAll, scale, 0);
-      const float s_odd = __shfl_sync(kWarpAll, scale, 16);
-      if (lane == it * 2) my_scale = s_even;
-      if (lane == it * 2 + 1) my_scale = s_odd;
     }
     if (lane < min(bpt, nb - seg * bpt)) p.act_scale[row * nb + seg * bpt + lane] = my_scale;
+
+    if (!more) break;
+#pragma unroll
+    for (int it = 0; it < P; ++it) {
+      gv[it] = gn[it];
+      uv[it] = un[it];
+    }
+    row = nrow;
+    seg = nseg;
+    rg = nrg;
+    ++task;
   }
 }
 
 namespace {
 template <int P>
 cudaError_t launch_p(const ActParams &p, cudaStream_t stream) {
-  const size_t smem = (size_t)(p.E + 1) * sizeof(int32_t);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(silu_quant_kernel<P>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  const size_t smem = (size_t)kSiluTabEntries * 4 + (size_t)(p.E + 1) * sizeof(int32_t);
+  cudaError_t e = cudaFuncSetAttribute(silu_quant_kernel<P>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   // enough warps for every row of every expert at full capacity, capped at a full device
   const int64_t tasks = (int64_t)p.E * p.cap * ((p.I / 128 + 2 * P - 1) / (2 * P));
   const int grid = persistent_grid((const void *)silu_quant_kernel<P>, kActThreads, tasks);
@@ -178,14 +267,13 @@ cudaError_t launch_p(const ActParams &p, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, silu_quant_kernel<P>, p);
+  e = cudaLaunchKernelEx(&cfg, silu_quant_kernel<P>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_silu_quant(const ActParams &p, cudaStream_t stream) {
   const int nb = p.I / 128;
-  if (nb % 8 == 0) return launch_p<4>(p, stream);
   if (nb % 4 == 0) return launch_p<2>(p, stream);
   return launch_p<1>(p, stream);
 }

@@ -298,41 +298,42 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-__device__ __forceinline__ float nudge(float q, int ulps) {
-  return __int_as_float(__float_as_int(q) + ulps);
-}
-
 // Candidate bytes for e4m3(RN(a / s)), e4m3(RN(b / s)) from r = RN(1 / s):
-// returns true, with the bytes in *out, when q~ = RN(a * r) and its 4-ulp
-// neighbours round to the same bytes (see the file comment); false when the
-// pair needs the exact division.
+// returns true, with the bytes in *out, when q~ = RN(a * r) moved down and
+// up by a factor 1 -+ 2^-20 rounds to the same bytes (see quant_bytes8);
+// false when the pair needs the exact division.
 __device__ __forceinline__ bool quant_pair_fast(float a, float b, float r, uint32_t *out) {
   const float qa = __fmul_rn(a, r), qb = __fmul_rn(b, r);
-  const uint32_t lo = e4m3x2(nudge(qa, -4), nudge(qb, -4));
-  const uint32_t hi = e4m3x2(nudge(qa, 4), nudge(qb, 4));
+  const uint32_t lo = e4m3x2(__fmul_rn(qa, 1.0f - 0x1p-20f), __fmul_rn(qb, 1.0f - 0x1p-20f));
+  const uint32_t hi = e4m3x2(__fmul_rn(qa, 1.0f + 0x1p-20f), __fmul_rn(qb, 1.0f + 0x1p-20f));
   *out = lo;
   return lo == hi;
 }
 
-// One lane's 8 values of a 128-element block held by a half-warp (lanes
-// 0-15 one block, 16-31 the next): the block scale amax/448 (to *scale) and
-// the 8 E4M3 bytes e4m3(RN(x / scale)), an all-zero block giving 0.  All 32
-// lanes must call it together.  Exact division, cheaply: with r = RN(1/scale),
-// q~ = RN(x * r) is within 3 binary32 ulps of RN(x / scale) (two roundings of
-// 2^-24 plus half an ulp); rounding to E4M3 is monotone, so if q~ moved 4
-// ulps down and up rounds to one byte, that byte is exact.  Otherwise (next
-// to an E4M3 midpoint, a zero element, or 1/scale overflowing) the lane
-// divides with IEEE __fdiv_rn, behind a warp-wide vote so the division is a
-// real branch.
-__device__ __forceinline__ uint2 quantise_block8(const float (&f)[8], float *scale_out) {
+// Largest |x| of a 128-element block held by a half-warp, 8 values per lane
+// (lanes 0-15 one block, 16-31 the next); all 32 lanes call it together.
+__device__ __forceinline__ float half_warp_amax(const float (&f)[8]) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
   for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-  const float scale = __fdiv_rn(amax, 448.0f);
-  const bool zero = amax == 0.0f;
-  const float r = zero ? 1.0f : __frcp_rn(scale);
+  return amax;
+}
+
+// The 8 E4M3 bytes e4m3(RN(x / scale)) of one lane, given its block's scale,
+// r = RN(1 / scale) and whether the block's amax is 0 (all bytes 0).  All 32
+// lanes call it together.  Exact division, cheaply: q~ = RN(x * r) is within
+// 3 binary32 ulps of RN(x / scale) (two roundings of 2^-24 plus half an ulp).
+// Multiplying q~ by 1 -+ 2^-20 moves it by at least 4 ulps less half an ulp
+// of rounding, i.e. past that interval on both sides; rounding to E4M3 is
+// monotone, so if both ends round to one byte, that byte is exact.  (Below
+// the normal range, where the move may round away, every candidate is
+// smaller than the least E4M3 subnormal's half and rounds to a zero of the
+// same sign.)  Otherwise (next to an E4M3 midpoint, or 1/scale overflowing)
+// the lane divides with IEEE __fdiv_rn, behind a warp-wide vote so the
+// division is a real branch.
+__device__ __forceinline__ uint2 quant_bytes8(const float (&f)[8], float scale, float r, bool zero) {
   const bool r_ok = r <= 3.0e38f;
   uint32_t b4[4];
   bool sure = true;
@@ -346,9 +347,20 @@ __device__ __forceinline__ uint2 quantise_block8(const float (&f)[8], float *sca
         b4[i] = e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
     }
   }
-  *scale_out = scale;
   if (zero) return make_uint2(0u, 0u);
   return make_uint2(b4[0] | (b4[1] << 16), b4[2] | (b4[3] << 16));
+}
+
+// One lane's 8 values of a 128-element block held by a half-warp: the block
+// scale amax/448 (to *scale) and the lane's 8 E4M3 bytes, an all-zero block
+// giving 0.  All 32 lanes call it together.
+__device__ __forceinline__ uint2 quantise_block8(const float (&f)[8], float *scale_out) {
+  const float amax = half_warp_amax(f);
+  const float scale = __fdiv_rn(amax, 448.0f);
+  const bool zero = amax == 0.0f;
+  const float r = zero ? 1.0f : __frcp_rn(scale);
+  *scale_out = scale;
+  return quant_bytes8(f, scale, r, zero);
 }
 
 // The status the dispatch and combine kernels see; read once per block.

@@ -6,7 +6,7 @@ both the CUDA path and the CPU oracle can consume exactly the same bytes.
 
 Recipe (numpy ``default_rng``; one independent child stream per quantity,
 spawned from ``SeedSequence(seed)`` in the order x, routing, logits,
-expert outputs, gate/up projections):
+expert outputs, gate/up projections, ragged batches, router logits):
 
 * ``x``: N(0,1) in float32, rounded to bf16 by torch's CPU cast (round to
   nearest even).  Returned as ``uint16`` bit patterns.
@@ -24,6 +24,10 @@ expert outputs, gate/up projections):
 * expert outputs: N(0,1) rounded to bf16, like ``x``.
 * gate/up projections (the first expert GEMM's output, [E, cap, 2I]): the
   gate half N(0, 2^2), the up half N(0,1), rounded to bf16.
+* ragged batches: valid tokens per logical rank uniform in [T/2, T]; a
+  seeded fraction of the routed entries replaced by -1 (masked); the entries
+  of tokens beyond a rank's count hold arbitrary expert ids.
+* router logits [N, E]: N(0,1) in float32.
 """
 from __future__ import annotations
 
@@ -31,7 +35,7 @@ import numpy as np
 
 from .configs import Workload
 
-_STREAMS = ("x", "routing", "logits", "expert_y", "gate_up")
+_STREAMS = ("x", "routing", "logits", "expert_y", "gate_up", "ragged", "router")
 
 
 def _rng(seed: int, what: str) -> np.random.Generator:
@@ -108,13 +112,33 @@ def gate_up(E: int, cap: int, I: int, seed: int = 0) -> np.ndarray:
 
 
 def gate_up_device(E: int, cap: int, I: int, seed: int = 0, device="cuda"):
-    """As ``gate_up`` drawn on the device with a seeded torch generator."""
+    """As ``gate_up`` drawn on the device with a seeded torch generator
+    (bf16 N(0,1), the gate half then doubled: exact in bf16)."""
     import torch
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
-    z = torch.randn((E, cap, 2 * I), generator=gen, device=device, dtype=torch.float32)
-    z[..., :I] *= 2.0
-    return z.to(torch.bfloat16)
+    z = torch.randn((E, cap, 2 * I), generator=gen, device=device, dtype=torch.bfloat16)
+    z[..., :I] *= 2
+    return z
+
+
+def ragged_batch(R: int, T: int, topk_idx: np.ndarray, E: int, mask_frac: float = 1 / 32,
+                 seed: int = 0):
+    """(num_tokens[R] int32, topk_idx with masked and garbage entries)."""
+    rng = _rng(seed, "ragged")
+    nt = rng.integers(T // 2, T + 1, size=R).astype(np.int32)
+    idx = np.array(topk_idx, dtype=np.int32, copy=True)
+    K = idx.shape[1]
+    idx[rng.random(idx.shape) < mask_frac] = -1
+    t = np.arange(R * T) % T
+    beyond = t >= np.repeat(nt, T)
+    idx[beyond] = rng.integers(-(1 << 20), 1 << 20, size=(int(beyond.sum()), K)).astype(np.int32)
+    return nt, idx
+
+
+def router_logits(N: int, E: int, seed: int = 0) -> np.ndarray:
+    """logits[N, E] float32, N(0,1)."""
+    return _rng(seed, "router").standard_normal((N, E), dtype=np.float32)
 
 
 def make(wl: Workload, seed: int = 0) -> dict:

@@ -158,3 +158,27 @@ def test_silu_mul_quant_full_size_dsv3_decode():
     assert bool((q[~pop] == gpu_check.SENTINEL_BYTE).all())
     assert bool((sc[~pop] == gpu_check.SENTINEL_SCALE).all())
     assert moe.read_status(b.workspace) == moe.Status.OK
+
+
+def test_silu_mul_quant_every_bf16_gate():
+    """Every finite bf16 gate value, one binade per 128-element block (so
+    each block's scale is set by gates of one magnitude), with up = 1 and
+    up = -3: bytes and scales equal the oracle's.  NaN and infinite gates are
+    left out (the sign of a NaN is not defined across implementations)."""
+    import combine_moe_dispatch_gb300 as moe
+    I = 2048
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    pats[(pats & 0x7F80) == 0x7F80] = 0
+    gate = pats.reshape(-1, I)                                  # 32 rows
+    rows = []
+    for u in (1.0, -3.0):
+        up = np.full_like(gate, inputs.to_bf16_bits(np.array([u], np.float32))[0])
+        rows.append(np.concatenate([gate, up], axis=1))
+    h = np.concatenate(rows)[None]                              # [1, 64, 2I]
+    E, cap = 1, h.shape[1]
+    counts = np.array([cap], np.int32)
+    shape = moe.make_shape(1, 16, 256, E, 1, cap)
+    ws = _workspace(moe, shape)
+    q, sc = _buffers(E, cap, I)
+    moe.silu_mul_quant(shape, I, gpu_check.dev(h), gpu_check.dev(counts), q, sc, ws)
+    _check(moe, E, cap, I, h, counts, q, sc)
