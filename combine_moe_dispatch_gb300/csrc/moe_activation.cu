@@ -59,31 +59,39 @@ __device__ __forceinline__ float silu_bf16(uint32_t h, const float *s_tab) {
   return in_tab ? tab : (t < 0 ? small : large);
 }
 
-// SiLU of the 8 bf16 gates in gw (two per word, low half first).  Both
-// halves of a word are indexed at once: with the sign bits cleared, adding
-// 0x4D00 to each half (no carry can cross) maps the table's magnitudes
-// [102 << 7, 134 << 7) to [0x8000, 0x9000), so a half is in the table iff
-// its top nibble is 1000b, and its low 12 bits are the index.  Lanes look
-// the table up unconditionally (the index is masked into range) and the
-// warp takes the exact selects only if some lane met a gate outside it.
-__device__ __forceinline__ void silu8(const uint32_t (&gw)[4], const float *s_tab, float (&sv)[8]) {
-  uint32_t outside = 0;
+// Table lookups of SiLU for the 8 bf16 gates in gw (two per word, low half
+// first).  Both halves of a word are indexed at once: with the sign bits
+// cleared, adding 0x4D00 to each half (no carry can cross) maps the table's
+// magnitudes [102 << 7, 134 << 7) to [0x8000, 0x9000), so a half is in the
+// table iff its top nibble is 1000b, and its low 12 bits are the index (the
+// sign adds 4096).  The byte offset is masked into range, so every lookup is
+// in bounds; *outside collects the words a caller must redo exactly
+// (silu_bf16) when (*outside & 0xF000F000) != 0.
+__device__ __forceinline__ void silu8_table(const uint4 &g, const float *s_tab, float (&sv)[8],
+                                            uint32_t &outside) {
+  const unsigned char *tab = reinterpret_cast<const unsigned char *>(s_tab);
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t d = (gw[i] & 0x7FFF7FFFu) + 0x4D004D00u;
     outside |= d ^ 0x80008000u;
-    const uint32_t i0 = (d & 0xFFFu) | ((gw[i] >> 3) & 0x1000u);
-    const uint32_t i1 = ((d >> 16) & 0xFFFu) | ((gw[i] >> 19) & 0x1000u);
-    sv[2 * i] = s_tab[i0];
-    sv[2 * i + 1] = s_tab[i1];
+    const uint32_t o0 = ((d << 2) & 0x3FFCu) | ((gw[i] >> 1) & 0x4000u);
+    const uint32_t o1 = ((d >> 14) & 0x3FFCu) | ((gw[i] >> 17) & 0x4000u);
+    sv[2 * i] = *reinterpret_cast<const float *>(tab + o0);
+    sv[2 * i + 1] = *reinterpret_cast<const float *>(tab + o1);
   }
-  if (__any_sync(kWarpAll, (outside & 0xF000F000u) != 0)) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      sv[2 * i] = silu_bf16(gw[i] & 0xFFFFu, s_tab);
-      sv[2 * i + 1] = silu_bf16(gw[i] >> 16, s_tab);
-    }
-  }
+}
+
+// amax / 448 rounded to nearest: q0 = RN(amax * RN(1/448)), then one
+// correction with the exact remainder (the method for divisors known in
+// advance of Brisebarre, Muller and Raina, IEEE Trans. Computers 2004).
+// Checked against IEEE division for every binary32 amax in [2^-120, FLT_MAX];
+// smaller and non-finite amax (subnormal quotients, inf) take __fdiv_rn.
+__device__ __forceinline__ float div448_fast(float amax) {
+  const float y = 1.0f / 448.0f;
+  const float q0 = __fmul_rn(amax, y);
+  const float r = __fmaf_rn(-q0, 448.0f, amax);
+  return __fmaf_rn(r, y, q0);
 }
 
 // Exclusive prefix of clamp(count[e], 0, cap) over e into out[0..E], by the
@@ -132,26 +140,119 @@ __device__ __forceinline__ int populated_expert(const int32_t *s_prefix, int E, 
   return lo;
 }
 
-template <int P>
+// The 2P blocks of task (row, seg): lane (half, sub) loads elements
+// [blk * 128 + sub * 8, + 8) of block blk = seg * 2P + 2 * it + half of the
+// gate and the up half.  EXACT: the row is a whole number of tasks, so every
+// block exists; otherwise blocks past the row read as zeros.
+template <int P, bool EXACT>
 __device__ __forceinline__ void load_task(const ActParams &p, int64_t row, int seg, int half, int sub,
                                           int nb, uint4 (&gv)[P], uint4 (&uv)[P]) {
-  const uint16_t *gate = p.expert_h + row * 2 * p.I;
+  const uint16_t *gate = p.expert_h + row * 2 * p.I + (int64_t)seg * (2 * P * 128) + half * 128 + sub * 8;
   const uint16_t *up = gate + p.I;
 #pragma unroll
   for (int it = 0; it < P; ++it) {
-    const int blk = seg * 2 * P + it * 2 + half;
-    const int64_t off = (int64_t)blk * 128 + sub * 8;
-    gv[it] = blk < nb ? __ldcs(reinterpret_cast<const uint4 *>(gate + off)) : make_uint4(0, 0, 0, 0);
-    uv[it] = blk < nb ? __ldcs(reinterpret_cast<const uint4 *>(up + off)) : make_uint4(0, 0, 0, 0);
+    const bool ok = EXACT || seg * 2 * P + it * 2 + half < nb;
+    gv[it] = ok ? __ldcs(reinterpret_cast<const uint4 *>(gate + it * 256)) : make_uint4(0, 0, 0, 0);
+    uv[it] = ok ? __ldcs(reinterpret_cast<const uint4 *>(up + it * 256)) : make_uint4(0, 0, 0, 0);
   }
 }
 
-template <int P>
+// One task: SiLU(gate) * up for the 2P blocks in gv/uv, the block scales
+// (computed once each, by lanes 0 .. 2P-1, which also store them) and the
+// E4M3 bytes.  All 32 lanes call it together.
+template <int P, bool EXACT>
+__device__ __forceinline__ void act_task(const ActParams &p, const float *s_tab, int64_t row, int seg,
+                                         int lane, int nb, const uint4 (&gv)[P], const uint4 (&uv)[P]) {
+  const int half = lane >> 4;
+  const int sub = lane & 15;
+  constexpr int bpt = 2 * P;
+  float a[P][8];
+  uint32_t outside = 0;
+#pragma unroll
+  for (int it = 0; it < P; ++it) silu8_table(gv[it], s_tab, a[it], outside);
+  if (__any_sync(kWarpAll, (outside & 0xF000F000u) != 0)) {   // a gate outside the table: exact cases
+#pragma unroll
+    for (int it = 0; it < P; ++it) {
+      const uint32_t gw[4] = {gv[it].x, gv[it].y, gv[it].z, gv[it].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[it][2 * i] = silu_bf16(gw[i] & 0xFFFFu, s_tab);
+        a[it][2 * i + 1] = silu_bf16(gw[i] >> 16, s_tab);
+      }
+    }
+  }
+  float am[P];
+#pragma unroll
+  for (int it = 0; it < P; ++it) {
+    const uint32_t uw[4] = {uv[it].x, uv[it].y, uv[it].z, uv[it].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      a[it][2 * i] = __fmul_rn(a[it][2 * i], bf16_lo(uw[i]));
+      a[it][2 * i + 1] = __fmul_rn(a[it][2 * i + 1], bf16_hi(uw[i]));
+    }
+    am[it] = half_warp_amax(a[it]);
+  }
+  // lane L < 2P owns block seg*2P + L: amax from half L & 1 of pair L >> 1
+  float mine = 0.0f;
+#pragma unroll
+  for (int it = 0; it < P; ++it) {
+    const float v = __shfl_sync(kWarpAll, am[it], (lane & 1) * 16);
+    if ((lane >> 1) == it) mine = v;
+  }
+  float my_scale = div448_fast(mine);
+  const bool tiny = mine != 0.0f && !(mine >= 0x1p-120f && mine <= 3.4028234e38f);
+  if (__any_sync(kWarpAll, tiny)) {
+    if (tiny) my_scale = __fdiv_rn(mine, 448.0f);
+  }
+  const float my_r = mine == 0.0f ? 1.0f : __frcp_rn(my_scale);
+
+  // bytes from RN(a * r) where provably exact, else (one vote per task) by division
+  uint2 q[P];
+  bool slow = false;
+#pragma unroll
+  for (int it = 0; it < P; ++it) {
+    const float scale = __shfl_sync(kWarpAll, my_scale, it * 2 + half);
+    const float r = __shfl_sync(kWarpAll, my_r, it * 2 + half);
+    bool sure;
+    q[it] = quant_bytes8_fast(a[it], r, &sure);
+    if (am[it] == 0.0f) q[it] = make_uint2(0u, 0u);
+    else slow |= !(sure && r <= 3.0e38f);
+    (void)scale;
+  }
+  if (__any_sync(kWarpAll, slow)) {
+#pragma unroll
+    for (int it = 0; it < P; ++it) {
+      const float scale = __shfl_sync(kWarpAll, my_scale, it * 2 + half);
+      if (am[it] != 0.0f) q[it] = quant_bytes8_exact(a[it], scale);
+    }
+  }
+  uint8_t *qrow = static_cast<uint8_t *>(p.act_q) + row * p.I + (int64_t)seg * (bpt * 128) + half * 128 + sub * 8;
+#pragma unroll
+  for (int it = 0; it < P; ++it) {
+    if (EXACT || seg * bpt + it * 2 + half < nb) *reinterpret_cast<uint2 *>(qrow + it * 256) = q[it];
+  }
+  if (lane < min(bpt, nb - seg * bpt)) p.act_scale[row * nb + seg * bpt + lane] = my_scale;
+}
+
+// Walks a warp's contiguous range of (populated row, segment) tasks.
+struct ActCursor {
+  int64_t row;
+  int rg, seg, e;
+  __device__ __forceinline__ void next(const int32_t *s_prefix, int E, int cap, int tpr) {
+    if (++seg == tpr) {
+      seg = 0;
+      ++rg;
+      while (e + 1 < E && s_prefix[e + 1] <= rg) ++e;   // experts without rows are skipped
+    }
+    row = (int64_t)e * cap + (rg - s_prefix[e]);
+  }
+};
+
+template <int P, bool EXACT>
 __global__ void __launch_bounds__(kActThreads)
 silu_quant_kernel(ActParams p) {
-  extern __shared__ __align__(16) unsigned char s_raw[];
-  float *s_tab = reinterpret_cast<float *>(s_raw);                                  // [8192]
-  int32_t *s_prefix = reinterpret_cast<int32_t *>(s_raw + kSiluTabEntries * 4);    // [E + 1]
+  __shared__ __align__(16) float s_tab[kSiluTabEntries];
+  extern __shared__ __align__(16) int32_t s_prefix[];                  // [E + 1]
   __shared__ int32_t s_status;
   for (int i = threadIdx.x; i < kSiluTabEntries / 4; i += kActThreads)
     reinterpret_cast<uint4 *>(s_tab)[i] = __ldg(reinterpret_cast<const uint4 *>(g_silu_table) + i);
@@ -166,97 +267,46 @@ silu_quant_kernel(ActParams p) {
   const int64_t warp0 = ((int64_t)blockIdx.x * kActThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kActThreads) >> 5;
   const int nb = p.I / 128;
-  constexpr int bpt = 2 * P;
-  const int tpr = (nb + bpt - 1) / bpt;
-  // each warp takes a contiguous range of (populated row, segment) tasks, so
-  // the row and its expert advance incrementally from one task to the next
+  const int tpr = (nb + 2 * P - 1) / (2 * P);
+  // each warp takes a contiguous range of tasks, so the row and its expert
+  // advance incrementally from one task to the next
   const int64_t ntasks = (int64_t)s_prefix[p.E] * tpr;
   const int64_t per_warp = (ntasks + nwarps - 1) / nwarps;
-  int64_t task = warp0 * per_warp;
-  const int64_t task_end = min(ntasks, task + per_warp);
-  if (task >= task_end) return;
+  const int64_t t0 = warp0 * per_warp;
+  const int64_t t1 = min(ntasks, t0 + per_warp);
+  if (t0 >= t1) return;
+  int n = (int)(t1 - t0);                                    // tasks left, the current one included
 
-  int rg = (int)(task / tpr);
-  int seg = (int)(task - (int64_t)rg * tpr);
-  int e = populated_expert(s_prefix, p.E, rg);
-  int64_t row = (int64_t)e * p.cap + (rg - s_prefix[e]);
-  uint4 gv[P], uv[P];
-  load_task<P>(p, row, seg, half, sub, nb, gv, uv);
+  ActCursor c;
+  c.rg = (int)(t0 / tpr);
+  c.seg = (int)(t0 - (int64_t)c.rg * tpr);
+  c.e = populated_expert(s_prefix, p.E, c.rg);
+  c.row = (int64_t)c.e * p.cap + (c.rg - s_prefix[c.e]);
+  // two register buffers in turn: the next task's rows load while this one computes
+  uint4 ga[P], ua[P], gb[P], ub[P];
+  load_task<P, EXACT>(p, c.row, c.seg, half, sub, nb, ga, ua);
   for (;;) {
-    // the next task's loads go out before this task's arithmetic
-    const bool more = task + 1 < task_end;
-    int nseg = seg + 1, nrg = rg;
-    if (nseg == tpr) {
-      nseg = 0;
-      ++nrg;
-      while (e + 1 < p.E && s_prefix[e + 1] <= nrg) ++e;   // experts without rows are skipped
-    }
-    const int64_t nrow = (int64_t)e * p.cap + (nrg - s_prefix[e]);
-    uint4 gn[P], un[P];
-    if (more) {
-      load_task<P>(p, nrow, nseg, half, sub, nb, gn, un);
-    } else {
-#pragma unroll
-      for (int it = 0; it < P; ++it) gn[it] = un[it] = make_uint4(0, 0, 0, 0);
-    }
-
-    float a[P][8], am[P];
-#pragma unroll
-    for (int it = 0; it < P; ++it) {
-      const uint32_t gw[4] = {gv[it].x, gv[it].y, gv[it].z, gv[it].w};
-      const uint32_t uw[4] = {uv[it].x, uv[it].y, uv[it].z, uv[it].w};
-      float sv[8];
-      silu8(gw, s_tab, sv);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[it][2 * i] = __fmul_rn(sv[2 * i], bf16_lo(uw[i]));
-        a[it][2 * i + 1] = __fmul_rn(sv[2 * i + 1], bf16_hi(uw[i]));
-      }
-      am[it] = half_warp_amax(a[it]);
-    }
-    // lane L < 2P owns block seg*2P + L: amax from half L & 1 of pair L >> 1
-    float mine = 0.0f;
-#pragma unroll
-    for (int it = 0; it < P; ++it) {
-      const float v = __shfl_sync(kWarpAll, am[it], (lane & 1) * 16);
-      if ((lane >> 1) == it) mine = v;
-    }
-    const float my_scale = __fdiv_rn(mine, 448.0f);
-    const float my_r = mine == 0.0f ? 1.0f : __frcp_rn(my_scale);
-    uint8_t *qrow = static_cast<uint8_t *>(p.act_q) + row * p.I;
-#pragma unroll
-    for (int it = 0; it < P; ++it) {
-      const float scale = __shfl_sync(kWarpAll, my_scale, it * 2 + half);
-      const float r = __shfl_sync(kWarpAll, my_r, it * 2 + half);
-      const uint2 q = quant_bytes8(a[it], scale, r, am[it] == 0.0f);
-      const int blk = seg * bpt + it * 2 + half;
-      if (blk < nb) *reinterpret_cast<uint2 *>(qrow + (int64_t)blk * 128 + sub * 8) = q;
-    }
-    if (lane < min(bpt, nb - seg * bpt)) p.act_scale[row * nb + seg * bpt + lane] = my_scale;
-
-    if (!more) break;
-#pragma unroll
-    for (int it = 0; it < P; ++it) {
-      gv[it] = gn[it];
-      uv[it] = un[it];
-    }
-    row = nrow;
-    seg = nseg;
-    rg = nrg;
-    ++task;
+    ActCursor nc = c;
+    nc.next(s_prefix, p.E, p.cap, tpr);
+    if (n > 1) load_task<P, EXACT>(p, nc.row, nc.seg, half, sub, nb, gb, ub);
+    act_task<P, EXACT>(p, s_tab, c.row, c.seg, lane, nb, ga, ua);
+    if (--n == 0) break;
+    c = nc;
+    nc.next(s_prefix, p.E, p.cap, tpr);
+    if (n > 1) load_task<P, EXACT>(p, nc.row, nc.seg, half, sub, nb, ga, ua);
+    act_task<P, EXACT>(p, s_tab, c.row, c.seg, lane, nb, gb, ub);
+    if (--n == 0) break;
+    c = nc;
   }
 }
 
 namespace {
-template <int P>
+template <int P, bool EXACT>
 cudaError_t launch_p(const ActParams &p, cudaStream_t stream) {
-  const size_t smem = (size_t)kSiluTabEntries * 4 + (size_t)(p.E + 1) * sizeof(int32_t);
-  cudaError_t e = cudaFuncSetAttribute(silu_quant_kernel<P>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  const size_t smem = (size_t)(p.E + 1) * sizeof(int32_t);
   // enough warps for every row of every expert at full capacity, capped at a full device
   const int64_t tasks = (int64_t)p.E * p.cap * ((p.I / 128 + 2 * P - 1) / (2 * P));
-  const int grid = persistent_grid((const void *)silu_quant_kernel<P>, kActThreads, tasks);
+  const int grid = persistent_grid((const void *)silu_quant_kernel<P, EXACT>, kActThreads, tasks);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -267,15 +317,16 @@ cudaError_t launch_p(const ActParams &p, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, silu_quant_kernel<P>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, silu_quant_kernel<P, EXACT>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_silu_quant(const ActParams &p, cudaStream_t stream) {
   const int nb = p.I / 128;
-  if (nb % 4 == 0) return launch_p<2>(p, stream);
-  return launch_p<1>(p, stream);
+  if (nb % 4 == 0) return launch_p<2, true>(p, stream);
+  if (nb % 2 == 0) return launch_p<1, true>(p, stream);
+  return launch_p<1, false>(p, stream);
 }
 
 }  // namespace moe

@@ -3,7 +3,6 @@
 // few PTX helpers (acquire/release flags, the global timer).
 #pragma once
 
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -293,21 +292,18 @@ __device__ __forceinline__ void pdl_wait_for_previous() {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Two floats -> two E4M3 bytes (first in the low byte), nearest even, saturating.
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
-  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-}
-
-// Candidate bytes for e4m3(RN(a / s)), e4m3(RN(b / s)) from r = RN(1 / s):
-// returns true, with the bytes in *out, when q~ = RN(a * r) moved down and
-// up by a factor 1 -+ 2^-20 rounds to the same bytes (see quant_bytes8);
-// false when the pair needs the exact division.
-__device__ __forceinline__ bool quant_pair_fast(float a, float b, float r, uint32_t *out) {
-  const float qa = __fmul_rn(a, r), qb = __fmul_rn(b, r);
-  const uint32_t lo = e4m3x2(__fmul_rn(qa, 1.0f - 0x1p-20f), __fmul_rn(qb, 1.0f - 0x1p-20f));
-  const uint32_t hi = e4m3x2(__fmul_rn(qa, 1.0f + 0x1p-20f), __fmul_rn(qb, 1.0f + 0x1p-20f));
-  *out = lo;
-  return lo == hi;
+// Four floats -> four E4M3 bytes, the first in the low byte: round to
+// nearest even, finite overflow saturated to +-448 (cvt ... e4m3x2 puts its
+// first source operand in the upper byte).
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
 }
 
 // Largest |x| of a 128-element block held by a half-warp, 8 values per lane
@@ -321,34 +317,56 @@ __device__ __forceinline__ float half_warp_amax(const float (&f)[8]) {
   return amax;
 }
 
-// The 8 E4M3 bytes e4m3(RN(x / scale)) of one lane, given its block's scale,
-// r = RN(1 / scale) and whether the block's amax is 0 (all bytes 0).  All 32
-// lanes call it together.  Exact division, cheaply: q~ = RN(x * r) is within
+// The 8 E4M3 bytes e4m3(RN(x / scale)) of one lane as two little-endian
+// words, from r = RN(1 / scale); *sure tells whether they are provably
+// exact.  Exact division, cheaply: q~ = RN(x * r) is within
 // 3 binary32 ulps of RN(x / scale) (two roundings of 2^-24 plus half an ulp).
 // Multiplying q~ by 1 -+ 2^-20 moves it by at least 4 ulps less half an ulp
 // of rounding, i.e. past that interval on both sides; rounding to E4M3 is
 // monotone, so if both ends round to one byte, that byte is exact.  (Below
 // the normal range, where the move may round away, every candidate is
 // smaller than the least E4M3 subnormal's half and rounds to a zero of the
-// same sign.)  Otherwise (next to an E4M3 midpoint, or 1/scale overflowing)
-// the lane divides with IEEE __fdiv_rn, behind a warp-wide vote so the
-// division is a real branch.
+// same sign.)  Otherwise (next to an E4M3 midpoint, or 1/scale overflowing,
+// which the caller checks: r > 3e38) the lane must divide.
+__device__ __forceinline__ uint32_t quant_bytes4_fast(float a, float b, float c, float d, float r,
+                                                      bool &sure) {
+  const float qa = __fmul_rn(a, r), qb = __fmul_rn(b, r), qc = __fmul_rn(c, r), qd = __fmul_rn(d, r);
+  constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
+  const uint32_t lo = e4m3x4(__fmul_rn(qa, kDown), __fmul_rn(qb, kDown), __fmul_rn(qc, kDown),
+                             __fmul_rn(qd, kDown));
+  const uint32_t hi = e4m3x4(__fmul_rn(qa, kUp), __fmul_rn(qb, kUp), __fmul_rn(qc, kUp),
+                             __fmul_rn(qd, kUp));
+  sure = sure && lo == hi;
+  return lo;
+}
+
+__device__ __forceinline__ uint2 quant_bytes8_fast(const float (&f)[8], float r, bool *sure) {
+  bool ok = true;
+  const uint32_t x = quant_bytes4_fast(f[0], f[1], f[2], f[3], r, ok);
+  const uint32_t y = quant_bytes4_fast(f[4], f[5], f[6], f[7], r, ok);
+  *sure = ok;
+  return make_uint2(x, y);
+}
+
+// The same bytes by IEEE division.
+__device__ __forceinline__ uint2 quant_bytes8_exact(const float (&f)[8], float scale) {
+  return make_uint2(e4m3x4(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale), __fdiv_rn(f[2], scale),
+                           __fdiv_rn(f[3], scale)),
+                    e4m3x4(__fdiv_rn(f[4], scale), __fdiv_rn(f[5], scale), __fdiv_rn(f[6], scale),
+                           __fdiv_rn(f[7], scale)));
+}
+
+// Both, for one lane: the fast bytes where provably exact, else (behind a
+// warp-wide vote, all 32 lanes calling together) the divided ones; an
+// all-zero block (amax 0) gives 0.
 __device__ __forceinline__ uint2 quant_bytes8(const float (&f)[8], float scale, float r, bool zero) {
-  const bool r_ok = r <= 3.0e38f;
-  uint32_t b4[4];
-  bool sure = true;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) sure &= quant_pair_fast(f[2 * i], f[2 * i + 1], r, &b4[i]);
-  const bool slow = !zero && !(r_ok && sure);
+  bool sure;
+  uint2 out = quant_bytes8_fast(f, r, &sure);
+  const bool slow = !zero && !(r <= 3.0e38f && sure);
   if (__any_sync(0xFFFFFFFFu, slow)) {
-    if (slow) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        b4[i] = e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
-    }
+    if (slow) out = quant_bytes8_exact(f, scale);
   }
-  if (zero) return make_uint2(0u, 0u);
-  return make_uint2(b4[0] | (b4[1] << 16), b4[2] | (b4[3] << 16));
+  return zero ? make_uint2(0u, 0u) : out;
 }
 
 // One lane's 8 values of a 128-element block held by a half-warp: the block
