@@ -254,6 +254,7 @@ silu_quant_kernel(ActParams p) {
   __shared__ __align__(16) float s_tab[kSiluTabEntries];
   extern __shared__ __align__(16) int32_t s_prefix[];                  // [E + 1]
   __shared__ int32_t s_status;
+  pdl_allow_dependents();
   for (int i = threadIdx.x; i < kSiluTabEntries / 4; i += kActThreads)
     reinterpret_cast<uint4 *>(s_tab)[i] = __ldg(reinterpret_cast<const uint4 *>(g_silu_table) + i);
   pdl_wait_for_previous();

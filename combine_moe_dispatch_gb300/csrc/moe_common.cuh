@@ -274,12 +274,16 @@ __device__ __forceinline__ int ld_dsmem(const int32_t *local, uint32_t rank) {
   return v;
 }
 
-// Programmatic dependent launch.  moe_plan's kernels allow the next kernel in
-// the stream to be scheduled as soon as all their blocks have started; the
-// dispatch and combine kernels do work that needs nothing from the plan
-// (loading and quantising x) and then wait here until the previous kernel
-// has completed and its writes are visible.  Without a programmatic
-// dependency the wait returns at once.
+// Programmatic dependent launch.  The plan and activation kernels allow the
+// next kernel in the stream to be scheduled as soon as all their blocks have
+// started (measured: the dispatch, combine and router kernels ran slower
+// when their successors started early, so they do not), and every kernel but
+// the plan's is launched as such a dependent: it may do work that needs
+// nothing from the previous kernel (dispatch loads and quantises x rows; the
+// activation stages its table) and then waits here until the previous kernel
+// has completed and its writes are visible.  No kernel writes anything
+// before that wait.  Without a programmatic dependency the wait returns at
+// once.
 __device__ __forceinline__ void pdl_allow_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -159,6 +159,13 @@ moe_status moe_plan_masked(const moe_shape *shape, const int32_t *topk_idx,
  *       this call.  An entry whose expert or slot is out of range is skipped
  *       and sets the status word (BAD_EXPERT / CAPACITY); an entry with
  *       slot_of = -1 (not routed, see moe_plan_masked) is skipped silently.
+ * Ordering: the kernel is launched as a programmatic dependent of the
+ *       previous kernel in the stream (normally moe_plan's) and starts
+ *       loading x before that kernel has completed; it reads slot_of, the
+ *       routes and the status only after.  So x must not be written by the
+ *       kernel just before this call in the stream if that kernel lets its
+ *       dependents start early (griddepcontrol.launch_dependents); moe_plan
+ *       itself waits for every earlier kernel.
  * Host errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA. */
 moe_status moe_dispatch(const moe_shape *shape, const void *x,
                         const int32_t *topk_idx, const int32_t *slot_of,
