@@ -569,37 +569,55 @@ def run_gpu(args, wl):
                     cold[c].append(1e3 * a.elapsed_time(b))
     del flush
 
-    # e2e: pinned host inputs in, result out, copies inside the timed region
+    # e2e: pinned host inputs in, result out, copies inside the timed region.
+    # Each step is one CUDA-graph replay of the copies and the public calls;
+    # up to 3 steps are in flight on their own streams and buffer sets (a
+    # serving loop's pipelining), each with its own host output buffer.
     hx = torch.from_numpy(d["x"].view(np.int16)).pin_memory()
     hidx = torch.from_numpy(d["topk_idx"]).pin_memory()
     hw = torch.from_numpy(d["topk_weights"]).pin_memory()
-    hy = torch.empty((N, H), dtype=torch.int16).pin_memory()
-    hcnt = torch.empty(E, dtype=torch.int32).pin_memory()
+    n_inflight = min(3, nsets)
+    hys = [torch.empty((N, H), dtype=torch.int16).pin_memory() for _ in range(n_inflight)]
+    hcnts = [torch.empty(E, dtype=torch.int32).pin_memory() for _ in range(n_inflight)]
     h2d = hx.numel() * 2 + hidx.numel() * 4 + hw.numel() * 4
-    d2h = hy.numel() * 2 + hcnt.numel() * 4
+    d2h = hys[0].numel() * 2 + hcnts[0].numel() * 4
+    e2e_streams = [torch.cuda.Stream(device) for _ in range(n_inflight)]
 
-    def e2e_step(bs):
+    def e2e_step(bs, st, hy, hcnt):
         bs.x.view(torch.int16).copy_(hx, non_blocking=True)
         bs.idx.copy_(hidx, non_blocking=True)
         bs.w.copy_(hw, non_blocking=True)
         for c in calls:
-            bs.do(c, stream)
+            bs.do(c, st)
         hy.copy_(bs.b16.y.view(torch.int16), non_blocking=True)
         hcnt.copy_(bs.b16.expert_num_tokens, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for i in range(max(1, args.warmup)):
-            e2e_step(sets[i % nsets])
-        stream.synchronize()
-        barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for s in range(args.steps):
-            e2e_step(sets[s % nsets])
-        b.record(stream)
-        b.synchronize()
+    e2e_graphs = []
+    for i_, st in enumerate(e2e_streams):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            e2e_step(sets[i_], torch.cuda.current_stream(device), hys[i_], hcnts[i_])
+        e2e_graphs.append(g)
+    torch.cuda.synchronize()
+    for i_ in range(max(1, args.warmup) * n_inflight):
+        with torch.cuda.stream(e2e_streams[i_ % n_inflight]):
+            e2e_graphs[i_ % n_inflight].replay()
+    torch.cuda.synchronize()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for st in e2e_streams:
+        st.wait_stream(stream)
+    for s_ in range(args.steps):
+        with torch.cuda.stream(e2e_streams[s_ % n_inflight]):
+            e2e_graphs[s_ % n_inflight].replay()
+    for st in e2e_streams:
+        stream.wait_stream(st)
+    b.record(stream)
+    b.synchronize()
     barrier()
     assert moe.read_status(sets[0].b16.workspace, stream) == moe.Status.OK
+    y_ok = bool((hys[(args.steps - 1) % n_inflight] == sets[(args.steps - 1) % n_inflight].b16.y.view(torch.int16).cpu()).all())
     e2e_step_ms = max_over_ranks(a.elapsed_time(b) / args.steps, world, device)
     e2e_value = step_bytes * world / (e2e_step_ms * 1e-3) / 1e9
 
@@ -661,7 +679,11 @@ def run_gpu(args, wl):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
-                    "note": "eager public calls; expert_y stays resident on the device, as the expert GEMM leaves it"},
+                    "steps_in_flight": n_inflight, "result_read_back": y_ok,
+                    "note": ("every step copies x, topk_idx, topk_weights in from pinned host memory and "
+                             "y, expert_num_tokens out, around the public calls, as one CUDA-graph replay; "
+                             f"{n_inflight} steps in flight on their own streams and buffer sets; expert_y "
+                             "stays resident on the device, as the expert GEMM leaves it")},
             "gpu_launches": len(calls) * args.steps,
             "clocks": clk,
         }
