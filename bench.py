@@ -111,14 +111,24 @@ def read_peaks():
     return 6800.0, "fallback"
 
 
+def source_hash(kernel: str) -> str:
+    """First 16 hex digits of the SHA-256 of the kernel's source file and the
+    shared header it includes: a recorded DRAM count is used only while both
+    are unchanged."""
+    h = hashlib.sha256()
+    for rel in (KERNEL_SOURCES[kernel], "combine_moe_dispatch_gb300/csrc/moe_common.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, or None when the
     kernel's source changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.md")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = source_hash(kernel)
     pat = re.compile(r"^traffic\s+(\S+)\s+(\S+)\s+(\d+)\s+(\S+)")
     with open(path) as f:
         for line in f:
