@@ -271,7 +271,7 @@ def run_reference(args, wl):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.description, "sample": desc},
+        "config": {**workload_config(wl, wl.cap), "sample": desc},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": desc, "host": f"{os.cpu_count()} cores, {cpu_model()}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -284,7 +284,21 @@ def run_reference(args, wl):
 # the GPU path
 # ---------------------------------------------------------------------------
 
+def workload_config(wl, cap: int) -> dict:
+    """The config keys both arms report for a workload."""
+    return {"workload": wl.description, "name": wl.name, "ranks": wl.R, "tokens_per_rank": wl.T,
+            "hidden": wl.H, "experts": wl.E, "top_k": wl.K, "capacity": cap, "routing": wl.routing}
+
+
+def aggregate_value(step_bytes: float, world: int, step_ms: float) -> float:
+    """Whole-job GB/s: every replica moves step_bytes per step; the step time
+    is the slowest replica's."""
+    return step_bytes * world / (step_ms * 1e-3) / 1e9
+
+
 def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest value over the ranks of the default process group (the
+    slowest replica's time); the value itself when there is one rank."""
     if world <= 1:
         return value
     import torch
@@ -553,7 +567,7 @@ def run_gpu(args, wl):
     assert all(moe.read_status(bs.b16.workspace, stream) == moe.Status.OK for bs in sets)
 
     step_ms = max_over_ranks(step_ms, world, device)
-    value = step_bytes * world / (step_ms * 1e-3) / 1e9
+    value = aggregate_value(step_bytes, world, step_ms)
 
     if args.only:
         if rank == 0:
@@ -629,7 +643,7 @@ def run_gpu(args, wl):
     assert moe.read_status(sets[0].b16.workspace, stream) == moe.Status.OK
     y_ok = bool((hys[(args.steps - 1) % n_inflight] == sets[(args.steps - 1) % n_inflight].b16.y.view(torch.int16).cpu()).all())
     e2e_step_ms = max_over_ranks(a.elapsed_time(b) / args.steps, world, device)
-    e2e_value = step_bytes * world / (e2e_step_ms * 1e-3) / 1e9
+    e2e_value = aggregate_value(step_bytes, world, e2e_step_ms)
 
     # roofline of the dominant kernel
     peak, peak_kind = read_peaks()
@@ -670,9 +684,7 @@ def run_gpu(args, wl):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": wl.description, "name": wl.name, "ranks": R,
-                       "tokens_per_rank": T, "hidden": H, "experts": E, "top_k": K,
-                       "capacity": cap, "routing": wl.routing, "calls_per_step": calls,
+            "config": {**workload_config(wl, cap), "calls_per_step": calls,
                        "io": "bf16 activations and expert outputs, e4m3 + fp32 scales for the fp8 payload",
                        "l2": (f"no flush: inputs larger than L2 -- each step moves {step_bytes / 1e6:.0f} MB "
                               f"({step_bytes / l2:.1f}x L2) and the timed loop rotates through "
