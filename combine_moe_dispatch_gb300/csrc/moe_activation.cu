@@ -82,17 +82,6 @@ __device__ __forceinline__ void silu8_table(const uint4 &g, const float *s_tab, 
   }
 }
 
-// amax / 448 rounded to nearest: q0 = RN(amax * RN(1/448)), then one
-// correction with the exact remainder (the method for divisors known in
-// advance of Brisebarre, Muller and Raina, IEEE Trans. Computers 2004).
-// Checked against IEEE division for every binary32 amax in [2^-120, FLT_MAX];
-// smaller and non-finite amax (subnormal quotients, inf) take __fdiv_rn.
-__device__ __forceinline__ float div448_fast(float amax) {
-  const float y = 1.0f / 448.0f;
-  const float q0 = __fmul_rn(amax, y);
-  const float r = __fmaf_rn(-q0, 448.0f, amax);
-  return __fmaf_rn(r, y, q0);
-}
 
 // Exclusive prefix of clamp(count[e], 0, cap) over e into out[0..E], by the
 // whole block (any E).

@@ -373,6 +373,18 @@ __device__ __forceinline__ uint2 quant_bytes8(const float (&f)[8], float scale, 
   return zero ? make_uint2(0u, 0u) : out;
 }
 
+// amax / 448 rounded to nearest: q0 = RN(amax * RN(1/448)), then one
+// correction with the exact remainder (the method for divisors known in
+// advance of Brisebarre, Muller and Raina, IEEE Trans. Computers 2004).
+// Checked against IEEE division for every binary32 amax in [2^-120, FLT_MAX];
+// smaller and non-finite amax (subnormal quotients, inf) take __fdiv_rn.
+__device__ __forceinline__ float div448_fast(float amax) {
+  const float y = 1.0f / 448.0f;
+  const float q0 = __fmul_rn(amax, y);
+  const float r = __fmaf_rn(-q0, 448.0f, amax);
+  return __fmaf_rn(r, y, q0);
+}
+
 // One lane's 8 values of a 128-element block held by a half-warp: the block
 // scale amax/448 (to *scale) and the lane's 8 E4M3 bytes, an all-zero block
 // giving 0.  All 32 lanes call it together.

@@ -14,27 +14,29 @@
 // running (programmatic dependent launch): each warp loads its first task
 // and only then waits for the plan's slots.  Tasks are software-pipelined:
 // the next task's row and routing loads are in flight while this task's
-// stores are issued (and, for fp8, while it is quantised).  A warp takes one (token, segment) task at a time
-// from a grid sized to fill every SM; segments are chosen to divide the row
-// evenly (1024 elements for H = 7168 or 4096), so all tasks are equal.  Its
+// stores are issued (and, for fp8, while it is quantised).  A warp takes
+// one (token, segment) task at a time from a grid sized to fill every SM;
+// segments are chosen to divide the row evenly (1024 elements for H = 7168
+// or 4096), so all tasks are equal.  Its
 // lanes read the segment once with 16-byte loads (all loads issued before
-// any store), then write it K times with coalesced 16-byte (bf16) or 8-byte
-// (fp8) stores.  In the fp8 path each half-warp owns one 128-element block:
-// the absmax is a 4-step butterfly over 16 lanes, and the block's scale is
-// computed once and shared by all K copies; the segment's scales are
-// gathered into the first lanes and stored as one run per destination row.
+// any store), then write it K times with coalesced 16-byte stores.  In the
+// fp8 path each half-warp owns one 128-element block: the absmax is a 4-step
+// butterfly over 16 lanes, and the block's scale (amax/448, exactly rounded)
+// and its reciprocal are computed once, by the lane that stores the scale,
+// and shared by all K copies; neighbouring lanes swap 8-byte halves so every
+// store is 16 bytes.  The first task is read and quantised before waiting
+// for the plan, which it does not need.
 //
 // Exact division, cheaply: q must be e4m3(RN(x / scale)).  With r =
 // RN(1/scale), q~ = RN(x * r) is within 3 binary32 ulps of RN(x / scale)
 // (two roundings of 2^-24 each, plus half an ulp).  Rounding to E4M3 is
-// monotone, so if q~ moved 4 ulps down and 4 ulps up rounds to the same
-// byte, that byte is e4m3(RN(x / scale)); otherwise (a quotient next to an
-// E4M3 midpoint, or a zero) the lane divides its 8 elements with IEEE
-// __fdiv_rn, behind a warp-wide vote so that the division is a real branch
-// taken only when needed.  The result is bit-identical to dividing every
-// element.
+// monotone, so if q~ * (1 - 2^-20) and q~ * (1 + 2^-20), at least 3.5 ulps
+// either side, round to the same byte, that byte is e4m3(RN(x / scale));
+// otherwise (a quotient next to an E4M3 midpoint) the lane divides its 8
+// elements with IEEE __fdiv_rn, behind one warp-wide vote per task, so the
+// division is a real branch taken only when needed.  The result is
+// bit-identical to dividing every element.
 #include <cuda_bf16.h>
-#include <cuda_fp8.h>
 
 #include "moe_common.cuh"
 
@@ -74,14 +76,14 @@ __device__ __forceinline__ unsigned check_routes(const DispatchParams &p, const 
   return __ballot_sync(kFull, ok);
 }
 
-// Block-wide: wait for the plan (programmatic dependency), then read the
-// status word it left; false if the block must write nothing.
-__device__ __forceinline__ bool wait_plan_ok(const WsHeader *hdr) {
-  __shared__ int32_t s_status;
+// Per warp: wait for the plan (programmatic dependency), then read the
+// status word it left (one lane, broadcast); false if the warp must write
+// nothing.  No block barrier: each warp leaves its pre-wait work on its own.
+__device__ __forceinline__ bool wait_plan_ok(const WsHeader *hdr, int lane) {
   pdl_wait_for_previous();
-  if (threadIdx.x == 0) s_status = read_status(hdr);
-  __syncthreads();
-  return s_status == MOE_OK;
+  int32_t st = 0;
+  if (lane == 0) st = read_status(hdr);
+  return __shfl_sync(0xFFFFFFFFu, st, 0) == MOE_OK;
 }
 
 // bf16 copy; U 16-byte chunks per lane per task (a 256*U-element segment).
@@ -138,10 +140,10 @@ dispatch_bf16_kernel(DispatchParams p) {
 
   // The first task's read of x needs nothing from the plan: issue it before
   // waiting for the plan to finish.
-  Bf16Task<U> t;
-  if (warp0 < ntasks) bf16_load<U>(p, warp0, tpr, lane, t);
-  if (!wait_plan_ok(p.hdr)) return;
   if (warp0 >= ntasks) return;
+  Bf16Task<U> t;
+  bf16_load<U>(p, warp0, tpr, lane, t);
+  if (!wait_plan_ok(p.hdr, lane)) return;
   Routes r = load_routes(p, t.g, lane);
   // Software pipeline: the next task's loads go out before this task's stores.
   for (int64_t task = warp0; task < ntasks; task += nwarps) {
@@ -173,7 +175,8 @@ template <int P>
 struct Fp8Task {     // one task's output
   int64_t g;
   int seg;
-  uint2 q[P];
+  uint2 q[P];       // this lane's 8 bytes of block seg*2P + 2*it + half
+  uint4 w16[P / 2 > 0 ? P / 2 : 1];   // P even: 16 bytes per lane pair (see fp8_quantise)
   float my_scale;   // lane L < 2P holds the scale of block seg*2P + L
 };
 
@@ -193,12 +196,17 @@ __device__ __forceinline__ void fp8_load(const DispatchParams &p, int64_t task, 
   }
 }
 
-// Quantise one loaded task (needs nothing from the plan).
+// Quantise one loaded task (needs nothing from the plan).  Each block's
+// scale and reciprocal are computed once, by the lane that stores the scale
+// (lane L < 2P owns block seg*2P + L), and handed to the half-warp that
+// quantises the block by shuffle; the slow exact division is voted on once
+// per task.  All 32 lanes call it together.
 template <int P>
 __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Task<P> &t) {
+  const int half = lane >> 4;
   t.g = a.g;
   t.seg = a.seg;
-  t.my_scale = 0.0f;
+  float am[P];
 #pragma unroll
   for (int it = 0; it < P; ++it) {
     const uint32_t w[4] = {a.v[it].x, a.v[it].y, a.v[it].z, a.v[it].w};
@@ -208,14 +216,67 @@ __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Ta
       f[2 * i] = bf16_lo(w[i]);
       f[2 * i + 1] = bf16_hi(w[i]);
     }
-    float scale;
-    const uint2 q = quantise_block8(f, &scale);
-    const uint32_t lo = q.x, hi = q.y;
-    t.q[it] = make_uint2(lo, hi);
-    const float s_even = __shfl_sync(kFull, scale, 0);
-    const float s_odd = __shfl_sync(kFull, scale, 16);
-    if (lane == it * 2) t.my_scale = s_even;
-    if (lane == it * 2 + 1) t.my_scale = s_odd;
+    am[it] = half_warp_amax(f);
+  }
+  float mine = 0.0f;
+#pragma unroll
+  for (int it = 0; it < P; ++it) {
+    const float v = __shfl_sync(kFull, am[it], (lane & 1) * 16);
+    if ((lane >> 1) == it) mine = v;
+  }
+  float my_scale = div448_fast(mine);
+  const bool odd = mine != 0.0f && !(mine >= 0x1p-120f && mine <= 3.4028234e38f);
+  if (__any_sync(kFull, odd)) {
+    if (odd) my_scale = __fdiv_rn(mine, 448.0f);
+  }
+  const float my_r = mine == 0.0f ? 1.0f : __frcp_rn(my_scale);
+  t.my_scale = my_scale;
+  bool slow = false;
+#pragma unroll
+  for (int it = 0; it < P; ++it) {
+    const uint32_t w[4] = {a.v[it].x, a.v[it].y, a.v[it].z, a.v[it].w};
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = bf16_lo(w[i]);
+      f[2 * i + 1] = bf16_hi(w[i]);
+    }
+    const float r = __shfl_sync(kFull, my_r, it * 2 + half);
+    bool sure;
+    t.q[it] = quant_bytes8_fast(f, r, &sure);
+    if (am[it] == 0.0f) t.q[it] = make_uint2(0u, 0u);
+    else slow |= !(sure && r <= 3.0e38f);
+  }
+  if (__any_sync(kFull, slow)) {
+#pragma unroll
+    for (int it = 0; it < P; ++it) {
+      const float scale = __shfl_sync(kFull, my_scale, it * 2 + half);
+      if (am[it] != 0.0f) {
+        const uint32_t w[4] = {a.v[it].x, a.v[it].y, a.v[it].z, a.v[it].w};
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          f[2 * i] = bf16_lo(w[i]);
+          f[2 * i + 1] = bf16_hi(w[i]);
+        }
+        t.q[it] = quant_bytes8_exact(f, scale);
+      }
+    }
+  }
+  // Pair neighbouring lanes for 16-byte stores: for each pair of iterations
+  // (2j, 2j+1), the even lane of a pair gets iteration 2j's bytes of both
+  // lanes and the odd lane iteration 2j+1's.
+  if constexpr (P % 2 == 0) {
+#pragma unroll
+    for (int j = 0; j < P / 2; ++j) {
+      const bool even = (lane & 1) == 0;
+      const uint2 give = even ? t.q[2 * j + 1] : t.q[2 * j];
+      uint2 got;
+      got.x = __shfl_xor_sync(kFull, give.x, 1);
+      got.y = __shfl_xor_sync(kFull, give.y, 1);
+      const uint2 keep = even ? t.q[2 * j] : t.q[2 * j + 1];
+      t.w16[j] = even ? make_uint4(keep.x, keep.y, got.x, got.y) : make_uint4(got.x, got.y, keep.x, keep.y);
+    }
   }
 }
 
@@ -235,17 +296,28 @@ __device__ __forceinline__ void fp8_store(const DispatchParams &p, int lane, con
     if (!((okmask >> k) & 1u)) continue;
     const int64_t row = (int64_t)e * p.cap + s;
     uint8_t *dst = static_cast<uint8_t *>(p.expert_x) + row * p.H;
+    if constexpr (P % 2 == 0) {
+      // lane pair (sub & ~1, sub | 1) writes 16 bytes at (sub & ~1) * 8 of
+      // block 2j (even lane) or 2j + 1 (odd lane) of its half
 #pragma unroll
-    for (int it = 0; it < P; ++it) {
-      const int blk = t.seg * bpt + it * 2 + half;
-      if (blk < nb) *reinterpret_cast<uint2 *>(dst + (int64_t)blk * 128 + sub * 8) = t.q[it];
+      for (int j = 0; j < P / 2; ++j) {
+        const int blk = t.seg * bpt + (2 * j + (lane & 1)) * 2 + half;
+        if (blk < nb)
+          *reinterpret_cast<uint4 *>(dst + (int64_t)blk * 128 + (sub & ~1) * 8) = t.w16[j];
+      }
+    } else {
+#pragma unroll
+      for (int it = 0; it < P; ++it) {
+        const int blk = t.seg * bpt + it * 2 + half;
+        if (blk < nb) *reinterpret_cast<uint2 *>(dst + (int64_t)blk * 128 + sub * 8) = t.q[it];
+      }
     }
     if (lane < nscale) p.expert_x_scale[row * nb + t.seg * bpt + lane] = t.my_scale;
   }
 }
 
 template <int P>
-__global__ void __launch_bounds__(kDispatchThreads)
+__global__ void __launch_bounds__(kDispatchThreads, P >= 4 ? 3 : 1)
 dispatch_fp8_kernel(DispatchParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * kDispatchThreads + threadIdx.x) >> 5;
@@ -254,17 +326,17 @@ dispatch_fp8_kernel(DispatchParams p) {
   const int tpr = (nb + 2 * P - 1) / (2 * P);
   const int64_t ntasks = (int64_t)p.N * tpr;
 
-  // The first task's read of x needs nothing from the plan: issue it before
-  // waiting for the plan to finish.  Then software-pipeline the tasks: the
-  // next task's x and routing loads are issued before this task's stores,
-  // and it is quantised while those stores drain.
-  Fp8Raw<P> a;
-  if (warp0 < ntasks) fp8_load<P>(p, warp0, tpr, lane, a);
-  if (!wait_plan_ok(p.hdr)) return;
+  // The first task's read and quantisation of x need nothing from the plan:
+  // they run before waiting for the plan to finish.  Then software-pipeline
+  // the tasks: the next task's x and routing loads are issued before this
+  // task's stores, and it is quantised while those stores drain.
   if (warp0 >= ntasks) return;
-  Routes r = load_routes(p, a.g, lane);
+  Fp8Raw<P> a;
+  fp8_load<P>(p, warp0, tpr, lane, a);
   Fp8Task<P> t;
   fp8_quantise<P>(a, lane, t);
+  if (!wait_plan_ok(p.hdr, lane)) return;
+  Routes r = load_routes(p, a.g, lane);
   for (int64_t task = warp0; task < ntasks; task += nwarps) {
     const int64_t next = task + nwarps;
     const bool more = next < ntasks;
@@ -296,17 +368,27 @@ cudaError_t launch_tasks(void (*kern)(DispatchParams), int64_t warp_tasks, const
 #ifndef MOE_MAX_UNITS
 #define MOE_MAX_UNITS 4
 #endif
-int pick_units(int units_per_row) {
+int pick_units(int units_per_row, int max_units) {
   for (int u : {4, 2, 1})
-    if (u <= MOE_MAX_UNITS && units_per_row % u == 0) return u;
-  return MOE_MAX_UNITS;
+    if (u <= max_units && units_per_row % u == 0) return u;
+  return max_units;
 }
+
+// The fp8 path takes up to 4 block pairs per task, with the kernel held to
+// 3 resident blocks per SM (80 registers): unbounded it needs 90 and runs 2
+// blocks per SM.  Measured at DeepSeek-V3 decode, alternating builds: 4
+// pairs at 3 blocks 14.8 us alone and 18.8 us after the plan; 2 pairs
+// 16.9 and 21.2 us.
+#ifndef MOE_FP8_MAX_PAIRS
+#define MOE_FP8_MAX_PAIRS 4
+#endif
+constexpr int kFp8MaxPairs = MOE_MAX_UNITS < MOE_FP8_MAX_PAIRS ? MOE_MAX_UNITS : MOE_FP8_MAX_PAIRS;
 
 }  // namespace
 
 cudaError_t launch_dispatch_bf16(const DispatchParams &p, cudaStream_t stream) {
   const int cpr = p.H / 8;
-  const int U = (cpr % 32 == 0) ? pick_units(cpr / 32) : MOE_MAX_UNITS;
+  const int U = (cpr % 32 == 0) ? pick_units(cpr / 32, MOE_MAX_UNITS) : MOE_MAX_UNITS;
   const int64_t tasks = (int64_t)p.N * ((cpr + 32 * U - 1) / (32 * U));
   switch (U) {
     case 1: return launch_tasks(dispatch_bf16_kernel<1>, tasks, p, stream);
@@ -317,13 +399,10 @@ cudaError_t launch_dispatch_bf16(const DispatchParams &p, cudaStream_t stream) {
 
 cudaError_t launch_dispatch_fp8(const DispatchParams &p, cudaStream_t stream) {
   const int nb = p.H / 128;
-  const int P = (nb % 2 == 0) ? pick_units(nb / 2) : MOE_MAX_UNITS;
+  const int P = (nb % 2 == 0) ? pick_units(nb / 2, kFp8MaxPairs) : kFp8MaxPairs;
   const int64_t tasks = (int64_t)p.N * ((nb + 2 * P - 1) / (2 * P));
-  switch (P) {
-    case 1: return launch_tasks(dispatch_fp8_kernel<1>, tasks, p, stream);
-    case 2: return launch_tasks(dispatch_fp8_kernel<2>, tasks, p, stream);
-    default: return launch_tasks(dispatch_fp8_kernel<4>, tasks, p, stream);
-  }
+  if (P == 1) return launch_tasks(dispatch_fp8_kernel<1>, tasks, p, stream);
+  return launch_tasks(dispatch_fp8_kernel<kFp8MaxPairs>, tasks, p, stream);
 }
 
 }  // namespace moe
