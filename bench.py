@@ -647,6 +647,11 @@ def run_gpu(args, wl):
 
     # roofline of the dominant kernel
     peak, peak_kind = read_peaks()
+    # the step's buffers are no longer needed: free them before the rows
+    # beyond the step allocate theirs
+    del step_graphs, call_graphs, e2e_graphs, sets, bs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     next_rows = None
     if not args.no_next_rows:
         next_rows = measure_next_rows(moe, torch, wl, d, device, stream, l2, peak, args.seed,

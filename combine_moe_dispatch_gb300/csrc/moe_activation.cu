@@ -195,26 +195,17 @@ __device__ __forceinline__ void act_task(const ActParams &p, const float *s_tab,
   }
   const float my_r = mine == 0.0f ? 1.0f : __frcp_rn(my_scale);
 
-  // bytes from RN(a * r) where provably exact, else (one vote per task) by division
+  // bytes from RN(a * r) where provably exact, else by division (per element)
   uint2 q[P];
-  bool slow = false;
+  float scale[P], r[P];
+  bool zero[P];
 #pragma unroll
   for (int it = 0; it < P; ++it) {
-    const float scale = __shfl_sync(kWarpAll, my_scale, it * 2 + half);
-    const float r = __shfl_sync(kWarpAll, my_r, it * 2 + half);
-    bool sure;
-    q[it] = quant_bytes8_fast(a[it], r, &sure);
-    if (am[it] == 0.0f) q[it] = make_uint2(0u, 0u);
-    else slow |= !(sure && r <= 3.0e38f);
-    (void)scale;
+    scale[it] = __shfl_sync(kWarpAll, my_scale, it * 2 + half);
+    r[it] = __shfl_sync(kWarpAll, my_r, it * 2 + half);
+    zero[it] = am[it] == 0.0f;
   }
-  if (__any_sync(kWarpAll, slow)) {
-#pragma unroll
-    for (int it = 0; it < P; ++it) {
-      const float scale = __shfl_sync(kWarpAll, my_scale, it * 2 + half);
-      if (am[it] != 0.0f) q[it] = quant_bytes8_exact(a[it], scale);
-    }
-  }
+  quantise_blocks<P>(a, scale, r, zero, q);
   uint8_t *qrow = static_cast<uint8_t *>(p.act_q) + row * p.I + (int64_t)seg * (bpt * 128) + half * 128 + sub * 8;
 #pragma unroll
   for (int it = 0; it < P; ++it) {
@@ -238,7 +229,7 @@ struct ActCursor {
 };
 
 template <int P, bool EXACT>
-__global__ void __launch_bounds__(kActThreads)
+__global__ void __launch_bounds__(kActThreads, P >= 2 ? 3 : 1)
 silu_quant_kernel(ActParams p) {
   __shared__ __align__(16) float s_tab[kSiluTabEntries];
   extern __shared__ __align__(16) int32_t s_prefix[];                  // [E + 1]

@@ -322,37 +322,20 @@ __device__ __forceinline__ float half_warp_amax(const float (&f)[8]) {
 }
 
 // The 8 E4M3 bytes e4m3(RN(x / scale)) of one lane as two little-endian
-// words, from r = RN(1 / scale); *sure tells whether they are provably
-// exact.  Exact division, cheaply: q~ = RN(x * r) is within
-// 3 binary32 ulps of RN(x / scale) (two roundings of 2^-24 plus half an ulp).
-// Multiplying q~ by 1 -+ 2^-20 moves it by at least 4 ulps less half an ulp
-// of rounding, i.e. past that interval on both sides; rounding to E4M3 is
-// monotone, so if both ends round to one byte, that byte is exact.  (Below
-// the normal range, where the move may round away, every candidate is
-// smaller than the least E4M3 subnormal's half and rounds to a zero of the
-// same sign.)  Otherwise (next to an E4M3 midpoint, or 1/scale overflowing,
-// which the caller checks: r > 3e38) the lane must divide.
-__device__ __forceinline__ uint32_t quant_bytes4_fast(float a, float b, float c, float d, float r,
-                                                      bool &sure) {
-  const float qa = __fmul_rn(a, r), qb = __fmul_rn(b, r), qc = __fmul_rn(c, r), qd = __fmul_rn(d, r);
-  constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
-  const uint32_t lo = e4m3x4(__fmul_rn(qa, kDown), __fmul_rn(qb, kDown), __fmul_rn(qc, kDown),
-                             __fmul_rn(qd, kDown));
-  const uint32_t hi = e4m3x4(__fmul_rn(qa, kUp), __fmul_rn(qb, kUp), __fmul_rn(qc, kUp),
-                             __fmul_rn(qd, kUp));
-  sure = sure && lo == hi;
-  return lo;
-}
+// words, exact, from r = RN(1 / scale) and an IEEE division only where
+// needed.  q~ = RN(x * r) is within 3 binary32 ulps of RN(x / scale) (two
+// roundings of 2^-24 plus half an ulp).  Multiplying q~ by 1 -+ 2^-20 moves
+// it by at least 4 ulps less half an ulp of rounding, i.e. past that
+// interval on both sides; rounding to E4M3 is monotone, so where both ends
+// give the same byte, that byte is exact.  (Below the normal range, where the
+// move may round away, every candidate is smaller than the least E4M3
+// subnormal's half and rounds to a zero of the same sign.)  Where the two
+// ends differ -- a quotient next to an E4M3 midpoint, which bf16 inputs hit
+// for about 1 element in 200 -- that element alone is divided with IEEE
+// __fdiv_rn.  If 1/scale overflows (r > 3e38) every element is divided.
+__device__ __forceinline__ uint32_t e4m3_byte(float v) { return e4m3x4(v, 0.0f, 0.0f, 0.0f) & 0xFFu; }
 
-__device__ __forceinline__ uint2 quant_bytes8_fast(const float (&f)[8], float r, bool *sure) {
-  bool ok = true;
-  const uint32_t x = quant_bytes4_fast(f[0], f[1], f[2], f[3], r, ok);
-  const uint32_t y = quant_bytes4_fast(f[4], f[5], f[6], f[7], r, ok);
-  *sure = ok;
-  return make_uint2(x, y);
-}
-
-// The same bytes by IEEE division.
+// The bytes by IEEE division of every element.
 __device__ __forceinline__ uint2 quant_bytes8_exact(const float (&f)[8], float scale) {
   return make_uint2(e4m3x4(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale), __fdiv_rn(f[2], scale),
                            __fdiv_rn(f[3], scale)),
@@ -360,17 +343,79 @@ __device__ __forceinline__ uint2 quant_bytes8_exact(const float (&f)[8], float s
                            __fdiv_rn(f[7], scale)));
 }
 
-// Both, for one lane: the fast bytes where provably exact, else (behind a
-// warp-wide vote, all 32 lanes calling together) the divided ones; an
-// all-zero block (amax 0) gives 0.
+// Fast E4M3 words of 4 values: lo from q~ * (1 - 2^-20), hi from
+// q~ * (1 + 2^-20); a byte is exact where lo and hi agree.
+__device__ __forceinline__ void quant_window4(float a, float b, float c, float d, float r, uint32_t &lo,
+                                              uint32_t &hi) {
+  const float qa = __fmul_rn(a, r), qb = __fmul_rn(b, r), qc = __fmul_rn(c, r), qd = __fmul_rn(d, r);
+  constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
+  lo = e4m3x4(__fmul_rn(qa, kDown), __fmul_rn(qb, kDown), __fmul_rn(qc, kDown), __fmul_rn(qd, kDown));
+  hi = e4m3x4(__fmul_rn(qa, kUp), __fmul_rn(qb, kUp), __fmul_rn(qc, kUp), __fmul_rn(qd, kUp));
+}
+
+// Replace the bytes of lo where lo and hi differ by the divided ones.
+__device__ __forceinline__ uint32_t quant_patch4(uint32_t lo, uint32_t hi, float a, float b, float c,
+                                                 float d, float scale) {
+  const uint32_t diff = lo ^ hi;
+  if (diff & 0x000000FFu) lo = (lo & 0xFFFFFF00u) | e4m3_byte(__fdiv_rn(a, scale));
+  if (diff & 0x0000FF00u) lo = (lo & 0xFFFF00FFu) | (e4m3_byte(__fdiv_rn(b, scale)) << 8);
+  if (diff & 0x00FF0000u) lo = (lo & 0xFF00FFFFu) | (e4m3_byte(__fdiv_rn(c, scale)) << 16);
+  if (diff & 0xFF000000u) lo = (lo & 0x00FFFFFFu) | (e4m3_byte(__fdiv_rn(d, scale)) << 24);
+  return lo;
+}
+
+// One lane's 8 bytes of a block with the given scale and r = RN(1/scale)
+// (zero: the block's amax is 0, all bytes 0): the window bytes, each byte
+// whose window ends disagree divided on its own, per lane, without a vote.
+// For bf16 inputs, where such bytes turn up in most warps' tasks.
 __device__ __forceinline__ uint2 quant_bytes8(const float (&f)[8], float scale, float r, bool zero) {
-  bool sure;
-  uint2 out = quant_bytes8_fast(f, r, &sure);
-  const bool slow = !zero && !(r <= 3.0e38f && sure);
-  if (__any_sync(0xFFFFFFFFu, slow)) {
-    if (slow) out = quant_bytes8_exact(f, scale);
+  if (zero) return make_uint2(0u, 0u);
+  if (!(r <= 3.0e38f)) return quant_bytes8_exact(f, scale);
+  uint2 q;
+  uint32_t h0, h1;
+  quant_window4(f[0], f[1], f[2], f[3], r, q.x, h0);
+  quant_window4(f[4], f[5], f[6], f[7], r, q.y, h1);
+  if (q.x != h0) q.x = quant_patch4(q.x, h0, f[0], f[1], f[2], f[3], scale);
+  if (q.y != h1) q.y = quant_patch4(q.y, h1, f[4], f[5], f[6], f[7], scale);
+  return q;
+}
+
+// A lane's P blocks of 8 values (block it: scale[it], r[it] = RN(1/scale),
+// zero[it]: its amax is 0) to E4M3 bytes, exact: the window bytes, then, if
+// any lane of the warp has a byte whose window ends disagree (one vote),
+// each such byte alone divided.  1/scale overflowing (r > 3e38) divides the
+// whole block.  For fp32 inputs, where such bytes are rare enough that one
+// vote per task beats a branch per word.  All 32 lanes call it together.
+template <int P>
+__device__ __forceinline__ void quantise_blocks(const float (&f)[P][8], const float (&scale)[P],
+                                                const float (&r)[P], const bool (&zero)[P],
+                                                uint2 (&q)[P]) {
+  uint32_t hi[P][2];
+  bool any = false;
+#pragma unroll
+  for (int it = 0; it < P; ++it) {
+    if (zero[it]) {
+      q[it] = make_uint2(0u, 0u);
+      hi[it][0] = hi[it][1] = 0u;
+    } else if (!(r[it] <= 3.0e38f)) {
+      q[it] = quant_bytes8_exact(f[it], scale[it]);
+      hi[it][0] = q[it].x;
+      hi[it][1] = q[it].y;
+    } else {
+      quant_window4(f[it][0], f[it][1], f[it][2], f[it][3], r[it], q[it].x, hi[it][0]);
+      quant_window4(f[it][4], f[it][5], f[it][6], f[it][7], r[it], q[it].y, hi[it][1]);
+      any |= (q[it].x != hi[it][0]) | (q[it].y != hi[it][1]);
+    }
   }
-  return zero ? make_uint2(0u, 0u) : out;
+  if (__any_sync(0xFFFFFFFFu, any)) {
+#pragma unroll
+    for (int it = 0; it < P; ++it) {
+      if (q[it].x != hi[it][0])
+        q[it].x = quant_patch4(q[it].x, hi[it][0], f[it][0], f[it][1], f[it][2], f[it][3], scale[it]);
+      if (q[it].y != hi[it][1])
+        q[it].y = quant_patch4(q[it].y, hi[it][1], f[it][4], f[it][5], f[it][6], f[it][7], scale[it]);
+    }
+  }
 }
 
 // amax / 448 rounded to nearest: q0 = RN(amax * RN(1/448)), then one
@@ -385,17 +430,6 @@ __device__ __forceinline__ float div448_fast(float amax) {
   return __fmaf_rn(r, y, q0);
 }
 
-// One lane's 8 values of a 128-element block held by a half-warp: the block
-// scale amax/448 (to *scale) and the lane's 8 E4M3 bytes, an all-zero block
-// giving 0.  All 32 lanes call it together.
-__device__ __forceinline__ uint2 quantise_block8(const float (&f)[8], float *scale_out) {
-  const float amax = half_warp_amax(f);
-  const float scale = __fdiv_rn(amax, 448.0f);
-  const bool zero = amax == 0.0f;
-  const float r = zero ? 1.0f : __frcp_rn(scale);
-  *scale_out = scale;
-  return quant_bytes8(f, scale, r, zero);
-}
 
 // The status the dispatch and combine kernels see; read once per block.
 __device__ __forceinline__ int32_t read_status(const WsHeader *hdr) {

@@ -32,10 +32,9 @@
 // (two roundings of 2^-24 each, plus half an ulp).  Rounding to E4M3 is
 // monotone, so if q~ * (1 - 2^-20) and q~ * (1 + 2^-20), at least 3.5 ulps
 // either side, round to the same byte, that byte is e4m3(RN(x / scale));
-// otherwise (a quotient next to an E4M3 midpoint) the lane divides its 8
-// elements with IEEE __fdiv_rn, behind one warp-wide vote per task, so the
-// division is a real branch taken only when needed.  The result is
-// bit-identical to dividing every element.
+// otherwise (a quotient next to an E4M3 midpoint, about 1 element in 200
+// for bf16 inputs) that element alone is divided with IEEE __fdiv_rn.  The
+// result is bit-identical to dividing every element.
 #include <cuda_bf16.h>
 
 #include "moe_common.cuh"
@@ -199,8 +198,7 @@ __device__ __forceinline__ void fp8_load(const DispatchParams &p, int64_t task, 
 // Quantise one loaded task (needs nothing from the plan).  Each block's
 // scale and reciprocal are computed once, by the lane that stores the scale
 // (lane L < 2P owns block seg*2P + L), and handed to the half-warp that
-// quantises the block by shuffle; the slow exact division is voted on once
-// per task.  All 32 lanes call it together.
+// quantises the block by shuffle.  All 32 lanes call it together.
 template <int P>
 __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Task<P> &t) {
   const int half = lane >> 4;
@@ -231,7 +229,6 @@ __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Ta
   }
   const float my_r = mine == 0.0f ? 1.0f : __frcp_rn(my_scale);
   t.my_scale = my_scale;
-  bool slow = false;
 #pragma unroll
   for (int it = 0; it < P; ++it) {
     const uint32_t w[4] = {a.v[it].x, a.v[it].y, a.v[it].z, a.v[it].w};
@@ -241,27 +238,9 @@ __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Ta
       f[2 * i] = bf16_lo(w[i]);
       f[2 * i + 1] = bf16_hi(w[i]);
     }
+    const float scale = __shfl_sync(kFull, my_scale, it * 2 + half);
     const float r = __shfl_sync(kFull, my_r, it * 2 + half);
-    bool sure;
-    t.q[it] = quant_bytes8_fast(f, r, &sure);
-    if (am[it] == 0.0f) t.q[it] = make_uint2(0u, 0u);
-    else slow |= !(sure && r <= 3.0e38f);
-  }
-  if (__any_sync(kFull, slow)) {
-#pragma unroll
-    for (int it = 0; it < P; ++it) {
-      const float scale = __shfl_sync(kFull, my_scale, it * 2 + half);
-      if (am[it] != 0.0f) {
-        const uint32_t w[4] = {a.v[it].x, a.v[it].y, a.v[it].z, a.v[it].w};
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          f[2 * i] = bf16_lo(w[i]);
-          f[2 * i + 1] = bf16_hi(w[i]);
-        }
-        t.q[it] = quant_bytes8_exact(f, scale);
-      }
-    }
+    t.q[it] = quant_bytes8(f, scale, r, am[it] == 0.0f);
   }
   // Pair neighbouring lanes for 16-byte stores: for each pair of iterations
   // (2j, 2j+1), the even lane of a pair gets iteration 2j's bytes of both
