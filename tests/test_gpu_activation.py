@@ -182,3 +182,35 @@ def test_silu_mul_quant_every_bf16_gate():
     q, sc = _buffers(E, cap, I)
     moe.silu_mul_quant(shape, I, gpu_check.dev(h), gpu_check.dev(counts), q, sc, ws)
     _check(moe, E, cap, I, h, counts, q, sc)
+
+
+def test_silu_mul_quant_midpoint_rich_rows():
+    """Gates >= 128 have SiLU(g) = g exactly; with up values of 1 to 3
+    significant bits, a = g * up keeps few significant bits, and like bf16
+    activations its quotients a / scale land next to an E4M3 rounding
+    midpoint often (the kernel then divides those bytes alone).  The rows are
+    checked to contain such bytes, and the kernel's output against the
+    oracle."""
+    import combine_moe_dispatch_gb300 as moe
+    import oracle
+    rng = np.random.default_rng(17)
+    E, cap, I = 3, 16, 1024
+    g = inputs.to_bf16_bits(rng.uniform(128, 4096, (E, cap, I)).astype(np.float32))
+    coarse = np.array([0.5, 0.75, 1.0, 1.25, 1.5, 2.0, 3.0], np.float32)
+    u = inputs.to_bf16_bits((rng.choice(coarse, (E, cap, I)) *
+                             rng.choice([-1.0, 1.0], (E, cap, I))).astype(np.float32))
+    h = np.concatenate([g, u], axis=2)
+    counts = np.array([cap, 9, cap], np.int32)
+    # how often the window test is undecided, emulated in binary32 on the host
+    a = (oracle.bf16_to_f32(g) * oracle.bf16_to_f32(u)).astype(np.float32).reshape(-1, 128)
+    amax = np.abs(a).max(axis=1)
+    r = (np.float32(1) / (amax / np.float32(448)).astype(np.float32)).astype(np.float32)
+    q = (a * r[:, None]).astype(np.float32)
+    lo = oracle.f32_to_e4m3((q * np.float32(1 - 2**-20)).astype(np.float32))
+    hi = oracle.f32_to_e4m3((q * np.float32(1 + 2**-20)).astype(np.float32))
+    assert (lo != hi).sum() > 50, "the rows must exercise the per-byte division"
+    shape = moe.make_shape(1, 16, 256, E, 1, cap)
+    ws = _workspace(moe, shape)
+    qd, sc = _buffers(E, cap, I)
+    moe.silu_mul_quant(shape, I, gpu_check.dev(h), gpu_check.dev(counts), qd, sc, ws)
+    _check(moe, E, cap, I, h, counts, qd, sc)
