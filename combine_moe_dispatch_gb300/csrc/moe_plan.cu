@@ -266,16 +266,22 @@ __global__ void __launch_bounds__(kClusterWarps * 32)
 plan_cluster_kernel(PlanParams p) {
   extern __shared__ int32_t smem[];
   const int E = p.E;
+  // CTA c owns experts [c * rows, (c + 1) * rows): it gathers every CTA's
+  // counts of them, hands each CTA its base, and writes their counts and
+  // offsets rows.
+  const int rows = (E + (int)gridDim.x - 1) / (int)gridDim.x;
   int32_t *wc = smem;                             // [16][E] warp counters -> warp bases
-  int32_t *s_tab = smem + kClusterWarps * E;      // [ncta][E] CTA histograms, row c from CTA c
-  int32_t *s_base = s_tab + kClusterMaxCtas * E;  // [E] exclusive prefix of this CTA
+  int32_t *s_hist = wc + kClusterWarps * E;       // [E] this CTA's histogram
+  int32_t *s_base = s_hist + E;                   // [E] this CTA's base (written by the owners)
   int32_t *s_eoff = s_base + E;                   // [E] this CTA's entries before expert e
-  int32_t *s_stage = s_eoff + E;                  // [2][16*32*8] (entry id, expert) in slot order
+  int32_t *s_own = s_eoff + E;                    // [ncta][rows] owned experts' counts, row c from CTA c
+  int32_t *s_tot = s_own + kClusterMaxCtas * rows;   // [rows] owned experts' totals
+  int32_t *s_stage = s_tot + rows;                // [2][16*32*8] (entry id, expert) in slot order
   int32_t *s_offs = s_stage + 2 * kClusterWarps * 32 * kClusterMaxBatches;
-                                                  // [R][rows] rank-start prefixes of this CTA's rows
-  const int rows = (E + (int)gridDim.x - 1) / (int)gridDim.x;   // offsets rows (experts) per CTA
-  __shared__ int32_t s_err[kClusterMaxCtas];      // error bits, entry c from CTA c
-  __shared__ int32_t s_cta_err, s_final;
+                                                  // [R][rows] rank-start prefixes of owned experts
+  __shared__ int32_t s_err[kClusterMaxCtas];      // last CTA: bad-expert bits, entry c from CTA c
+  __shared__ int32_t s_cap[kClusterMaxCtas];      // last CTA: capacity bits, entry c from owner c
+  __shared__ int32_t s_cta_err, s_cta_cap;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -310,7 +316,10 @@ plan_cluster_kernel(PlanParams p) {
     e_in[b] = (b < p.batches && pl < routed_ent) ? __ldg(p.topk_idx + ent0 + pl) : -1;
   }
   for (int i = tid; i < kClusterWarps * E; i += nthreads) wc[i] = 0;
-  if (tid == 0) s_cta_err = 0;
+  if (tid == 0) {
+    s_cta_err = 0;
+    s_cta_cap = 0;
+  }
   int32_t my_err = 0;
   __syncthreads();
 
@@ -354,38 +363,69 @@ plan_cluster_kernel(PlanParams p) {
 #pragma unroll
     for (int w = 0; w < kClusterWarps; ++w) {
       const int cw = c[w];
-      c[w] = run;                                  // c[] now holds the exclusive prefixes
-      wc[w * E + e] = run;
+      wc[w * E + e] = run;                         // exclusive prefix over the CTA's warps
       run += cw;
     }
-    // 3a. push the CTA histogram into row `cta` of every CTA's table, and
-    //     the in-CTA prefix of every chunk that starts a rank to the last CTA
-    for (uint32_t q = 0; q < ncta; ++q) st_dsmem(s_tab + (int)cta * E + e, q, run);
+    s_hist[e] = run;
+    // 3a. to the owner of e: this CTA's count of e, and the in-CTA prefix
+    //     of every chunk of this CTA that starts a rank
+    const uint32_t owner = (uint32_t)(e / rows);
+    const int oe = e - (int)owner * rows;
+    st_dsmem(s_own + (int)cta * rows + oe, owner, run);
     for (int w = first_rank_warp; w < kClusterWarps; w += p.chunks_per_rank) {
       const int ch = (int)cta * kClusterWarps + w;
       if (ch >= p.num_chunks) break;
-      st_dsmem(s_offs + (ch / p.chunks_per_rank) * rows + e % rows, e / rows, wc[w * E + e]);
+      st_dsmem(s_offs + (ch / p.chunks_per_rank) * rows + oe, owner, wc[w * E + e]);
     }
   }
-  if (tid == 0)
-    for (uint32_t q = 0; q < ncta; ++q) st_dsmem(s_err + cta, q, s_cta_err);
-
-  // 3b. one cluster barrier: every table is complete and visible locally
-  cluster_barrier();
+  if (tid == 0) st_dsmem(s_err + cta, ncta - 1, s_cta_err);
   const bool last = cta == ncta - 1;
-  int32_t err = 0;
-  for (int e = tid; e < E; e += nthreads) {
-    int b = 0, tot = 0;
+
+  // 3b. cluster barrier (every owner gets its experts' counts from every
+  //     CTA), with this CTA's own scan, which needs nothing from the peers,
+  //     between the two halves
+  cluster_arrive_release();
+  const int n_cta = block_exclusive_scan(s_hist, s_eoff, E);
+  cluster_wait_acquire();
+
+  // 3c. owners: each CTA's base for the owned experts (pushed to that CTA),
+  //     the totals (counts), the capacity check, and the offsets rows
+  const int e0 = (int)cta * rows, e1 = min(E, e0 + rows);
+  int32_t cap_err = 0;
+  for (int e = e0 + tid; e < e1; e += nthreads) {
+    int run = 0;
     for (uint32_t c = 0; c < ncta; ++c) {
-      const int h = s_tab[(int)c * E + e];
-      b += (c < cta) ? h : 0;
-      tot += h;
+      const int h = s_own[(int)c * rows + (e - e0)];
+      s_own[(int)c * rows + (e - e0)] = run;       // exclusive over CTAs
+      st_dsmem(s_base + e, c, run);
+      run += h;
     }
-    s_base[e] = b;
-    if (last && tot > p.cap) err |= (int32_t)kErrCapacity;
+    p.expert_num_tokens[e] = run;
+    s_tot[e - e0] = run;
+    if (run > p.cap) cap_err = (int32_t)kErrCapacity;
   }
-  if (last && tid < (int)ncta) err |= s_err[tid];
-  const int n_cta = block_exclusive_scan(s_tab + (int)cta * E, s_eoff, E);
+  cap_err = __reduce_or_sync(0xFFFFFFFFu, cap_err);
+  if (lane == 0 && cap_err) atomicOr(&s_cta_cap, cap_err);
+  __syncthreads();                                 // s_own, s_tot, s_cta_cap complete
+  if (tid == 0) st_dsmem(s_cap + cta, ncta - 1, s_cta_cap);
+  // 3d. cluster barrier (every CTA gets its bases for all experts, the last
+  //     CTA every error bit; no remote access follows), with the owned
+  //     offsets rows, which need nothing from the peers, between the halves
+  cluster_arrive_release();
+  {
+    // offsets[e][r] = (counts of the CTAs before the one where rank r
+    // starts) + (in-CTA prefix pushed by that CTA); rows [e0, e1) of the
+    // matrix, one contiguous run
+    const int R1 = p.R + 1;
+    for (int i = tid; i < (e1 - e0) * R1; i += nthreads) {
+      const int e = e0 + i / R1, rr = i % R1;
+      const int cr = (rr * p.chunks_per_rank) / kClusterWarps;   // CTA where rank rr starts
+      p.expert_rank_offsets[(int64_t)e0 * R1 + i] =
+          rr == p.R ? s_tot[e - e0] : s_own[cr * rows + (e - e0)] + s_offs[rr * rows + (e - e0)];
+    }
+  }
+
+  cluster_wait_acquire();
 
   // 4. slots; return addresses staged in (expert, slot) order so that the
   //    src_of rows go out as contiguous runs
@@ -412,40 +452,12 @@ plan_cluster_kernel(PlanParams p) {
     const int slot = s_base[e] + (i - s_eoff[e]);
     if (slot < p.cap) p.src_of[(int64_t)e * p.cap + slot] = stage_v[i];
   }
-  // offsets[e][r] = (histograms of the CTAs before the one where rank r
-  // starts) + (in-CTA prefix pushed by that CTA).  This CTA writes rows
-  // [e0, e1) of the matrix, one contiguous run, and their counts.
-  __syncthreads();                                   // s_base / s_tab are reused below
-  {
-    const int e0 = (int)cta * rows, e1 = min(E, e0 + rows);
-    for (int e = e0 + tid; e < e1; e += nthreads) {
-      int run = 0;
-      for (uint32_t c = 0; c < ncta; ++c) {
-        const int h = s_tab[(int)c * E + e];
-        s_tab[(int)c * E + e] = run;                 // exclusive over CTAs (rows e0..e1 only)
-        run += h;
-      }
-      p.expert_num_tokens[e] = run;
-      s_base[e] = run;                               // the total (this CTA's slots are done)
-    }
-    __syncthreads();
-    const int R1 = p.R + 1;
-    for (int i = tid; i < (e1 - e0) * R1; i += nthreads) {
-      const int e = e0 + i / R1, rr = i % R1;
-      const int cr = (rr * p.chunks_per_rank) / kClusterWarps;   // CTA where rank rr starts
-      p.expert_rank_offsets[(int64_t)e0 * R1 + i] =
-          rr == p.R ? s_base[e] : s_tab[cr * E + e] + s_offs[rr * rows + (e - e0)];
-    }
-  }
   if (last) {
+    int32_t err = tid < (int)ncta ? (s_err[tid] | s_cap[tid]) : 0;
     err = __reduce_or_sync(0xFFFFFFFFu, err);
-    if (tid == 0) s_final = 0;
-    __syncthreads();
-    if (lane == 0 && err) atomicOr(&s_final, err);
-    __syncthreads();
     if (tid == 0)
-      p.hdr->status = (s_final & kErrBadExpert) ? MOE_ERR_BAD_EXPERT
-                      : (s_final & kErrCapacity) ? MOE_ERR_CAPACITY : MOE_OK;
+      p.hdr->status = (err & kErrBadExpert) ? MOE_ERR_BAD_EXPERT
+                      : (err & kErrCapacity) ? MOE_ERR_CAPACITY : MOE_OK;
   }
 }
 
@@ -551,9 +563,10 @@ cudaError_t launch_plan(const PlanParams &p_in, cudaStream_t stream) {
   PlanParams p = p_in;
   if (cluster_geometry(p)) {
     const int ctas = (p.num_chunks + kClusterWarps - 1) / kClusterWarps;
-    const size_t csmem = ((size_t)(kClusterWarps + kClusterMaxCtas + 2) * p.E +
-                          (size_t)p.R * ((p.E + ctas - 1) / ctas) +
-                          2 * kClusterWarps * 32 * kClusterMaxBatches) * sizeof(int32_t);
+    const size_t rows = (size_t)((p.E + ctas - 1) / ctas);
+    const size_t csmem = ((size_t)(kClusterWarps + 3) * p.E + (kClusterMaxCtas + 1) * rows +
+                          (size_t)p.R * rows + 2 * kClusterWarps * 32 * kClusterMaxBatches) *
+                         sizeof(int32_t);
     bool fits = false;
     cudaError_t e = csmem <= kClusterMaxSmem ? cluster_fits(ctas, csmem, &fits) : cudaSuccess;
     if (e != cudaSuccess) return e;
