@@ -163,10 +163,24 @@ cudaError_t launch_variant(const CombineParams &p, cudaStream_t stream) {
 }
 }  // namespace
 
+// Chunks per lane and resident blocks per SM, by K.  Measured (graphs of
+// back-to-back launches over rotating buffer sets): Mixtral (K = 2) 2 chunks
+// at 4 blocks 18.5 us, 4 at 3 18.7, 4 at 2 20.2, 1 at 8 19.8; DeepSeek-V3
+// decode (K = 8) 2 at 2 21.4 us, 1 at 4 23.4, 2 at 3 29.5.
+#ifndef MOE_COMBINE_U2
+#define MOE_COMBINE_U2 2
+#endif
+#ifndef MOE_COMBINE_MINB2
+#define MOE_COMBINE_MINB2 4
+#endif
+#ifndef MOE_COMBINE_MINB8
+#define MOE_COMBINE_MINB8 (MOE_COMBINE_U8 == 1 ? 4 : 2)
+#endif
+
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
-  if (p.K <= 2) return launch_variant<2, 4, 2>(p, stream);
+  if (p.K <= 2) return launch_variant<2, MOE_COMBINE_U2, MOE_COMBINE_MINB2>(p, stream);
   if (p.K <= 4) return launch_variant<4, 2, 3>(p, stream);
-  return launch_variant<8, MOE_COMBINE_U8, (MOE_COMBINE_U8 == 1 ? 4 : 2)>(p, stream);
+  return launch_variant<8, MOE_COMBINE_U8, MOE_COMBINE_MINB8>(p, stream);
 }
 
 }  // namespace moe
