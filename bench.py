@@ -595,12 +595,12 @@ def run_gpu(args, wl):
 
     # e2e: pinned host inputs in, result out, copies inside the timed region.
     # Each step is one CUDA-graph replay of the copies and the public calls;
-    # up to 3 steps are in flight on their own streams and buffer sets (a
-    # serving loop's pipelining), each with its own host output buffer.
+    # up to --e2e-streams steps are in flight on their own streams and buffer
+    # sets (a serving loop's pipelining), each with its own host output buffer.
     hx = torch.from_numpy(d["x"].view(np.int16)).pin_memory()
     hidx = torch.from_numpy(d["topk_idx"]).pin_memory()
     hw = torch.from_numpy(d["topk_weights"]).pin_memory()
-    n_inflight = min(3, nsets)
+    n_inflight = max(1, min(args.e2e_streams, nsets))
     hys = [torch.empty((N, H), dtype=torch.int16).pin_memory() for _ in range(n_inflight)]
     hcnts = [torch.empty(E, dtype=torch.int32).pin_memory() for _ in range(n_inflight)]
     h2d = hx.numel() * 2 + hidx.numel() * 4 + hw.numel() * 4
@@ -730,6 +730,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=3,
+                    help="end-to-end steps in flight, each on its own stream and buffer set")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the per-call timing of the masked plan, combine with the shared "
                          "expert, activation and router")
