@@ -333,14 +333,9 @@ __device__ __forceinline__ float half_warp_amax(const float (&f)[8]) {
 
 // The 8 E4M3 bytes e4m3(RN(x / scale)) of one lane as two little-endian
 // words, exact, from r = RN(1 / scale) and an IEEE division only where
-// needed.  q~ = RN(x * r) is within 3 binary32 ulps of RN(x / scale) (two
-// roundings of 2^-24 plus half an ulp).  Multiplying q~ by 1 -+ 2^-20 moves
-// it by at least 4 ulps less half an ulp of rounding, i.e. past that
-// interval on both sides; rounding to E4M3 is monotone, so where both ends
-// give the same byte, that byte is exact.  (Below the normal range, where the
-// move may round away, every candidate is smaller than the least E4M3
-// subnormal's half and rounds to a zero of the same sign.)  Where the two
-// ends differ -- a quotient next to an E4M3 midpoint, which bf16 inputs hit
+// needed: x is multiplied by r scaled down and up by 2^-20 (quant_window4),
+// which brackets RN(x / scale); where both ends give the same byte, that
+// byte is exact.  Where the two ends differ -- a quotient next to an E4M3 midpoint, which bf16 inputs hit
 // for about 1 element in 200 -- that element alone is divided with IEEE
 // __fdiv_rn.  If 1/scale overflows (r > 3e38) every element is divided.
 __device__ __forceinline__ uint32_t e4m3_byte(float v) { return e4m3x4(v, 0.0f, 0.0f, 0.0f) & 0xFFu; }
@@ -353,14 +348,22 @@ __device__ __forceinline__ uint2 quant_bytes8_exact(const float (&f)[8], float s
                            __fdiv_rn(f[7], scale)));
 }
 
-// Fast E4M3 words of 4 values: lo from q~ * (1 - 2^-20), hi from
-// q~ * (1 + 2^-20); a byte is exact where lo and hi agree.
-__device__ __forceinline__ void quant_window4(float a, float b, float c, float d, float r, uint32_t &lo,
-                                              uint32_t &hi) {
-  const float qa = __fmul_rn(a, r), qb = __fmul_rn(b, r), qc = __fmul_rn(c, r), qd = __fmul_rn(d, r);
-  constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
-  lo = e4m3x4(__fmul_rn(qa, kDown), __fmul_rn(qb, kDown), __fmul_rn(qc, kDown), __fmul_rn(qd, kDown));
-  hi = e4m3x4(__fmul_rn(qa, kUp), __fmul_rn(qb, kUp), __fmul_rn(qc, kUp), __fmul_rn(qd, kUp));
+// Fast E4M3 words of 4 values from rl = RN(r * (1 - 2^-20)) and
+// rh = RN(r * (1 + 2^-20)), r = RN(1 / scale): lo = e4m3(RN(x * rl)) and
+// hi = e4m3(RN(x * rh)).  RN(x * rl) is at most x/scale * (1 - 2^-20) *
+// (1 + 2^-24)^3 < x/scale * (1 - 2^-24) in magnitude, below RN(x / scale),
+// and RN(x * rh) above it likewise; rounding to E4M3 is monotone, so a byte
+// where lo and hi agree is e4m3(RN(x / scale)).  (Below the normal range
+// every candidate rounds to a zero of x's sign.)
+__device__ __forceinline__ void quant_window4(float a, float b, float c, float d, float rl, float rh,
+                                              uint32_t &lo, uint32_t &hi) {
+  lo = e4m3x4(__fmul_rn(a, rl), __fmul_rn(b, rl), __fmul_rn(c, rl), __fmul_rn(d, rl));
+  hi = e4m3x4(__fmul_rn(a, rh), __fmul_rn(b, rh), __fmul_rn(c, rh), __fmul_rn(d, rh));
+}
+
+// rl and rh of quant_window4.
+__device__ __forceinline__ float2 quant_window_r(float r) {
+  return make_float2(__fmul_rn(r, 1.0f - 0x1p-20f), __fmul_rn(r, 1.0f + 0x1p-20f));
 }
 
 // Replace the bytes of lo where lo and hi differ by the divided ones.
@@ -383,8 +386,9 @@ __device__ __forceinline__ uint2 quant_bytes8(const float (&f)[8], float scale, 
   if (!(r <= 3.0e38f)) return quant_bytes8_exact(f, scale);
   uint2 q;
   uint32_t h0, h1;
-  quant_window4(f[0], f[1], f[2], f[3], r, q.x, h0);
-  quant_window4(f[4], f[5], f[6], f[7], r, q.y, h1);
+  const float2 rw = quant_window_r(r);
+  quant_window4(f[0], f[1], f[2], f[3], rw.x, rw.y, q.x, h0);
+  quant_window4(f[4], f[5], f[6], f[7], rw.x, rw.y, q.y, h1);
   if (q.x != h0) q.x = quant_patch4(q.x, h0, f[0], f[1], f[2], f[3], scale);
   if (q.y != h1) q.y = quant_patch4(q.y, h1, f[4], f[5], f[6], f[7], scale);
   return q;
@@ -412,8 +416,9 @@ __device__ __forceinline__ void quantise_blocks(const float (&f)[P][8], const fl
       hi[it][0] = q[it].x;
       hi[it][1] = q[it].y;
     } else {
-      quant_window4(f[it][0], f[it][1], f[it][2], f[it][3], r[it], q[it].x, hi[it][0]);
-      quant_window4(f[it][4], f[it][5], f[it][6], f[it][7], r[it], q[it].y, hi[it][1]);
+      const float2 rw = quant_window_r(r[it]);
+      quant_window4(f[it][0], f[it][1], f[it][2], f[it][3], rw.x, rw.y, q[it].x, hi[it][0]);
+      quant_window4(f[it][4], f[it][5], f[it][6], f[it][7], rw.x, rw.y, q[it].y, hi[it][1]);
       any |= (q[it].x != hi[it][0]) | (q[it].y != hi[it][1]);
     }
   }

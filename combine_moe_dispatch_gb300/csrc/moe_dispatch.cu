@@ -28,13 +28,13 @@
 // for the plan, which it does not need.
 //
 // Exact division, cheaply: q must be e4m3(RN(x / scale)).  With r =
-// RN(1/scale), q~ = RN(x * r) is within 3 binary32 ulps of RN(x / scale)
-// (two roundings of 2^-24 each, plus half an ulp).  Rounding to E4M3 is
-// monotone, so if q~ * (1 - 2^-20) and q~ * (1 + 2^-20), at least 3.5 ulps
-// either side, round to the same byte, that byte is e4m3(RN(x / scale));
-// otherwise (a quotient next to an E4M3 midpoint, about 1 element in 200
-// for bf16 inputs) that element alone is divided with IEEE __fdiv_rn.  The
-// result is bit-identical to dividing every element.
+// RN(1/scale), x * RN(r * (1 - 2^-20)) and x * RN(r * (1 + 2^-20)), rounded,
+// bracket RN(x / scale) (three roundings of at most 2^-24 each cannot close
+// a 2^-20 gap).  Rounding to E4M3 is monotone, so where both give the same
+// byte, that byte is e4m3(RN(x / scale)); otherwise (a quotient next to an
+// E4M3 midpoint, about 1 element in 200 for bf16 inputs) that element alone
+// is divided with IEEE __fdiv_rn.  The result is bit-identical to dividing
+// every element.
 #include <cuda_bf16.h>
 
 #include "moe_common.cuh"
