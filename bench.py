@@ -2,9 +2,11 @@
 """Benchmark of the MoE dispatch/combine hot path on one GB300 (or N replicas).
 
 One step = one pass of the whole path over one batch of seeded synthetic
-input: moe_plan, moe_dispatch (bf16 payload), moe_dispatch (fp8 e4m3 1x128
-payload, reusing the plan) and moe_combine, on the DeepSeek-V3-shaped decode
-layer by default (8 logical ranks x 128 tokens, H=7168, E=256, top-8).
+input: moe_plan_dispatch (the plan and the bf16 dispatch, one launch up to
+16384 routed entries), moe_dispatch (fp8 e4m3 1x128 payload, reusing the
+plan) and moe_combine, on the DeepSeek-V3-shaped decode layer by default
+(8 logical ranks x 128 tokens, H=7168, E=256, top-8).  Each call is also
+timed alone, and the plan and both dispatches also as separate launches.
 
 Timing: each step is one CUDA-graph replay of the calls (how a serving
 engine runs a layer: one graph per batch size); K steps run back to back
@@ -50,7 +52,11 @@ KERNEL_SOURCES = {
     "dispatch_bf16": "combine_moe_dispatch_gb300/csrc/moe_dispatch.cu",
     "dispatch_fp8": "combine_moe_dispatch_gb300/csrc/moe_dispatch.cu",
     "combine": "combine_moe_dispatch_gb300/csrc/moe_combine.cu",
+    "plan_dispatch_bf16": "combine_moe_dispatch_gb300/csrc/moe_plan_dispatch.cu",
+    "plan_dispatch_fp8": "combine_moe_dispatch_gb300/csrc/moe_plan_dispatch.cu",
 }
+# moe_plan_dispatch runs as one launch up to this many routed entries (N*K)
+FUSED_MAX_ENTRIES = 16384
 
 
 # ---------------------------------------------------------------------------
@@ -69,6 +75,10 @@ def call_bytes(wl) -> dict:
         "dispatch_fp8": N * H * 2 + 2 * maps + N * K * H + N * K * (H // 128) * 4,
         # read K expert rows per token, topk_idx, slot_of, weights; write y
         "combine": N * K * H * 2 + 3 * maps + N * H * 2,
+        # the plan and the dispatch in one call: the bytes of both
+        "plan_dispatch_bf16": 3 * maps + E * 4 + E * (R + 1) * 4 + N * H * 2 + 2 * maps + N * K * H * 2,
+        "plan_dispatch_fp8": (3 * maps + E * 4 + E * (R + 1) * 4 + N * H * 2 + 2 * maps + N * K * H
+                              + N * K * (H // 128) * 4),
     }
 
 
@@ -93,9 +103,20 @@ def next_row_bytes(wl, routed_masked: int, valid_tokens: int) -> dict:
 
 
 def step_calls(wl) -> list:
-    """Every row of the hot path: plan, both dispatch payloads (fp8 needs
-    H % 128 == 0), combine."""
+    """Every row of the hot path, as separate calls: plan, both dispatch
+    payloads (fp8 needs H % 128 == 0), combine.  Their bytes make a step's."""
     return ["plan", "dispatch_bf16"] + (["dispatch_fp8"] if wl.H % 128 == 0 else []) + ["combine"]
+
+
+def step_sequence(wl) -> list:
+    """The calls one step makes: the plan fused with the bf16 dispatch, the
+    fp8 dispatch on that plan, the combine."""
+    return ["plan_dispatch_bf16"] + (["dispatch_fp8"] if wl.H % 128 == 0 else []) + ["combine"]
+
+
+def launches_per_step(wl) -> int:
+    fused = wl.N * wl.K <= FUSED_MAX_ENTRIES
+    return (1 if fused else 2) + (1 if wl.H % 128 == 0 else 0) + 1
 
 
 # ---------------------------------------------------------------------------
@@ -321,9 +342,9 @@ class BufferSet:
         self.x = torch.from_numpy(d["x"].view(np.int16)).to(device).view(torch.bfloat16)
         self.w = torch.from_numpy(d["topk_weights"]).to(device)
         self.b16 = moe.Buffers(self.sh16, device=device, expert_y=False,
-                               expert_x="dispatch_bf16" in calls)
+                               expert_x=any(c.endswith("dispatch_bf16") for c in calls))
         self.b8 = (moe.Buffers(self.sh8, device=device, expert_y=False, expert_x=True)
-                   if "dispatch_fp8" in calls else None)
+                   if any(c.endswith("dispatch_fp8") for c in calls) else None)
         self.ey = inputs.expert_outputs_device(E, cap, H, seed, device=device)
         self.moe = moe
 
@@ -340,13 +361,17 @@ class BufferSet:
         elif name == "combine":
             moe.combine(self.sh16, self.ey, self.idx, b16.slot_of, self.w, b16.y, b16.workspace,
                         stream)
+        elif name == "plan_dispatch_bf16":
+            b16.plan_dispatch(self.x, self.idx, stream)
+        elif name == "plan_dispatch_fp8":
+            b8.plan_dispatch(self.x, self.idx, stream)
 
     @staticmethod
     def nbytes(wl, cap, calls):
         per = wl.N * wl.H * 2 * 2 + wl.E * cap * wl.H * 2           # x, y, expert_y
-        if "dispatch_bf16" in calls:
+        if any(c.endswith("dispatch_bf16") for c in calls):
             per += wl.E * cap * wl.H * 2
-        if "dispatch_fp8" in calls:
+        if any(c.endswith("dispatch_fp8") for c in calls):
             per += wl.E * cap * wl.H + wl.E * cap * (wl.H // 128) * 4
         return per
 
@@ -485,8 +510,11 @@ def run_gpu(args, wl):
     d = inputs.make(wl, args.seed)
     N, H, E, K, R, T, cap = wl.N, wl.H, wl.E, wl.K, wl.R, wl.T, wl.cap
     calls = step_calls(wl)
+    seq = step_sequence(wl)
+    timed = calls + [c.replace("dispatch_", "plan_dispatch_") for c in calls if c.startswith("dispatch_")]
     if args.only:
         calls = [c for c in calls if c in ("plan", args.only)]
+        seq = timed = calls if args.only in calls else [args.only]
     if args.tight_capacity:
         cap = int(np.bincount(d["topk_idx"].ravel(), minlength=E).max())
     cb = call_bytes(wl)
@@ -495,12 +523,12 @@ def run_gpu(args, wl):
 
     # Enough buffer sets that one rotation moves >= 2x L2 in its smallest call,
     # within half of the free device memory.
-    smallest = min(cb[c] for c in calls if c != "plan") if len(calls) > 1 else cb["plan"]
+    smallest = min(cb[c] for c in timed if c != "plan") if len(timed) > 1 else cb[timed[0]]
     nsets = max(2, min(6, -(-2 * l2 // max(1, smallest))))
     free = torch.cuda.mem_get_info(device)[0]
-    while nsets > 1 and nsets * BufferSet.nbytes(wl, cap, calls) > free // 2:
+    while nsets > 1 and nsets * BufferSet.nbytes(wl, cap, timed) > free // 2:
         nsets -= 1
-    sets = [BufferSet(moe, torch, wl, d, device, calls, cap, args.seed + i) for i in range(nsets)]
+    sets = [BufferSet(moe, torch, wl, d, device, timed, cap, args.seed + i) for i in range(nsets)]
     stream = torch.cuda.Stream(device)
     torch.cuda.synchronize()
 
@@ -508,7 +536,7 @@ def run_gpu(args, wl):
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             for bs in sets:
-                for c in calls:
+                for c in timed:
                     bs.do(c, stream)
     stream.synchronize()
     assert all(moe.read_status(bs.b16.workspace, stream) == moe.Status.OK for bs in sets)
@@ -520,13 +548,13 @@ def run_gpu(args, wl):
         return g
 
     # one graph per buffer set: one whole step
-    step_graphs = [capture(lambda st, bs=bs: [bs.do(c, st) for c in calls]) for bs in sets]
+    step_graphs = [capture(lambda st, bs=bs: [bs.do(c, st) for c in seq]) for bs in sets]
     # one graph per call: M back-to-back launches over the rotating sets
     reps = max(1, 24 // nsets)
     call_graphs = {c: capture(lambda st, c=c: [bs.do(c, st) for _ in range(reps) for bs in sets])
-                   for c in calls}
-    # the dispatch as a user runs it: the plan, then the dispatch that may
-    # start while the plan finishes
+                   for c in timed}
+    # the plan and the dispatch as two calls: the plan, then the dispatch
+    # that may start while the plan finishes
     for c in calls:
         if c.startswith("dispatch_"):
             call_graphs["plan+" + c] = capture(
@@ -578,11 +606,11 @@ def run_gpu(args, wl):
     # cold single calls (diagnostic): eager, L2 flushed by a 2x L2 write before
     # each, CUDA events around the call; includes the launch and event latency
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
-    cold = {c: [] for c in calls}
+    cold = {c: [] for c in timed}
     bs = sets[0]
     with torch.cuda.stream(stream):
         for it in range(13):
-            for c in calls:
+            for c in timed:
                 flush.zero_()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -611,7 +639,7 @@ def run_gpu(args, wl):
         bs.x.view(torch.int16).copy_(hx, non_blocking=True)
         bs.idx.copy_(hidx, non_blocking=True)
         bs.w.copy_(hw, non_blocking=True)
-        for c in calls:
+        for c in seq:
             bs.do(c, st)
         hy.copy_(bs.b16.y.view(torch.int16), non_blocking=True)
         hcnt.copy_(bs.b16.expert_num_tokens, non_blocking=True)
@@ -657,14 +685,14 @@ def run_gpu(args, wl):
         next_rows = measure_next_rows(moe, torch, wl, d, device, stream, l2, peak, args.seed,
                                       args.warmup)
     means = {c: statistics.median(v) for c, v in per_call.items()}
-    dom = max((c for c in calls), key=means.get)
+    dom = max((c for c in seq), key=means.get)
     achieved = cb[dom] / (means[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "peak_source": f"{peak_kind} hbm_gbs", "unit": UNIT, "frac": achieved / peak,
                 "traffic": recorded_traffic(dom, wl.name),
                 "algorithmic_bytes": cb[dom]}
     calls_out = {}
-    for c in calls:
+    for c in timed:
         us = 1e3 * means[c]
         calls_out[c] = {"us": us, "bytes": cb[c], "gbs": cb[c] / (us * 1e-6) / 1e9,
                         "frac_of_peak": cb[c] / (us * 1e-6) / 1e9 / peak,
@@ -672,12 +700,17 @@ def run_gpu(args, wl):
     disp = {}
     for p_ in ("bf16", "fp8"):
         c = f"dispatch_{p_}"
-        if c in calls:
-            us = 1e3 * means["plan+" + c]
+        if c in calls and "plan_" + c in means:
+            us = 1e3 * means["plan_" + c]
+            two = 1e3 * means["plan+" + c]
             b_ = cb["plan"] + cb[c]
             disp[p_] = {"us": us, "gbs": b_ / (us * 1e-6) / 1e9,
                         "frac_of_peak": b_ / (us * 1e-6) / 1e9 / peak,
-                        "note": "moe_plan then moe_dispatch, back to back in one graph"}
+                        "two_launches_us": two,
+                        "two_launches_frac_of_peak": b_ / (two * 1e-6) / 1e9 / peak,
+                        "note": ("us: moe_plan_dispatch (one launch when N*K <= "
+                                 f"{FUSED_MAX_ENTRIES}); two_launches: moe_plan then moe_dispatch, "
+                                 "back to back in one graph")}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -689,7 +722,7 @@ def run_gpu(args, wl):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": {**workload_config(wl, cap), "calls_per_step": calls,
+            "config": {**workload_config(wl, cap), "calls_per_step": seq,
                        "io": "bf16 activations and expert outputs, e4m3 + fp32 scales for the fp8 payload",
                        "l2": (f"no flush: inputs larger than L2 -- each step moves {step_bytes / 1e6:.0f} MB "
                               f"({step_bytes / l2:.1f}x L2) and the timed loop rotates through "
@@ -711,7 +744,7 @@ def run_gpu(args, wl):
                              "y, expert_num_tokens out, around the public calls, as one CUDA-graph replay; "
                              f"{n_inflight} steps in flight on their own streams and buffer sets; expert_y "
                              "stays resident on the device, as the expert GEMM leaves it")},
-            "gpu_launches": len(calls) * args.steps,
+            "gpu_launches": launches_per_step(wl) * args.steps,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)

@@ -82,6 +82,7 @@ SIGNATURES = {
     "moe_combine_shared": ([_SP, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_router_topk": ([_SP, _P, _P, _P, _P], ctypes.c_int),
     "moe_silu_mul_quant": ([_SP, ctypes.c_int32, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "moe_plan_dispatch": ([_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
 }
 
 _lib = None
@@ -172,6 +173,18 @@ def dispatch(shape: Shape, x, topk_idx, slot_of, expert_x, expert_x_scale, works
                                      _ptr(expert_x), _ptr(expert_x_scale), _ptr(workspace),
                                      _stream(stream))
     return _check(st, "moe_dispatch", check)
+
+
+def plan_dispatch(shape: Shape, x, topk_idx, expert_num_tokens, expert_rank_offsets, slot_of,
+                  src_of, expert_x, expert_x_scale, workspace, stream=None, check=True) -> Status:
+    """moe_plan followed by moe_dispatch, in one launch where the shape allows."""
+    st = load_library().moe_plan_dispatch(ctypes.byref(shape), _ptr(x), _ptr(topk_idx),
+                                          _ptr(expert_num_tokens), _ptr(expert_rank_offsets),
+                                          _ptr(slot_of), _ptr(src_of), _ptr(expert_x),
+                                          _ptr(expert_x_scale), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(),
+                                          _stream(stream))
+    return _check(st, "moe_plan_dispatch", check)
 
 
 def combine(shape: Shape, expert_y, topk_idx, slot_of, topk_weights, y, workspace,
@@ -274,6 +287,11 @@ class Buffers:
     def dispatch(self, x, topk_idx, stream=None, check=True):
         return dispatch(self.shape, x, topk_idx, self.slot_of, self.expert_x, self.expert_x_scale,
                         self.workspace, stream, check)
+
+    def plan_dispatch(self, x, topk_idx, stream=None, check=True):
+        return plan_dispatch(self.shape, x, topk_idx, self.expert_num_tokens,
+                             self.expert_rank_offsets, self.slot_of, self.src_of, self.expert_x,
+                             self.expert_x_scale, self.workspace, stream, check)
 
     def combine(self, topk_idx, topk_weights, expert_y=None, stream=None, check=True):
         ey = self.expert_y if expert_y is None else expert_y

@@ -198,6 +198,52 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *to
   return from_cuda(fp8 ? launch_dispatch_fp8(p, s) : launch_dispatch_bf16(p, s));
 }
 
+moe_status moe_plan_dispatch(const moe_shape *shape, const void *x, const int32_t *topk_idx,
+                             int32_t *expert_num_tokens, int32_t *expert_rank_offsets,
+                             int32_t *slot_of, int32_t *src_of, void *expert_x,
+                             float *expert_x_scale, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  const bool fp8 = shape->payload == MOE_PAYLOAD_FP8_E4M3;
+  const bool empty = shape->tokens_per_rank == 0;
+  if (!empty && (!x || !expert_x || (fp8 && !expert_x_scale))) return MOE_ERR_INVALID_ARG;
+  if (!empty && (!aligned(x, 16) || !aligned(expert_x, 16) || (fp8 && !aligned(expert_x_scale, 4))))
+    return MOE_ERR_ALIGNMENT;
+  FusedParams f;
+  if (empty || !plan_dispatch_geometry(*shape, f)) {
+    // outside the fused path's limits: the plan, then the dispatch
+    st = plan_common(shape, topk_idx, nullptr, 0, expert_num_tokens, expert_rank_offsets, slot_of,
+                     src_of, workspace, workspace_bytes, stream);
+    if (st != MOE_OK || empty) return st;
+    return moe_dispatch(shape, x, topk_idx, slot_of, expert_x, expert_x_scale, workspace, stream);
+  }
+  if (!topk_idx || !slot_of || !expert_num_tokens || !expert_rank_offsets || !src_of)
+    return MOE_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < ws_layout(*shape).total) return MOE_ERR_WORKSPACE;
+  if (!aligned(topk_idx, 4) || !aligned(expert_num_tokens, 4) || !aligned(expert_rank_offsets, 4) ||
+      !aligned(slot_of, 4) || !aligned(src_of, 4) || !aligned(workspace, 16))
+    return MOE_ERR_ALIGNMENT;
+  f.d.x = static_cast<const uint16_t *>(x);
+  f.d.topk_idx = topk_idx;
+  f.d.slot_of = slot_of;
+  f.d.expert_x = expert_x;
+  f.d.expert_x_scale = fp8 ? expert_x_scale : nullptr;
+  f.d.hdr = header(workspace);
+  f.d.N = shape->num_ranks * shape->tokens_per_rank;
+  f.d.H = shape->hidden;
+  f.d.E = shape->num_experts;
+  f.d.K = shape->top_k;
+  f.d.cap = shape->capacity;
+  f.topk_idx = topk_idx;
+  f.expert_num_tokens = expert_num_tokens;
+  f.expert_rank_offsets = expert_rank_offsets;
+  f.slot_of = slot_of;
+  f.src_of = src_of;
+  f.vec_idx = aligned(topk_idx, 16) ? 1 : 0;
+  return from_cuda(launch_plan_dispatch(f, fp8, (cudaStream_t)stream));
+}
+
 static moe_status combine_common(const moe_shape *shape, const void *expert_y,
                                  const int32_t *topk_idx, const int32_t *slot_of,
                                  const float *topk_weights, const void *shared, void *y,

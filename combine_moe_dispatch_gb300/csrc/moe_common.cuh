@@ -57,7 +57,9 @@ struct WsHeader {
   int32_t status;       // moe_status of the last plan (and of later dispatch/combine)
   uint32_t debug_flags; // kDebug* test hooks
   uint64_t timeout_ns;  // limit of every wait; 0 = kDefaultTimeoutNs
-  uint32_t reserved[56];
+  uint32_t arrivals;    // fused plan+dispatch: blocks arrived (bits 0-15), blocks that saw a
+                        // bad expert (16-23) or an over-capacity expert (24-31); reset by the last
+  uint32_t reserved[55];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
@@ -125,6 +127,33 @@ struct DispatchParams {
   int N, H, E, K, cap;
 };
 
+// Plan and dispatch in one launch (moe_plan_dispatch.cu): taken up to
+// kFusedMaxEntries routed entries, since every block reads the whole routing
+// table, and while the block's tables fit kFusedMaxSmem.
+constexpr int64_t kFusedMaxEntries = 16384;
+constexpr int kFusedMaxGrid = 255;      // the arrival word counts blocks in 8-bit fields
+constexpr size_t kFusedMaxSmem = 200 * 1024;   // the routing table (<= 64 KB) and the block's tables
+
+struct FusedParams {
+  DispatchParams d;            // x, expert_x, expert_x_scale, hdr, N, H, E, K, cap
+  const int32_t *topk_idx;
+  int32_t *expert_num_tokens;
+  int32_t *expert_rank_offsets;
+  int32_t *slot_of;
+  int32_t *src_of;
+  int R, T;
+  int units;                   // bf16: 16-byte chunks per lane per task; fp8: block pairs
+  int tpr;                     // tasks per token row
+  int64_t ntasks;              // N * tpr
+  int q_tasks;                 // tasks per block (a contiguous run)
+  int grid;                    // blocks, one per SM at most
+  int owned;                   // experts per block for counts and offsets
+  int max_run;                 // routed entries of one block's tokens, at most
+  int ebits;                   // bits of the largest expert id
+  int vec_idx;                 // topk_idx is 16-byte aligned (16-byte loads)
+  size_t smem_bytes;
+};
+
 struct CombineParams {
   const uint16_t *expert_y;
   const uint16_t *shared;      // [N, H] bf16 shared-expert output, or null
@@ -167,6 +196,10 @@ cudaError_t launch_plan(const PlanParams &p, cudaStream_t stream);
 cudaError_t launch_dispatch_bf16(const DispatchParams &p, cudaStream_t stream);
 cudaError_t launch_dispatch_fp8(const DispatchParams &p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+// Fill the launch geometry of the fused plan + dispatch; false when the shape
+// is outside the fused path's limits (then run moe_plan and moe_dispatch).
+bool plan_dispatch_geometry(const moe_shape &s, FusedParams &p);
+cudaError_t launch_plan_dispatch(const FusedParams &p, bool fp8, cudaStream_t stream);
 cudaError_t launch_router(const RouterParams &p, cudaStream_t stream);
 cudaError_t launch_silu_quant(const ActParams &p, cudaStream_t stream);
 cudaError_t launch_set_debug(WsHeader *hdr, uint32_t flags, uint64_t timeout_ns,
@@ -282,6 +315,57 @@ __device__ __forceinline__ int ld_dsmem(const int32_t *local, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
   return v;
+}
+
+// Lanes of this warp whose key equals this lane's key (keys < 2^bits, or -1
+// for "no key", which matches only other -1 lanes).  Every lane executes
+// every ballot (no lane leaves early), as the full-warp ballots require.
+__device__ __forceinline__ unsigned peers_with_same_key(int key, int bits) {
+  const unsigned none = __ballot_sync(0xFFFFFFFFu, key < 0);
+  unsigned m = ~none;
+  for (int b = 0; b < bits; ++b) {
+    const int bit = (key >> b) & 1;
+    const unsigned set = __ballot_sync(0xFFFFFFFFu, bit);
+    m &= bit ? set : ~set;
+  }
+  return key < 0 ? none : m;
+}
+
+// --- bulk copy global -> shared with an mbarrier (one CTA) ---
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Arrive on `bar` announcing `bytes` of asynchronous copies, then copy
+// `bytes` (a multiple of 16, both addresses 16-byte aligned) from global
+// `src` to shared `dst`; the copy completes the announced bytes.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `bar` for at most `deadline` (global timer,
+// ns) and a bounded number of polls; false when the wait ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t deadline) {
+  constexpr uint32_t kMaxPolls = 1u << 24;
+  for (uint32_t it = 0; it < kMaxPolls; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u && global_timer_ns() > deadline) return false;
+  }
+  return false;
 }
 
 // Programmatic dependent launch.  The plan and activation kernels allow the

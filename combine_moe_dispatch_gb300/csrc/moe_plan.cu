@@ -212,20 +212,6 @@ plan_kernel(PlanParams p) {
 // kernel has no flags, counters or spin-waits in global memory.
 // ---------------------------------------------------------------------------
 
-// Lanes of this warp whose key equals this lane's key (keys < 2^bits, or -1
-// for "no key", which matches only other -1 lanes).  Every lane executes
-// every ballot (no lane leaves early), as the full-warp ballots require.
-__device__ __forceinline__ unsigned peers_with_same_key(int key, int bits) {
-  const unsigned none = __ballot_sync(0xFFFFFFFFu, key < 0);
-  unsigned m = ~none;
-  for (int b = 0; b < bits; ++b) {
-    const int bit = (key >> b) & 1;
-    const unsigned set = __ballot_sync(0xFFFFFFFFu, bit);
-    m &= bit ? set : ~set;
-  }
-  return key < 0 ? none : m;
-}
-
 // Exclusive scan of in[0..n) into out[0..n) by the whole block (n <= 2 *
 // blockDim.x); returns the total.  Starts and ends with __syncthreads.
 __device__ __forceinline__ int block_exclusive_scan(const int32_t *in, int32_t *out, int n) {

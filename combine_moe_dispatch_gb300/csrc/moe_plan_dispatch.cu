@@ -1,0 +1,398 @@
+// moe_plan_dispatch.cu -- the plan and the dispatch in one launch.
+//
+// What it computes: exactly what moe_plan followed by moe_dispatch computes
+// (moe_plan.cu, moe_dispatch.cu): counts, per-rank offsets, stable slots,
+// return addresses, and the bf16 or fp8 expert rows ("Efficient and portable
+// mixture-of-experts communication", Dispatch; "Enabling trillion-parameter
+// models on AWS EFA", Send and Receive Buffers; "Lower latency and higher
+// throughput with multi-node DeepSeek deployment", Quantization).
+//
+// Why: at decode sizes the plan is a chain of short dependent steps (load the
+// routes, rank, exchange counts, scan, write) whose latency, and the kernel
+// boundary after it, is a third of plan + dispatch.  Here no block waits for
+// another: each finds the slots it needs from the routing table itself.
+//
+// How: block b takes the contiguous run of Q (token, segment) tasks
+// [b*Q, (b+1)*Q), so its tokens form one range [g_lo, g_hi] and its routed
+// entries the run [g_lo*K, (g_hi+1)*K).  The slot of an entry (g, k) with
+// expert e is the number of entries of e before the run plus the number of
+// entries of e inside the run before (g, k).  Block b also owns the experts
+// [b*O, (b+1)*O) and writes their counts and offsets rows.
+//   1. Thread 0 starts one bulk copy (cp.async.bulk, completed on an
+//      mbarrier, waited for with a time limit) of the whole routing table
+//      into shared memory, and every warp issues the loads of its first
+//      task's x segment.  The copy engine leaves the SM's load pipeline to
+//      the x loads; when the table went through that pipeline as plain
+//      loads, it waited behind them (about 2 us at DeepSeek-V3 decode).
+//   2. The block marks the experts of its run in a shared byte table.
+//   3. Warp 0 ranks the run stably (one ballot per bit of the expert id finds
+//      the lanes with the same expert; a shared per-expert counter carries
+//      the count across 32-entry batches).  Meanwhile the other warps scan
+//      the table in shared memory: an entry before the run whose expert is
+//      marked adds one to that expert's count, and an entry of an owned
+//      expert adds one to that expert's count for its rank.
+//   4. slot = count before the run + rank in the run, kept in shared memory.
+//      Thread 0 adds the block's arrival and error bits to one workspace
+//      word with one atomic whose result it reads only at the end: the last
+//      block to arrive writes the status word (no block waits for another).
+//   5. The warps run their tasks as moe_dispatch does, software-pipelined,
+//      with the routes read from shared memory; each warp quantises (fp8)
+//      its first task after the block's last barrier, so its stores start as
+//      soon as its own task is ready.
+//   6. After its tasks the block writes slot_of and src_of for the tokens
+//      whose first segment it holds, and each owner its experts' counts and
+//      offsets rows: stores issued earlier would wait behind the x loads.
+// Every block copies and scans all N*K routes, which pays only while the
+// table is small: the fused path is taken up to kFusedMaxEntries routed
+// entries (at Kimi-K2 decode, 32768 entries, two launches measured faster);
+// larger shapes run moe_plan and moe_dispatch as two launches.  One block per
+// SM, as many threads as the dispatch kernels keep resident per SM (768 for
+// fp8, 1024 for bf16).
+//
+// Data errors: the status word ends up exactly as moe_plan would set it, and
+// the plan outputs are those of moe_plan.  But no block waits for the
+// verdict of the others, so the rows of entries whose expert is in range and
+// whose slot is below cap may already have been written when the status
+// reports an error; moe_dispatch would write none.
+#include <cuda_bf16.h>
+
+#include "moe_dispatch_tasks.cuh"
+
+namespace moe {
+
+// bf16 and fp8 tasks behind one interface: load (no routing needed), prep
+// (fp8: quantise; bf16: nothing), store to the K rows.
+template <int U>
+struct Bf16Path {
+  using Raw = Bf16Task<U>;
+  using Out = Bf16Task<U>;
+  static __device__ __forceinline__ void load(const DispatchParams &p, int64_t task, int tpr,
+                                              int lane, Raw &a) {
+    bf16_load<U>(p, task, tpr, lane, a);
+  }
+  static __device__ __forceinline__ void prep(const Raw &a, int, Out &t) { t = a; }
+  static __device__ __forceinline__ void store(const DispatchParams &p, int lane, const Out &t,
+                                               const Routes &r) {
+    bf16_store<U>(p, lane, t, r);
+  }
+  static __device__ __forceinline__ int64_t token(const Out &t) { return t.g; }
+};
+
+template <int P>
+struct Fp8Path {
+  using Raw = Fp8Raw<P>;
+  using Out = Fp8Task<P>;
+  static __device__ __forceinline__ void load(const DispatchParams &p, int64_t task, int tpr,
+                                              int lane, Raw &a) {
+    fp8_load<P>(p, task, tpr, lane, a);
+  }
+  static __device__ __forceinline__ void prep(const Raw &a, int lane, Out &t) {
+    fp8_quantise<P>(a, lane, t);
+  }
+  static __device__ __forceinline__ void store(const DispatchParams &p, int lane, const Out &t,
+                                               const Routes &r) {
+    fp8_store<P>(p, lane, t, r);
+  }
+  static __device__ __forceinline__ int64_t token(const Out &t) { return t.g; }
+};
+
+// Routes of token g from the block's run: lane k < K holds (expert, slot);
+// slot -1 (a bad id, or a slot at or beyond cap) makes the store skip it.
+__device__ __forceinline__ Routes run_routes(const int32_t *s_rexp, const int32_t *s_rslot,
+                                             int64_t g, int64_t g_lo, int K, int cap, int lane) {
+  Routes r{-1, -1};
+  if (lane < K) {
+    const int i = (int)(g - g_lo) * K + lane;
+    r.e = s_rexp[i];
+    const int s = s_rslot[i];
+    r.s = (r.e >= 0 && s < cap) ? s : -1;
+  }
+  return r;
+}
+
+// Status of a block, as one atomic add to the workspace's arrival word:
+// bits 0-7 count the blocks that arrived, 8-15 those whose wait for the
+// routing table ran out, 16-23 those that saw a bad expert id, 24-31 those
+// that saw an expert over capacity (8-bit fields: at most 255 blocks).
+__device__ __forceinline__ uint32_t arrival_code(uint32_t err) {
+  return 1u | ((err & kErrTimeout) ? 1u << 8 : 0u) | ((err & kErrBadExpert) ? 1u << 16 : 0u) |
+         ((err & kErrCapacity) ? 1u << 24 : 0u);
+}
+
+// Called by the block's thread 0 with the arrival word after its own add:
+// the last block to arrive writes the status word and resets the count.
+__device__ __forceinline__ void finish_status(WsHeader *hdr, uint32_t arrived) {
+  if ((arrived & 0xFFu) != gridDim.x) return;
+  hdr->status = ((arrived >> 8) & 0xFFu)    ? MOE_ERR_TIMEOUT
+                : ((arrived >> 16) & 0xFFu) ? MOE_ERR_BAD_EXPERT
+                : (arrived >> 24)           ? MOE_ERR_CAPACITY
+                                            : MOE_OK;
+  hdr->arrivals = 0;
+}
+
+template <class Path, int THREADS>
+__global__ void __launch_bounds__(THREADS, 1)
+plan_dispatch_kernel(FusedParams p) {
+  constexpr int kWarps = THREADS / 32;
+  constexpr int kScanners = THREADS - 32;   // warps 1.. scan, warp 0 ranks
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ uint32_t s_err;
+  const int E = p.d.E, K = p.d.K, R = p.R, cap = p.d.cap;
+  const int total = p.d.N * K;
+  const size_t tab_bytes = ((size_t)total * 4 + 15) & ~(size_t)15;
+  int32_t *s_tab = reinterpret_cast<int32_t *>(smem);                      // [N*K] the routing table
+  uint8_t *s_code = smem + tab_bytes;                                      // [E] expert used by the run
+  int32_t *s_pre = reinterpret_cast<int32_t *>(s_code + ((E + 15) & ~15)); // [E] entries before the run
+  int32_t *s_loc = s_pre + E;                                              // [E] ranking counters
+  int32_t *s_ocnt = s_loc + E;                                             // [O][R] owned experts per rank
+  int32_t *s_rexp = s_ocnt + p.owned * R;                                  // [run] expert, -1 if bad
+  int32_t *s_rslot = s_rexp + p.max_run;                                   // [run] rank, then slot
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t t0 = (int64_t)blockIdx.x * p.q_tasks;
+  const int64_t t1 = min(t0 + (int64_t)p.q_tasks, p.ntasks);
+  const int64_t g_lo = t0 / p.tpr, g_hi = (t1 - 1) / p.tpr;
+  const int lo_ent = (int)(g_lo * K);
+  const int run = (int)(g_hi - g_lo + 1) * K;
+  const int own0 = blockIdx.x * p.owned;
+
+  // 1. the routing table into shared memory: one bulk copy of its 16-byte
+  //    part by the copy engine (it leaves the SM's load pipeline to the x
+  //    loads), plain loads for the rest (all of it when the table is not
+  //    16-byte aligned); the first task's x loads, which need nothing from
+  //    the routing
+  const int nbulk = p.vec_idx ? (total & ~3) : 0;
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    if (nbulk > 0) bulk_copy_g2s(s_tab, p.topk_idx, (uint32_t)nbulk * 4u, &s_bar);
+  }
+  for (int q = nbulk + tid; q < total; q += THREADS) s_tab[q] = __ldg(p.topk_idx + q);
+  const int64_t my0 = t0 + warp;
+  const bool has0 = my0 < t1;
+  typename Path::Raw a;
+  if (has0) Path::load(p.d, my0, p.tpr, lane, a);
+  for (int i = tid; i < E; i += THREADS) {
+    s_code[i] = 0;
+    s_pre[i] = 0;
+    s_loc[i] = 0;
+  }
+  for (int i = tid; i < p.owned * R; i += THREADS) s_ocnt[i] = 0;
+  if (tid == 0) s_err = 0;
+  __syncthreads();   // also publishes the barrier's initialisation
+  const bool tab_ok = nbulk == 0 || mbar_wait_bounded(&s_bar, 0, global_timer_ns() + kDefaultTimeoutNs);
+  if (!__syncthreads_and(tab_ok)) {
+    // the copy did not land in time: wait once more (bounded) so that no
+    // copy into this block's shared memory is left in flight, report, and
+    // write nothing
+    if (tid == 0) {
+      mbar_wait_bounded(&s_bar, 0, global_timer_ns() + kDefaultTimeoutNs);
+      const uint32_t code = arrival_code(kErrTimeout);
+      finish_status(p.d.hdr, atomicAdd(&p.d.hdr->arrivals, code) + code);
+    }
+    return;
+  }
+
+  // 2. mark the run's experts
+  uint32_t err = 0;
+  for (int i = tid; i < run; i += THREADS) {
+    const int e = s_tab[lo_ent + i];
+    const bool ok = (unsigned)e < (unsigned)E;
+    s_rexp[i] = ok ? e : -1;
+    if (ok) s_code[e] = 1;   // every writer stores the same value
+    else err |= kErrBadExpert;
+  }
+  __syncthreads();
+
+  // 3. rank the run (warp 0) / count entries before the run and of owned
+  //    experts (the other warps)
+  if (warp == 0) {
+    const unsigned lt = (1u << lane) - 1u;
+    for (int i0 = 0; i0 < run; i0 += 32) {
+      const int i = i0 + lane;
+      const int e = i < run ? s_rexp[i] : -1;
+      const unsigned same = peers_with_same_key(e, p.ebits);
+      const int before = __popc(same & lt);
+      const int base = e >= 0 ? s_loc[e] : 0;
+      __syncwarp();
+      if (e >= 0 && before == 0) s_loc[e] = base + __popc(same);
+      __syncwarp();
+      if (i < run) s_rslot[i] = base + before;
+    }
+  } else {
+    const int tk = p.T * K;      // entries per rank
+    auto visit = [&](int q, int e) {
+      if ((unsigned)e >= (unsigned)E) return;   // a bad id is reported by its run's block
+      if (q < lo_ent && s_code[e]) atomicAdd(&s_pre[e], 1);
+      const unsigned o = (unsigned)(e - own0);
+      if (o < (unsigned)p.owned) atomicAdd(&s_ocnt[o * R + q / tk], 1);
+    };
+    const int4 *t4 = reinterpret_cast<const int4 *>(s_tab);
+    const int n4 = total >> 2;
+    for (int j = tid - 32; j < n4; j += kScanners) {
+      const int4 w = t4[j];
+      visit(4 * j, w.x);
+      visit(4 * j + 1, w.y);
+      visit(4 * j + 2, w.z);
+      visit(4 * j + 3, w.w);
+    }
+    for (int q = 4 * n4 + tid - 32; q < total; q += kScanners) visit(q, s_tab[q]);
+  }
+  __syncthreads();
+
+  // 4. slots (in shared memory only: the plan outputs are written after the
+  //    tasks, so no store here waits behind the x loads in flight); errors
+  for (int i = tid; i < run; i += THREADS) {
+    const int e = s_rexp[i];
+    const int slot = e >= 0 ? s_pre[e] + s_rslot[i] : -1;
+    if (e >= 0 && slot >= cap) err |= kErrCapacity;
+    s_rslot[i] = slot;
+  }
+  for (int j = warp; j < p.owned; j += kWarps) {
+    if (own0 + j >= E) break;
+    int sum = 0;
+    for (int r = lane; r < R; r += 32) sum += s_ocnt[j * R + r];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (sum > cap) err |= kErrCapacity;
+  }
+  if (err) atomicOr(&s_err, err);
+  __syncthreads();
+  // One atomic per block carries its arrival and its errors; its result is
+  // used only at the end, so its round trip overlaps the tasks.
+  uint32_t arrived = 0;
+  if (tid == 0) {
+    const uint32_t code = arrival_code(s_err);
+    arrived = atomicAdd(&p.d.hdr->arrivals, code) + code;
+  }
+
+  // 5. the tasks, software-pipelined as in moe_dispatch.  Each warp
+  //    quantises (fp8) its first task only now, so that its stores start as
+  //    soon as its own task is ready, not when every warp's is.
+  if (has0) {
+    typename Path::Out t;
+    Path::prep(a, lane, t);
+    Routes r = run_routes(s_rexp, s_rslot, Path::token(t), g_lo, K, cap, lane);
+    for (int64_t task = my0; task < t1; task += kWarps) {
+      const int64_t next = task + kWarps;
+      const bool more = next < t1;
+      typename Path::Raw an;
+      if (more) Path::load(p.d, next, p.tpr, lane, an);
+      Path::store(p.d, lane, t, r);
+      if (more) {
+        Path::prep(an, lane, t);
+        r = run_routes(s_rexp, s_rslot, next / p.tpr, g_lo, K, cap, lane);
+      }
+    }
+  }
+
+  // 6. the plan outputs: slot_of and src_of of the tokens whose segment 0
+  //    is in this block; each owner's counts and offsets rows
+  const int64_t gw0 = (t0 + p.tpr - 1) / p.tpr;
+  const int64_t gw1 = (t1 + p.tpr - 1) / p.tpr;
+  for (int i = tid; i < run; i += THREADS) {
+    const int64_t g = g_lo + i / K;
+    if (g >= gw0 && g < gw1) {
+      const int e = s_rexp[i], slot = s_rslot[i], q = lo_ent + i;
+      p.slot_of[q] = slot;
+      if (e >= 0 && slot < cap) p.src_of[(int64_t)e * cap + slot] = q;
+    }
+  }
+  for (int j = warp; j < p.owned; j += kWarps) {
+    const int e = own0 + j;
+    if (e >= E) break;
+    int32_t *row = p.expert_rank_offsets + (int64_t)e * (R + 1);
+    int sum = 0;
+    for (int r0 = 0; r0 < R; r0 += 32) {
+      const int r = r0 + lane;
+      const int c = r < R ? s_ocnt[j * R + r] : 0;
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += v;
+      }
+      if (r < R) row[r] = sum + incl - c;
+      sum += __shfl_sync(kFull, incl, 31);
+    }
+    if (lane == 0) {
+      row[R] = sum;
+      p.expert_num_tokens[e] = sum;
+    }
+  }
+  if (tid == 0) finish_status(p.d.hdr, arrived);
+}
+
+namespace {
+
+constexpr int kFusedFp8Threads = 768;    // 3 x 256: the fp8 dispatch's residency per SM
+constexpr int kFusedBf16Threads = 1024;  // 4 x 256: the bf16 dispatch's residency per SM
+
+template <class Path, int THREADS>
+cudaError_t launch_fused(const FusedParams &p, cudaStream_t stream) {
+  auto kern = plan_dispatch_kernel<Path, THREADS>;
+  if (p.smem_bytes > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)p.smem_bytes);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<p.grid, THREADS, p.smem_bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool plan_dispatch_geometry(const moe_shape &s, FusedParams &p) {
+  const int64_t N = (int64_t)s.num_ranks * s.tokens_per_rank;
+  if (N < 1 || N * s.top_k > kFusedMaxEntries) return false;
+  const bool fp8 = s.payload == MOE_PAYLOAD_FP8_E4M3;
+  int tpr;
+  if (fp8) {
+    const int nb = s.hidden / 128;
+    const int P = (nb % 2 == 0) ? pick_units(nb / 2, kFp8MaxPairs) : kFp8MaxPairs;
+    tpr = (nb + 2 * P - 1) / (2 * P);
+    p.units = P;
+  } else {
+    const int cpr = s.hidden / 8;
+    const int U = (cpr % 32 == 0) ? pick_units(cpr / 32, MOE_MAX_UNITS) : MOE_MAX_UNITS;
+    tpr = (cpr + 32 * U - 1) / (32 * U);
+    p.units = U;
+  }
+  const int64_t ntasks = N * tpr;
+  const int64_t sms = device_sm_count() < kFusedMaxGrid ? device_sm_count() : kFusedMaxGrid;
+  const int64_t q = (ntasks + sms - 1) / sms;
+  const int grid = (int)((ntasks + q - 1) / q);
+  const int owned = (s.num_experts + grid - 1) / grid;
+  const int64_t max_run = (q / tpr + 2) * s.top_k;
+  const size_t tab = ((size_t)(N * s.top_k) * 4 + 15) & ~(size_t)15;
+  const size_t smem = tab + (size_t)((s.num_experts + 15) & ~15) + 8 * (size_t)s.num_experts +
+                      4 * (size_t)owned * s.num_ranks + 8 * (size_t)max_run;
+  if (smem > kFusedMaxSmem) return false;
+  p.R = s.num_ranks;
+  p.T = s.tokens_per_rank;
+  p.tpr = tpr;
+  p.ntasks = ntasks;
+  p.q_tasks = (int)q;
+  p.grid = grid;
+  p.owned = owned;
+  p.max_run = (int)max_run;
+  int bits = 1;
+  while ((1 << bits) < s.num_experts) ++bits;
+  p.ebits = bits;
+  p.smem_bytes = smem;
+  return true;
+}
+
+cudaError_t launch_plan_dispatch(const FusedParams &p, bool fp8, cudaStream_t stream) {
+  if (fp8) {
+    if (p.units == 1) return launch_fused<Fp8Path<1>, kFusedFp8Threads>(p, stream);
+    return launch_fused<Fp8Path<kFp8MaxPairs>, kFusedFp8Threads>(p, stream);
+  }
+  switch (p.units) {
+    case 1: return launch_fused<Bf16Path<1>, kFusedBf16Threads>(p, stream);
+    case 2: return launch_fused<Bf16Path<2>, kFusedBf16Threads>(p, stream);
+    default: return launch_fused<Bf16Path<4>, kFusedBf16Threads>(p, stream);
+  }
+}
+
+}  // namespace moe

@@ -172,6 +172,35 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x,
                         void *expert_x, float *expert_x_scale,
                         void *workspace, void *stream);
 
+/* Plan and dispatch in one call: the outputs of moe_plan followed by
+ * moe_dispatch, bit for bit, from a single kernel launch where the shape
+ * allows it.
+ *
+ * Follows the passages of moe_plan and moe_dispatch.  At decode sizes the
+ * plan is a short chain of dependent steps whose latency, plus the kernel
+ * boundary, is a large part of plan + dispatch; here every thread block
+ * finds the slots of its own tokens by reading the routing table itself, so
+ * no block waits for another.  Taken when N*K <= 16384 and the block tables
+ * fit in shared memory; other shapes (and T = 0) run moe_plan and
+ * moe_dispatch, two launches, with the same results.
+ * In:   x, topk_idx as moe_dispatch and moe_plan.
+ * Out:  expert_num_tokens, expert_rank_offsets, slot_of, src_of as moe_plan;
+ *       expert_x, expert_x_scale as moe_dispatch.
+ * Work: as moe_plan (the status word is replaced by this call).
+ * Device errors: the status word and the plan outputs are exactly those of
+ *       moe_plan.  Unlike moe_dispatch, which writes nothing after a plan
+ *       error, rows of entries whose expert is in range and whose slot is
+ *       below cap may be written even when the status reports BAD_EXPERT or
+ *       CAPACITY: no block waits for the others' verdict.
+ * Ordering: not a programmatic dependent: the call waits for every earlier
+ *       kernel in the stream, as moe_plan does.
+ * Host errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA. */
+moe_status moe_plan_dispatch(const moe_shape *shape, const void *x, const int32_t *topk_idx,
+                             int32_t *expert_num_tokens, int32_t *expert_rank_offsets,
+                             int32_t *slot_of, int32_t *src_of, void *expert_x,
+                             float *expert_x_scale, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
 /* Combine: y[g] = bf16( sum over k of w[g,k] * expert_y[idx[g,k]][slot_of[g,k]] ).
  *
  * Follows "Efficient and portable mixture-of-experts communication",

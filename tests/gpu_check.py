@@ -12,6 +12,10 @@ Checks per call:
 * combine: within 1 bf16 ulp of the oracle (and the number of elements that
   are not bit-identical is reported); expert_y rows beyond each count are
   NaN, so any stray read would surface as NaN in y.
+With ``fused=True`` the plan and the dispatch are one moe_plan_dispatch
+call, checked the same way; after a data error it may have written rows of
+valid entries below cap, so there only "no row outside [0, min(count, cap))
+was written" is checked.
 """
 from __future__ import annotations
 
@@ -67,11 +71,15 @@ class Result(dict):
 
 def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
              payloads=("bf16", "fp8"), expert_y="host", combine_tokens=None, seed=0,
-             expect_status=None, masked=False, num_tokens=None) -> Result:
+             expect_status=None, masked=False, num_tokens=None, fused=False,
+             idx_device=None) -> Result:
     """Run plan/dispatch/combine on the GPU and compare with the oracle.
     ``expert_y``: "host" (seeded numpy, full [E,cap,H]) or "device" (seeded
     torch generator on the GPU, for shapes too large for the host).
-    ``combine_tokens``: token ids the oracle recomputes (None = all)."""
+    ``combine_tokens``: token ids the oracle recomputes (None = all).
+    ``fused``: plan and dispatch through moe_plan_dispatch.
+    ``idx_device``: the device copy of ``idx`` to pass (e.g. a view that is
+    not 16-byte aligned); default a fresh tensor."""
     N = R * T
     res = Result(mismatch={}, max_ulp=0, not_bit_exact=0)
     if masked:
@@ -88,7 +96,7 @@ def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
     if expect_status is None:
         expect_status = {oracle.OK: moe.Status.OK, oracle.CAPACITY: moe.Status.CAPACITY,
                          oracle.BAD_EXPERT: moe.Status.BAD_EXPERT}[st_o]
-    idx_d = dev(idx.astype(np.int32))
+    idx_d = dev(idx.astype(np.int32)) if idx_device is None else idx_device
     x_d = dev(x)
     w_d = dev(w.astype(np.float32))
     e_t = idx_d.long().view(-1)
@@ -103,9 +111,15 @@ def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
         if buf.expert_x_scale is not None:
             buf.expert_x_scale.fill_(SENTINEL_SCALE)
         buf.src_of.fill_(-1)
-        do_plan(buf)
+        if fused:
+            assert not masked
+            buf.plan_dispatch(x_d, idx_d)
+        else:
+            do_plan(buf)
         st = moe.read_status(buf.workspace)
         assert st == expect_status, f"plan status {st!r}, expected {expect_status!r}"
+        if expect_status == moe.Status.BAD_EXPERT and fused:
+            return res
         if expect_status == moe.Status.BAD_EXPERT:
             buf.dispatch(x_d, idx_d)
             torch.cuda.synchronize()
@@ -119,9 +133,14 @@ def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
         for e in range(E):
             n = min(int(cnt[e]), cap)
             assert np.array_equal(g_src[e, :n], src_o[e, :n]), f"src_of row {e}"
-        buf.dispatch(x_d, idx_d)
+        if not fused:
+            buf.dispatch(x_d, idx_d)
         torch.cuda.synchronize()
         touched = rows_touched(buf.expert_x, E, cap)
+        if expect_status == moe.Status.CAPACITY and fused:
+            below = populated_mask(np.minimum(cnt, cap), cap)
+            assert not (touched & ~below).any(), "fused call wrote a row outside [0, min(count, cap))"
+            continue
         if expect_status == moe.Status.CAPACITY:
             assert not touched.any(), "dispatch wrote rows although the plan reported CAPACITY"
             continue

@@ -96,6 +96,22 @@ def test_host_rejections_enqueue_nothing(lib):
     assert lib.moe_silu_mul_quant(sp, 256, None, _p(A), _p(A), _p(A), _p(A), None) == Status.INVALID_ARG
     assert lib.moe_silu_mul_quant(sp, 256, _p(A), _p(A), _p(A + 1), _p(A), _p(A), None) == Status.ALIGNMENT
     assert lib.moe_silu_mul_quant(sp, 256, _p(A), _p(A), _p(A), _p(A), None, None) == Status.WORKSPACE
+    # plan + dispatch in one call: the checks of both
+    pd = lib.moe_plan_dispatch
+    assert pd(sp, None, _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None, _p(A), ws_bytes, None) \
+        == Status.INVALID_ARG
+    assert pd(sp, _p(A), None, _p(A), _p(A), _p(A), _p(A), _p(A), None, _p(A), ws_bytes, None) \
+        == Status.INVALID_ARG
+    assert pd(sp, _p(A + 8), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None, _p(A), ws_bytes, None) \
+        == Status.ALIGNMENT
+    assert pd(sp, _p(A), _p(A + 2), _p(A), _p(A), _p(A), _p(A), _p(A), None, _p(A), ws_bytes, None) \
+        == Status.ALIGNMENT
+    assert pd(sp, _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None, _p(A), ws_bytes - 1, None) \
+        == Status.WORKSPACE
+    assert pd(ctypes.byref(s8), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None, _p(A), ws_bytes,
+              None) == Status.INVALID_ARG
+    assert pd(ctypes.byref(bad), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None, _p(A), 1 << 20,
+              None) == Status.INVALID_ARG
     out = ctypes.c_int(0)
     assert lib.moe_read_status(None, None, ctypes.byref(out)) == Status.INVALID_ARG
     assert lib.moe_workspace_init(None, 256, None) == Status.INVALID_ARG
