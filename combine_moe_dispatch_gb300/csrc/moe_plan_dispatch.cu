@@ -384,14 +384,22 @@ bool plan_dispatch_geometry(const moe_shape &s, FusedParams &p) {
 }
 
 cudaError_t launch_plan_dispatch(const FusedParams &p, bool fp8, cudaStream_t stream) {
+  // The kernel's task size must be the one the geometry was made for: the
+  // tasks per row (p.tpr) come from it, and the kernel indexes the blocks
+  // of a task with its own size.
   if (fp8) {
-    if (p.units == 1) return launch_fused<Fp8Path<1>, kFusedFp8Threads>(p, stream);
-    return launch_fused<Fp8Path<kFp8MaxPairs>, kFusedFp8Threads>(p, stream);
+    switch (p.units) {
+      case 1: return launch_fused<Fp8Path<1>, kFusedFp8Threads>(p, stream);
+      case 2: return launch_fused<Fp8Path<2>, kFusedFp8Threads>(p, stream);
+      case 4: return launch_fused<Fp8Path<4>, kFusedFp8Threads>(p, stream);
+      default: return cudaErrorInvalidValue;
+    }
   }
   switch (p.units) {
     case 1: return launch_fused<Bf16Path<1>, kFusedBf16Threads>(p, stream);
     case 2: return launch_fused<Bf16Path<2>, kFusedBf16Threads>(p, stream);
-    default: return launch_fused<Bf16Path<4>, kFusedBf16Threads>(p, stream);
+    case 4: return launch_fused<Bf16Path<4>, kFusedBf16Threads>(p, stream);
+    default: return cudaErrorInvalidValue;
   }
 }
 

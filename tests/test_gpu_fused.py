@@ -49,6 +49,8 @@ SMALL = [
     ("e2048", 1, 256, 256, 2048, 8, ("bf16", "fp8")),
     ("h8", 3, 17, 8, 5, 2, ("bf16",)),
     ("wide_rows", 2, 96, 7168, 64, 4, ("bf16", "fp8")),
+    ("two_pairs_per_task", 2, 64, 1536, 16, 4, ("bf16", "fp8")),     # 12 blocks: 3 tasks of 2 pairs
+    ("ten_pairs_per_row", 1, 48, 2560, 24, 2, ("bf16", "fp8")),      # 20 blocks: 5 tasks of 2 pairs
     ("at_the_limit", 2, 1024, 256, 128, 8, ("bf16", "fp8")),
     ("beyond_the_limit", 2, 1025, 256, 128, 8, ("bf16", "fp8")),
 ]
