@@ -47,13 +47,15 @@ from combine_moe_dispatch_gb300.configs import WORKLOADS  # noqa: E402
 with open(os.path.join(ROOT, "BASELINE.json")) as _f:
     METRIC = json.load(_f)["metric"]
 UNIT = "GB/s"
+_CSRC = "combine_moe_dispatch_gb300/csrc/"
+# the source files each timed kernel is built from (besides moe_common.cuh)
 KERNEL_SOURCES = {
-    "plan": "combine_moe_dispatch_gb300/csrc/moe_plan.cu",
-    "dispatch_bf16": "combine_moe_dispatch_gb300/csrc/moe_dispatch.cu",
-    "dispatch_fp8": "combine_moe_dispatch_gb300/csrc/moe_dispatch.cu",
-    "combine": "combine_moe_dispatch_gb300/csrc/moe_combine.cu",
-    "plan_dispatch_bf16": "combine_moe_dispatch_gb300/csrc/moe_plan_dispatch.cu",
-    "plan_dispatch_fp8": "combine_moe_dispatch_gb300/csrc/moe_plan_dispatch.cu",
+    "plan": (_CSRC + "moe_plan.cu",),
+    "dispatch_bf16": (_CSRC + "moe_dispatch.cu", _CSRC + "moe_dispatch_tasks.cuh"),
+    "dispatch_fp8": (_CSRC + "moe_dispatch.cu", _CSRC + "moe_dispatch_tasks.cuh"),
+    "combine": (_CSRC + "moe_combine.cu",),
+    "plan_dispatch_bf16": (_CSRC + "moe_plan_dispatch.cu", _CSRC + "moe_dispatch_tasks.cuh"),
+    "plan_dispatch_fp8": (_CSRC + "moe_plan_dispatch.cu", _CSRC + "moe_dispatch_tasks.cuh"),
 }
 # moe_plan_dispatch runs as one launch up to this many routed entries (N*K)
 FUSED_MAX_ENTRIES = 16384
@@ -133,11 +135,11 @@ def read_peaks():
 
 
 def source_hash(kernel: str) -> str:
-    """First 16 hex digits of the SHA-256 of the kernel's source file and the
-    shared header it includes: a recorded DRAM count is used only while both
-    are unchanged."""
+    """First 16 hex digits of the SHA-256 of the kernel's source files and the
+    shared header they include: a recorded DRAM count is used only while all
+    of them are unchanged."""
     h = hashlib.sha256()
-    for rel in (KERNEL_SOURCES[kernel], "combine_moe_dispatch_gb300/csrc/moe_common.cuh"):
+    for rel in KERNEL_SOURCES[kernel] + (_CSRC + "moe_common.cuh",):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -221,22 +221,31 @@ plan_dispatch_kernel(FusedParams p) {
     }
   } else {
     const int tk = p.T * K;      // entries per rank
-    auto visit = [&](int q, int e) {
-      if ((unsigned)e >= (unsigned)E) return;   // a bad id is reported by its run's block
-      if (q < lo_ent && s_code[e]) atomicAdd(&s_pre[e], 1);
+    // entry q of expert e: before the run and marked -> s_pre; owned -> its
+    // rank's counter.  The rank r = q / tk is computed once per 16 bytes.
+    auto visit = [&](int q, int e, int r) {
+      const bool ok = (unsigned)e < (unsigned)E;   // a bad id is reported by its run's block
+      const int ec = ok ? e : 0;
+      if (ok && q < lo_ent && s_code[ec]) atomicAdd(&s_pre[ec], 1);
       const unsigned o = (unsigned)(e - own0);
-      if (o < (unsigned)p.owned) atomicAdd(&s_ocnt[o * R + q / tk], 1);
+      if (ok && o < (unsigned)p.owned) atomicAdd(&s_ocnt[o * R + r], 1);
     };
     const int4 *t4 = reinterpret_cast<const int4 *>(s_tab);
     const int n4 = total >> 2;
     for (int j = tid - 32; j < n4; j += kScanners) {
       const int4 w = t4[j];
-      visit(4 * j, w.x);
-      visit(4 * j + 1, w.y);
-      visit(4 * j + 2, w.z);
-      visit(4 * j + 3, w.w);
+      const int q = 4 * j;
+      // q is a multiple of 4, so with tk >= 2 the 4 entries cross at most
+      // one rank boundary after q's own rank; tk = 1 divides each entry
+      const int r = q / tk;
+      const int nxt = (r + 1) * tk;
+      const bool one = tk >= 2;
+      visit(q, w.x, r);
+      visit(q + 1, w.y, one ? r + (q + 1 >= nxt) : (q + 1) / tk);
+      visit(q + 2, w.z, one ? r + (q + 2 >= nxt) : (q + 2) / tk);
+      visit(q + 3, w.w, one ? r + (q + 3 >= nxt) : (q + 3) / tk);
     }
-    for (int q = 4 * n4 + tid - 32; q < total; q += kScanners) visit(q, s_tab[q]);
+    for (int q = 4 * n4 + tid - 32; q < total; q += kScanners) visit(q, s_tab[q], q / tk);
   }
   __syncthreads();
 

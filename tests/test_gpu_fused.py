@@ -46,6 +46,8 @@ SMALL = [
     ("one_expert", 2, 33, 256, 1, 1, ("bf16", "fp8")),
     ("k32", 1, 50, 256, 40, 32, ("bf16", "fp8")),
     ("many_ranks", 64, 40, 256, 16, 2, ("bf16",)),
+    ("one_token_per_rank_k1", 64, 1, 256, 8, 1, ("bf16", "fp8")),  # a rank boundary every entry
+    ("one_token_per_rank_k3", 40, 1, 256, 8, 3, ("bf16",)),
     ("e2048", 1, 256, 256, 2048, 8, ("bf16", "fp8")),
     ("h8", 3, 17, 8, 5, 2, ("bf16",)),
     ("wide_rows", 2, 96, 7168, 64, 4, ("bf16", "fp8")),
