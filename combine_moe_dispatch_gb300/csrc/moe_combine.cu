@@ -63,9 +63,11 @@ combine_kernel(CombineParams p) {
   const int tpr = (cpr + cpt - 1) / cpt;
   const int64_t ntasks = (int64_t)p.N * tpr;
 
-  for (int64_t task = warp0; task < ntasks; task += nwarps) {
-    const int64_t g = task / tpr;
-    const int seg = (int)(task - g * tpr);
+  if (warp0 >= ntasks) return;
+  TaskCursor cur(warp0, nwarps, tpr);
+  for (int64_t task = warp0; task < ntasks; task += nwarps, cur = cur.next()) {
+    const int64_t g = cur.g;
+    const int seg = cur.seg;
     int e_l = -1, s_l = -1;
     float w_l = 0.0f;
     if (lane < p.K) {

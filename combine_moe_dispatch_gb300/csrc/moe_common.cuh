@@ -317,6 +317,32 @@ __device__ __forceinline__ int ld_dsmem(const int32_t *local, uint32_t rank) {
   return v;
 }
 
+// (token, segment) of a warp's tasks task0, task0 + stride, task0 + 2 stride,
+// ...: the stride's whole rows and remainder are found once, so stepping to
+// the next task needs no 64-bit division.  32-bit fields: tokens are below
+// 2^31 (N*K < 2^31) and the stride is a grid's warps.
+struct TaskCursor {
+  int g, seg, dg, dseg, tpr;
+  __device__ __forceinline__ TaskCursor(int64_t task0, int64_t stride, int tpr_) {
+    tpr = tpr_;
+    const int64_t g0 = task0 / tpr_;
+    g = (int)g0;
+    seg = (int)(task0 - g0 * tpr_);
+    dg = (int)(stride / tpr_);
+    dseg = (int)(stride - (int64_t)dg * tpr_);
+  }
+  __device__ __forceinline__ TaskCursor next() const {
+    TaskCursor n = *this;
+    n.g += dg;
+    n.seg += dseg;
+    if (n.seg >= tpr) {
+      n.seg -= tpr;
+      ++n.g;
+    }
+    return n;
+  }
+};
+
 // Lanes of this warp whose key equals this lane's key (keys < 2^bits, or -1
 // for "no key", which matches only other -1 lanes).  Every lane executes
 // every ballot (no lane leaves early), as the full-warp ballots require.

@@ -75,18 +75,20 @@ dispatch_bf16_kernel(DispatchParams p) {
   // The first task's read of x needs nothing from the plan: issue it before
   // waiting for the plan to finish.
   if (warp0 >= ntasks) return;
+  TaskCursor cur(warp0, nwarps, tpr);
   Bf16Task<U> t;
-  bf16_load<U>(p, warp0, tpr, lane, t);
+  bf16_load<U>(p, cur.g, cur.seg, lane, t);
   if (!wait_plan_ok(p.hdr, lane)) return;
   Routes r = load_routes(p, t.g, lane);
   // Software pipeline: the next task's loads go out before this task's stores.
   for (int64_t task = warp0; task < ntasks; task += nwarps) {
     const int64_t next = task + nwarps;
     const bool more = next < ntasks;
+    cur = cur.next();
     Bf16Task<U> tn;
     Routes rn;
     if (more) {
-      bf16_load<U>(p, next, tpr, lane, tn);
+      bf16_load<U>(p, cur.g, cur.seg, lane, tn);
       rn = load_routes(p, tn.g, lane);
     }
     bf16_store<U>(p, lane, t, r);
@@ -111,9 +113,11 @@ dispatch_fp8_kernel(DispatchParams p) {
   // they run before waiting for the plan to finish.  Then software-pipeline
   // the tasks: the next task's x and routing loads are issued before this
   // task's stores, and it is quantised while those stores drain.
+  // (The token and segment of a task come from a division here: a
+  // TaskCursor's registers would make this kernel spill at its 80.)
   if (warp0 >= ntasks) return;
   Fp8Raw<P> a;
-  fp8_load<P>(p, warp0, tpr, lane, a);
+  fp8_load<P>(p, warp0 / tpr, (int)(warp0 % tpr), lane, a);
   Fp8Task<P> t;
   fp8_quantise<P>(a, lane, t);
   if (!wait_plan_ok(p.hdr, lane)) return;
@@ -123,8 +127,9 @@ dispatch_fp8_kernel(DispatchParams p) {
     const bool more = next < ntasks;
     Routes rn;
     if (more) {
-      fp8_load<P>(p, next, tpr, lane, a);
-      rn = load_routes(p, next / tpr, lane);
+      const int64_t g = next / tpr;
+      fp8_load<P>(p, g, (int)(next - g * tpr), lane, a);
+      rn = load_routes(p, g, lane);
     }
     fp8_store<P>(p, lane, t, r);
     if (more) {

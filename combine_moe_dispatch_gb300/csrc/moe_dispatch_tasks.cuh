@@ -9,6 +9,7 @@
 
 namespace moe {
 
+
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
@@ -42,11 +43,11 @@ struct Bf16Task {
 };
 
 template <int U>
-__device__ __forceinline__ void bf16_load(const DispatchParams &p, int64_t task, int tpr, int lane,
+__device__ __forceinline__ void bf16_load(const DispatchParams &p, int64_t g, int seg, int lane,
                                           Bf16Task<U> &t) {
   const int cpr = p.H / 8;
-  t.g = task / tpr;
-  t.seg = (int)(task - t.g * tpr);
+  t.g = g;
+  t.seg = seg;
   const uint16_t *src = p.x + t.g * p.H;
   const int c0 = t.seg * 32 * U + lane;
 #pragma unroll
@@ -93,13 +94,13 @@ struct Fp8Task {     // one task's output
 };
 
 template <int P>
-__device__ __forceinline__ void fp8_load(const DispatchParams &p, int64_t task, int tpr, int lane,
+__device__ __forceinline__ void fp8_load(const DispatchParams &p, int64_t g, int seg, int lane,
                                          Fp8Raw<P> &a) {
   const int half = lane >> 4;
   const int sub = lane & 15;
   const int nb = p.H / 128;
-  a.g = task / tpr;
-  a.seg = (int)(task - a.g * tpr);
+  a.g = g;
+  a.seg = seg;
   const uint16_t *src = p.x + a.g * p.H;
 #pragma unroll
   for (int it = 0; it < P; ++it) {

@@ -66,9 +66,9 @@ template <int U>
 struct Bf16Path {
   using Raw = Bf16Task<U>;
   using Out = Bf16Task<U>;
-  static __device__ __forceinline__ void load(const DispatchParams &p, int64_t task, int tpr,
+  static __device__ __forceinline__ void load(const DispatchParams &p, const TaskCursor &c,
                                               int lane, Raw &a) {
-    bf16_load<U>(p, task, tpr, lane, a);
+    bf16_load<U>(p, c.g, c.seg, lane, a);
   }
   static __device__ __forceinline__ void prep(const Raw &a, int, Out &t) { t = a; }
   static __device__ __forceinline__ void store(const DispatchParams &p, int lane, const Out &t,
@@ -82,9 +82,9 @@ template <int P>
 struct Fp8Path {
   using Raw = Fp8Raw<P>;
   using Out = Fp8Task<P>;
-  static __device__ __forceinline__ void load(const DispatchParams &p, int64_t task, int tpr,
+  static __device__ __forceinline__ void load(const DispatchParams &p, const TaskCursor &c,
                                               int lane, Raw &a) {
-    fp8_load<P>(p, task, tpr, lane, a);
+    fp8_load<P>(p, c.g, c.seg, lane, a);
   }
   static __device__ __forceinline__ void prep(const Raw &a, int lane, Out &t) {
     fp8_quantise<P>(a, lane, t);
@@ -170,8 +170,9 @@ plan_dispatch_kernel(FusedParams p) {
   for (int q = nbulk + tid; q < total; q += THREADS) s_tab[q] = __ldg(p.topk_idx + q);
   const int64_t my0 = t0 + warp;
   const bool has0 = my0 < t1;
+  TaskCursor cur(my0, kWarps, p.tpr);
   typename Path::Raw a;
-  if (has0) Path::load(p.d, my0, p.tpr, lane, a);
+  if (has0) Path::load(p.d, cur, lane, a);
   for (int i = tid; i < E; i += THREADS) {
     s_code[i] = 0;
     s_pre[i] = 0;
@@ -285,12 +286,13 @@ plan_dispatch_kernel(FusedParams p) {
     for (int64_t task = my0; task < t1; task += kWarps) {
       const int64_t next = task + kWarps;
       const bool more = next < t1;
+      cur = cur.next();
       typename Path::Raw an;
-      if (more) Path::load(p.d, next, p.tpr, lane, an);
+      if (more) Path::load(p.d, cur, lane, an);
       Path::store(p.d, lane, t, r);
       if (more) {
         Path::prep(an, lane, t);
-        r = run_routes(s_rexp, s_rslot, next / p.tpr, g_lo, K, cap, lane);
+        r = run_routes(s_rexp, s_rslot, cur.g, g_lo, K, cap, lane);
       }
     }
   }
