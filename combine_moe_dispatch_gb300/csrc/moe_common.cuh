@@ -465,10 +465,25 @@ __device__ __forceinline__ uint2 quant_bytes8_exact(const float (&f)[8], float s
 // and RN(x * rh) above it likewise; rounding to E4M3 is monotone, so a byte
 // where lo and hi agree is e4m3(RN(x / scale)).  (Below the normal range
 // every candidate rounds to a zero of x's sign.)
+// (x0 * s, x1 * s), each rounded to nearest even (IEEE binary32, no flush
+// to zero): one packed two-lane multiply of sm_100-class GPUs.
+__device__ __forceinline__ void fmul2_rn(float x0, float x1, float s, float &y0, float &y1) {
+  uint64_t a, b, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(b) : "f"(s));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(y0), "=f"(y1) : "l"(r));
+}
+
 __device__ __forceinline__ void quant_window4(float a, float b, float c, float d, float rl, float rh,
                                               uint32_t &lo, uint32_t &hi) {
-  lo = e4m3x4(__fmul_rn(a, rl), __fmul_rn(b, rl), __fmul_rn(c, rl), __fmul_rn(d, rl));
-  hi = e4m3x4(__fmul_rn(a, rh), __fmul_rn(b, rh), __fmul_rn(c, rh), __fmul_rn(d, rh));
+  float al, bl, cl, dl, ah, bh, ch, dh;
+  fmul2_rn(a, b, rl, al, bl);
+  fmul2_rn(c, d, rl, cl, dl);
+  fmul2_rn(a, b, rh, ah, bh);
+  fmul2_rn(c, d, rh, ch, dh);
+  lo = e4m3x4(al, bl, cl, dl);
+  hi = e4m3x4(ah, bh, ch, dh);
 }
 
 // rl and rh of quant_window4.
