@@ -127,3 +127,16 @@ def test_missing_library_fails_loudly(tmp_path):
             moe.load_library(str(tmp_path / "nope.so"))
     finally:
         moe._lib = saved
+
+
+def test_bench_knows_the_fused_limit():
+    """bench.py counts one launch for moe_plan_dispatch up to the library's
+    fused limit and two beyond it: the two constants must agree."""
+    import importlib.util
+    src = open(os.path.join(ROOT, "combine_moe_dispatch_gb300", "csrc", "moe_common.cuh")).read()
+    m = re.search(r"kFusedMaxEntries\s*=\s*(\d+)", src)
+    assert m, "kFusedMaxEntries not found"
+    spec = importlib.util.spec_from_file_location("bench_for_test", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    assert bench.FUSED_MAX_ENTRIES == int(m.group(1))
