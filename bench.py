@@ -44,8 +44,7 @@ sys.path.insert(0, ROOT)
 from combine_moe_dispatch_gb300 import inputs  # noqa: E402
 from combine_moe_dispatch_gb300.configs import WORKLOADS  # noqa: E402
 
-with open(os.path.join(ROOT, "BASELINE.json")) as _f:
-    METRIC = json.load(_f)["metric"]
+METRIC = "dispatch/combine µs and HBM GB/s (% of peak), DeepSeek-V3 shape, 1 GB300"
 UNIT = "GB/s"
 _CSRC = "combine_moe_dispatch_gb300/csrc/"
 # the source files each timed kernel is built from (besides moe_common.cuh)
