@@ -133,14 +133,22 @@ def read_peaks():
     return 6800.0, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and blank lines: what a change must
+    touch to change the compiled kernel."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.strip() for line in text.splitlines() if line.strip())
+
+
 def source_hash(kernel: str) -> str:
-    """First 16 hex digits of the SHA-256 of the kernel's source files and the
-    shared header they include: a recorded DRAM count is used only while all
-    of them are unchanged."""
+    """First 16 hex digits of the SHA-256 of the code (comments left out) of
+    the kernel's source files and the shared header they include: a recorded
+    DRAM count is used only while all of them are unchanged."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel] + (_CSRC + "moe_common.cuh",):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

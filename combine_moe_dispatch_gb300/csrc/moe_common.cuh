@@ -57,8 +57,9 @@ struct WsHeader {
   int32_t status;       // moe_status of the last plan (and of later dispatch/combine)
   uint32_t debug_flags; // kDebug* test hooks
   uint64_t timeout_ns;  // limit of every wait; 0 = kDefaultTimeoutNs
-  uint32_t arrivals;    // fused plan+dispatch: blocks arrived (bits 0-15), blocks that saw a
-                        // bad expert (16-23) or an over-capacity expert (24-31); reset by the last
+  uint32_t arrivals;    // fused plan+dispatch: blocks arrived (bits 0-7), blocks whose table
+                        // copy timed out (8-15), that saw a bad expert (16-23) or an
+                        // over-capacity expert (24-31); reset by the last block to arrive
   uint32_t reserved[55];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");

@@ -120,8 +120,9 @@ __device__ __forceinline__ uint32_t arrival_code(uint32_t err) {
          ((err & kErrCapacity) ? 1u << 24 : 0u);
 }
 
-// Called by the block's thread 0 with the arrival word after its own add:
-// the last block to arrive writes the status word and resets the count.
+// Called by the one thread of a block that made the block's add, with the
+// arrival word after that add: the last block to arrive writes the status
+// word and resets the count.
 __device__ __forceinline__ void finish_status(WsHeader *hdr, uint32_t arrived) {
   if ((arrived & 0xFFu) != gridDim.x) return;
   hdr->status = ((arrived >> 8) & 0xFFu)    ? MOE_ERR_TIMEOUT
