@@ -361,6 +361,19 @@ cudaError_t launch_fused(const FusedParams &p, cudaStream_t stream) {
 
 }  // namespace
 
+// Task size of the fused kernel: up to 4 block pairs (fp8) or 4 chunks per
+// lane (bf16), 1024 elements.  Half-size tasks, which start the first
+// stores after half the quantisation, measured slower at DeepSeek-V3
+// decode: fp8 18.7 against 17.3 us, bf16 25.8 against 24.0 us.
+#ifndef MOE_FUSED_FP8_MAX_PAIRS
+#define MOE_FUSED_FP8_MAX_PAIRS 4
+#endif
+#ifndef MOE_FUSED_BF16_MAX_UNITS
+#define MOE_FUSED_BF16_MAX_UNITS 4
+#endif
+constexpr int kFusedFp8MaxPairs = MOE_FUSED_FP8_MAX_PAIRS;
+constexpr int kFusedBf16MaxUnits = MOE_FUSED_BF16_MAX_UNITS;
+
 bool plan_dispatch_geometry(const moe_shape &s, FusedParams &p) {
   const int64_t N = (int64_t)s.num_ranks * s.tokens_per_rank;
   if (N < 1 || N * s.top_k > kFusedMaxEntries) return false;
@@ -368,12 +381,12 @@ bool plan_dispatch_geometry(const moe_shape &s, FusedParams &p) {
   int tpr;
   if (fp8) {
     const int nb = s.hidden / 128;
-    const int P = (nb % 2 == 0) ? pick_units(nb / 2, kFp8MaxPairs) : kFp8MaxPairs;
+    const int P = (nb % 2 == 0) ? pick_units(nb / 2, kFusedFp8MaxPairs) : kFusedFp8MaxPairs;
     tpr = (nb + 2 * P - 1) / (2 * P);
     p.units = P;
   } else {
     const int cpr = s.hidden / 8;
-    const int U = (cpr % 32 == 0) ? pick_units(cpr / 32, MOE_MAX_UNITS) : MOE_MAX_UNITS;
+    const int U = (cpr % 32 == 0) ? pick_units(cpr / 32, kFusedBf16MaxUnits) : kFusedBf16MaxUnits;
     tpr = (cpr + 32 * U - 1) / (32 * U);
     p.units = U;
   }
