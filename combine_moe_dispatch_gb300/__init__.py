@@ -19,6 +19,7 @@ from . import buildlib as _build
 
 PAYLOAD_BF16 = 0
 PAYLOAD_FP8_E4M3 = 1
+PAYLOAD_FP8_E4M3_TSCALE = 2   # E4M3 bytes, scales [E, H/128, cap]
 
 
 class Status(enum.IntEnum):
@@ -54,10 +55,14 @@ class Shape(ctypes.Structure):
     def N(self) -> int:
         return self.num_ranks * self.tokens_per_rank
 
+    @property
+    def fp8(self) -> bool:
+        return self.payload != PAYLOAD_BF16
+
     def __repr__(self):
         return (f"Shape(R={self.num_ranks}, T={self.tokens_per_rank}, H={self.hidden}, "
                 f"E={self.num_experts}, K={self.top_k}, cap={self.capacity}, "
-                f"payload={'fp8' if self.payload else 'bf16'})")
+                f"payload={['bf16', 'fp8', 'fp8, transposed scales'][self.payload]})")
 
 
 def make_shape(R, T, H, E, K, cap, payload=PAYLOAD_BF16) -> Shape:
@@ -246,7 +251,8 @@ def workspace_set_debug(workspace, flags: int, timeout_ns: int = 0, stream=None,
 class Buffers:
     """Device buffers of one shape, allocated with torch (the library itself
     allocates nothing).  ``expert_x`` is uint8 [E, cap, H] for the fp8
-    payload, bf16 otherwise; ``expert_x_scale`` is None for bf16."""
+    payloads, bf16 otherwise; ``expert_x_scale`` is [E, cap, H/128], or
+    [E, H/128, cap] for PAYLOAD_FP8_E4M3_TSCALE, and None for bf16."""
 
     def __init__(self, shape: Shape, device="cuda", expert_y: bool = True, expert_x: bool = True):
         import torch
@@ -265,9 +271,10 @@ class Buffers:
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
         if not expert_x:
             self.expert_x = self.expert_x_scale = None
-        elif shape.payload == PAYLOAD_FP8_E4M3:
+        elif shape.fp8:
             self.expert_x = torch.empty((E, cap, H), dtype=torch.uint8, device=device)
-            self.expert_x_scale = torch.empty((E, cap, H // 128), dtype=torch.float32, device=device)
+            sdims = (E, H // 128, cap) if shape.payload == PAYLOAD_FP8_E4M3_TSCALE else (E, cap, H // 128)
+            self.expert_x_scale = torch.empty(sdims, dtype=torch.float32, device=device)
         else:
             self.expert_x = torch.empty((E, cap, H), dtype=torch.bfloat16, device=device)
             self.expert_x_scale = None

@@ -149,7 +149,7 @@ __device__ __forceinline__ void load_task(const ActParams &p, int64_t row, int s
 // One task: SiLU(gate) * up for the 2P blocks in gv/uv, the block scales
 // (computed once each, by lanes 0 .. 2P-1, which also store them) and the
 // E4M3 bytes.  All 32 lanes call it together.
-template <int P, bool EXACT>
+template <int P, bool EXACT, bool TS>
 __device__ __forceinline__ void act_task(const ActParams &p, const float *s_tab, int64_t row, int seg,
                                          int lane, int nb, const uint4 (&gv)[P], const uint4 (&uv)[P]) {
   const int half = lane >> 4;
@@ -211,7 +211,15 @@ __device__ __forceinline__ void act_task(const ActParams &p, const float *s_tab,
   for (int it = 0; it < P; ++it) {
     if (EXACT || seg * bpt + it * 2 + half < nb) *reinterpret_cast<uint2 *>(qrow + it * 256) = q[it];
   }
-  if (lane < min(bpt, nb - seg * bpt)) p.act_scale[row * nb + seg * bpt + lane] = my_scale;
+  if (lane < min(bpt, nb - seg * bpt)) {
+    const int blk = seg * bpt + lane;
+    int64_t at = row * nb + blk;                      // [E, cap, I/128]
+    if (TS) {                                         // [E, I/128, cap]; E * cap < 2^31
+      const int e = (int)row / p.cap, s = (int)row - e * p.cap;
+      at = ((int64_t)e * nb + blk) * p.cap + s;
+    }
+    p.act_scale[at] = my_scale;
+  }
 }
 
 // Walks a warp's contiguous range of (populated row, segment) tasks.
@@ -228,7 +236,7 @@ struct ActCursor {
   }
 };
 
-template <int P, bool EXACT>
+template <int P, bool EXACT, bool TS>
 __global__ void __launch_bounds__(kActThreads, P >= 2 ? 3 : 1)
 silu_quant_kernel(ActParams p) {
   __shared__ __align__(16) float s_tab[kSiluTabEntries];
@@ -270,24 +278,24 @@ silu_quant_kernel(ActParams p) {
     ActCursor nc = c;
     nc.next(s_prefix, p.E, p.cap, tpr);
     if (n > 1) load_task<P, EXACT>(p, nc.row, nc.seg, half, sub, nb, gb, ub);
-    act_task<P, EXACT>(p, s_tab, c.row, c.seg, lane, nb, ga, ua);
+    act_task<P, EXACT, TS>(p, s_tab, c.row, c.seg, lane, nb, ga, ua);
     if (--n == 0) break;
     c = nc;
     nc.next(s_prefix, p.E, p.cap, tpr);
     if (n > 1) load_task<P, EXACT>(p, nc.row, nc.seg, half, sub, nb, ga, ua);
-    act_task<P, EXACT>(p, s_tab, c.row, c.seg, lane, nb, gb, ub);
+    act_task<P, EXACT, TS>(p, s_tab, c.row, c.seg, lane, nb, gb, ub);
     if (--n == 0) break;
     c = nc;
   }
 }
 
 namespace {
-template <int P, bool EXACT>
+template <int P, bool EXACT, bool TS>
 cudaError_t launch_p(const ActParams &p, cudaStream_t stream) {
   const size_t smem = (size_t)(p.E + 1) * sizeof(int32_t);
   // enough warps for every row of every expert at full capacity, capped at a full device
   const int64_t tasks = (int64_t)p.E * p.cap * ((p.I / 128 + 2 * P - 1) / (2 * P));
-  const int grid = persistent_grid((const void *)silu_quant_kernel<P, EXACT>, kActThreads, tasks);
+  const int grid = persistent_grid((const void *)silu_quant_kernel<P, EXACT, TS>, kActThreads, tasks);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -298,16 +306,23 @@ cudaError_t launch_p(const ActParams &p, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, silu_quant_kernel<P, EXACT>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, silu_quant_kernel<P, EXACT, TS>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 }  // namespace
 
-cudaError_t launch_silu_quant(const ActParams &p, cudaStream_t stream) {
+template <bool TS>
+cudaError_t launch_layout(const ActParams &p, cudaStream_t stream) {
   const int nb = p.I / 128;
-  if (nb % 4 == 0) return launch_p<2, true>(p, stream);
-  if (nb % 2 == 0) return launch_p<1, true>(p, stream);
-  return launch_p<1, false>(p, stream);
+  if (nb % 4 == 0) return launch_p<2, true, TS>(p, stream);
+  if (nb % 2 == 0) return launch_p<1, true, TS>(p, stream);
+  return launch_p<1, false, TS>(p, stream);
+}
+
+cudaError_t launch_silu_quant(const ActParams &p, cudaStream_t stream) {
+  // the scale layout is a template parameter: the default layout's kernel
+  // carries no code for the other
+  return p.scale_t ? launch_layout<true>(p, stream) : launch_layout<false>(p, stream);
 }
 
 }  // namespace moe

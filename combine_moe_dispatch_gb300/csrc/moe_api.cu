@@ -63,14 +63,15 @@ moe_status check_shape(const moe_shape *s) {
   if (s->num_ranks <= 0 || s->tokens_per_rank < 0 || s->hidden <= 0 || s->num_experts <= 0 ||
       s->top_k <= 0 || s->capacity <= 0)
     return MOE_ERR_INVALID_ARG;
-  if (s->payload != MOE_PAYLOAD_BF16 && s->payload != MOE_PAYLOAD_FP8_E4M3)
+  if (s->payload != MOE_PAYLOAD_BF16 && s->payload != MOE_PAYLOAD_FP8_E4M3 &&
+      s->payload != MOE_PAYLOAD_FP8_E4M3_TSCALE)
     return MOE_ERR_INVALID_ARG;
   if (s->top_k > kMaxTopK || s->num_experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   const int64_t N = (int64_t)s->num_ranks * s->tokens_per_rank;
   if (N * s->top_k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)s->num_experts * s->capacity >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if (s->hidden % 8 != 0) return MOE_ERR_UNSUPPORTED;
-  if (s->payload == MOE_PAYLOAD_FP8_E4M3 && s->hidden % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (s->payload != MOE_PAYLOAD_BF16 && s->hidden % 128 != 0) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -175,7 +176,7 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *to
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   if (shape->tokens_per_rank == 0) return MOE_OK;   // empty batch: nothing to read or write
-  const bool fp8 = shape->payload == MOE_PAYLOAD_FP8_E4M3;
+  const bool fp8 = shape->payload != MOE_PAYLOAD_BF16;
   if (!x || !topk_idx || !slot_of || !expert_x || (fp8 && !expert_x_scale))
     return MOE_ERR_INVALID_ARG;
   if (!workspace) return MOE_ERR_WORKSPACE;
@@ -194,6 +195,7 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *to
   p.E = shape->num_experts;
   p.K = shape->top_k;
   p.cap = shape->capacity;
+  p.scale_t = shape->payload == MOE_PAYLOAD_FP8_E4M3_TSCALE;
   cudaStream_t s = (cudaStream_t)stream;
   return from_cuda(fp8 ? launch_dispatch_fp8(p, s) : launch_dispatch_bf16(p, s));
 }
@@ -205,7 +207,7 @@ moe_status moe_plan_dispatch(const moe_shape *shape, const void *x, const int32_
                              void *stream) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
-  const bool fp8 = shape->payload == MOE_PAYLOAD_FP8_E4M3;
+  const bool fp8 = shape->payload != MOE_PAYLOAD_BF16;
   const bool empty = shape->tokens_per_rank == 0;
   if (!empty && (!x || !expert_x || (fp8 && !expert_x_scale))) return MOE_ERR_INVALID_ARG;
   if (!empty && (!aligned(x, 16) || !aligned(expert_x, 16) || (fp8 && !aligned(expert_x_scale, 4))))
@@ -235,6 +237,7 @@ moe_status moe_plan_dispatch(const moe_shape *shape, const void *x, const int32_
   f.d.E = shape->num_experts;
   f.d.K = shape->top_k;
   f.d.cap = shape->capacity;
+  f.d.scale_t = shape->payload == MOE_PAYLOAD_FP8_E4M3_TSCALE;
   f.topk_idx = topk_idx;
   f.expert_num_tokens = expert_num_tokens;
   f.expert_rank_offsets = expert_rank_offsets;
@@ -339,6 +342,7 @@ moe_status moe_silu_mul_quant(const moe_shape *shape, int32_t intermediate, cons
   p.E = shape->num_experts;
   p.cap = shape->capacity;
   p.I = intermediate;
+  p.scale_t = shape->payload == MOE_PAYLOAD_FP8_E4M3_TSCALE;
   return from_cuda(launch_silu_quant(p, (cudaStream_t)stream));
 }
 

@@ -126,6 +126,7 @@ struct DispatchParams {
   float *expert_x_scale;
   WsHeader *hdr;
   int N, H, E, K, cap;
+  int scale_t;                 // fp8: scales [E, H/128, cap] instead of [E, cap, H/128]
 };
 
 // Plan and dispatch in one launch (moe_plan_dispatch.cu): taken up to
@@ -170,9 +171,10 @@ struct ActParams {
   const uint16_t *expert_h;          // [E, cap, 2I] bf16: gate | up
   const int32_t *expert_num_tokens;  // [E]
   void *act_q;                       // [E, cap, I] e4m3
-  float *act_scale;                  // [E, cap, I/128]
+  float *act_scale;                  // [E, cap, I/128], or [E, I/128, cap] with scale_t
   WsHeader *hdr;
   int E, cap, I;
+  int scale_t;
 };
 
 struct RouterParams {

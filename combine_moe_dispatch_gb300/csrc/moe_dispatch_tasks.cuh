@@ -205,7 +205,11 @@ __device__ __forceinline__ void fp8_store(const DispatchParams &p, int lane, con
         if (blk < nb) *reinterpret_cast<uint2 *>(dst + (int64_t)blk * 128 + sub * 8) = t.q[it];
       }
     }
-    if (lane < nscale) p.expert_x_scale[row * nb + t.seg * bpt + lane] = t.my_scale;
+    if (lane < nscale) {
+      const int blk = t.seg * bpt + lane;
+      const int64_t at = p.scale_t ? ((int64_t)e * nb + blk) * p.cap + s : row * nb + blk;
+      p.expert_x_scale[at] = t.my_scale;
+    }
   }
 }
 

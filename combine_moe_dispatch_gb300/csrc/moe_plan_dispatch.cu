@@ -377,7 +377,7 @@ constexpr int kFusedBf16MaxUnits = MOE_FUSED_BF16_MAX_UNITS;
 bool plan_dispatch_geometry(const moe_shape &s, FusedParams &p) {
   const int64_t N = (int64_t)s.num_ranks * s.tokens_per_rank;
   if (N < 1 || N * s.top_k > kFusedMaxEntries) return false;
-  const bool fp8 = s.payload == MOE_PAYLOAD_FP8_E4M3;
+  const bool fp8 = s.payload != MOE_PAYLOAD_BF16;
   int tpr;
   if (fp8) {
     const int nb = s.hidden / 128;

@@ -57,7 +57,11 @@ typedef enum {
 
 typedef enum {
   MOE_PAYLOAD_BF16 = 0,     /* expert_x rows are bf16 copies of x */
-  MOE_PAYLOAD_FP8_E4M3 = 1  /* expert_x rows are OCP E4M3 bytes + fp32 scales */
+  MOE_PAYLOAD_FP8_E4M3 = 1, /* expert_x rows are OCP E4M3 bytes + fp32 scales [E, cap, H/128] */
+  MOE_PAYLOAD_FP8_E4M3_TSCALE = 2  /* the same bytes; the scales transposed per expert,
+                                      [E, H/128, cap], as a grouped GEMM loads them: the
+                                      scales of one 128-column block of one expert's rows
+                                      are contiguous */
 } moe_payload;
 
 /* Problem shape.  Limits: all sizes >= 1 except T, which may be 0 (an empty
@@ -150,8 +154,9 @@ moe_status moe_plan_masked(const moe_shape *shape, const int32_t *topk_idx,
  * Out:  expert_x     [E, cap, H]: bf16 (payload BF16) or E4M3 bytes (payload
  *                    FP8_E4M3), 16-byte aligned.  Row (e, s) is written only
  *                    for s < count[e]; other rows are not touched.
- *       expert_x_scale [E, cap, H/128] fp32 for FP8_E4M3 (4-byte aligned),
- *                    NULL for BF16.  Per 128-block: scale = amax / 448,
+ *       expert_x_scale [E, cap, H/128] fp32 for FP8_E4M3, [E, H/128, cap] for
+ *                    FP8_E4M3_TSCALE (4-byte aligned), NULL for BF16.  Per
+ *                    128-block: scale = amax / 448,
  *                    q = e4m3_rn_satfinite(x / scale); an all-zero block has
  *                    scale 0 and q = 0.
  * Work: the workspace moe_plan used; the call writes nothing if its status
@@ -274,7 +279,8 @@ moe_status moe_router_topk(const moe_shape *shape, const float *logits, int32_t 
  * In:   expert_h [E, cap, 2*intermediate] bf16, 16-byte aligned;
  *       expert_num_tokens [E] int32 (from moe_plan);
  * Out:  act_q [E, cap, intermediate] E4M3 (16-byte aligned) and act_scale
- *       [E, cap, intermediate/128] fp32, rows below the count only.
+ *       [E, cap, intermediate/128] fp32, or [E, intermediate/128, cap] when
+ *       shape->payload is FP8_E4M3_TSCALE; rows below the count only.
  * Work: the workspace of the plan that produced the counts; nothing is
  *       written if its status word is set.  Uses E and cap of `shape`.
  * Errors: INVALID_ARG, UNSUPPORTED (intermediate % 128 != 0), ALIGNMENT,

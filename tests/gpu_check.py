@@ -104,7 +104,8 @@ def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
     bf16_buf = None
 
     for payload in payloads:
-        code = moe.PAYLOAD_FP8_E4M3 if payload == "fp8" else moe.PAYLOAD_BF16
+        code = {"bf16": moe.PAYLOAD_BF16, "fp8": moe.PAYLOAD_FP8_E4M3,
+                "fp8t": moe.PAYLOAD_FP8_E4M3_TSCALE}[payload]
         shape = moe.make_shape(R, T, H, E, K, cap, code)
         buf = moe.Buffers(shape, expert_y=False)
         buf.expert_x.view(torch.uint8).fill_(SENTINEL_BYTE)
@@ -162,11 +163,13 @@ def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
             exp_q = np.repeat(q_o[0], K, axis=0)[sel]
             bad = np.nonzero((got_q != exp_q).any(axis=1))[0]
             assert bad.size == 0, f"fp8 bytes differ in {bad.size} rows (first entry {bad[:4]})"
-            got_s = buf.expert_x_scale[e_t[sel_d], s_t[sel_d]].cpu().numpy()
+            # the scales as [E, cap, H/128] whatever the layout
+            sc_rows = buf.expert_x_scale.transpose(1, 2) if payload == "fp8t" else buf.expert_x_scale
+            got_s = sc_rows[e_t[sel_d], s_t[sel_d]].cpu().numpy()
             exp_s = np.repeat(sc_o[0], K, axis=0)[sel]
             assert np.array_equal(got_s.view(np.uint32), exp_s.view(np.uint32)), "fp8 scales"
             pop = populated_mask(cnt, cap)
-            assert bool((buf.expert_x_scale[~pop] == SENTINEL_SCALE).all()), "scales beyond count"
+            assert bool((sc_rows[~pop] == SENTINEL_SCALE).all()), "scales beyond count"
 
     # combine (bf16 expert outputs), reusing the plan of a bf16 buffer
     if expect_status != moe.Status.OK or N == 0:

@@ -54,6 +54,9 @@ def test_workspace_size(lib):
     assert moe.workspace_size(make_shape(1, 1, 8, 4096, 1, 1)) == 0        # E > 2048
     assert moe.workspace_size(make_shape(1, 1, 12, 1, 1, 1)) == 0          # H % 8
     assert moe.workspace_size(make_shape(1, 1, 136, 1, 1, 1, moe.PAYLOAD_FP8_E4M3)) == 0
+    assert moe.workspace_size(make_shape(1, 1, 136, 1, 1, 1, moe.PAYLOAD_FP8_E4M3_TSCALE)) == 0
+    assert moe.workspace_size(make_shape(1, 1, 128, 1, 1, 1, moe.PAYLOAD_FP8_E4M3_TSCALE)) > 0
+    assert moe.workspace_size(make_shape(1, 1, 128, 1, 1, 1, 3)) == 0      # no such payload
     assert moe.workspace_size(make_shape(1, 1, 8, 2, 1, 1 << 30)) == 0     # E*cap >= 2^31
     assert moe.workspace_size(make_shape(1, 1, 8, 1, 1, 1, 7)) == 0        # payload
 

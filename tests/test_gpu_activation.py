@@ -214,3 +214,21 @@ def test_silu_mul_quant_midpoint_rich_rows():
     qd, sc = _buffers(E, cap, I)
     moe.silu_mul_quant(shape, I, gpu_check.dev(h), gpu_check.dev(counts), qd, sc, ws)
     _check(moe, E, cap, I, h, counts, qd, sc)
+
+
+@pytest.mark.parametrize("I", [384, 2048])
+def test_silu_mul_quant_transposed_scales(I):
+    """PAYLOAD_FP8_E4M3_TSCALE: the same bytes, the scales stored [E, I/128,
+    cap]; compared with the oracle's [E, cap, I/128] scales transposed, and
+    every scale of an unwritten row still the sentinel."""
+    import combine_moe_dispatch_gb300 as moe
+    E, cap = 6, 12
+    counts = np.array([3, 0, 12, 15, -4, 7], np.int32)
+    h = inputs.gate_up(E, cap, I, seed=I + 1)
+    shape = moe.make_shape(1, 16, 256, E, 2, cap, moe.PAYLOAD_FP8_E4M3_TSCALE)
+    ws = _workspace(moe, shape)
+    q = torch.full((E, cap, I), gpu_check.SENTINEL_BYTE, dtype=torch.uint8, device="cuda")
+    sc_t = torch.full((E, I // 128, cap), gpu_check.SENTINEL_SCALE, dtype=torch.float32, device="cuda")
+    moe.silu_mul_quant(shape, I, gpu_check.dev(h), gpu_check.dev(counts), q, sc_t, ws)
+    _check(moe, E, cap, I, h, counts, q, sc_t.transpose(1, 2))
+    assert moe.read_status(ws) == moe.Status.OK

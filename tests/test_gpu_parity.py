@@ -306,3 +306,29 @@ def test_router_topk(N, E, K):
     st, cnt, off, slot, src = oracle.plan(1, N, E, K, N, idx_o)
     assert moe.read_status(b.workspace) == moe.Status.OK
     assert np.array_equal(b.slot_of.cpu().numpy(), slot)
+
+
+TSCALE = [
+    # name, R, T, H, E, K
+    ("tscale_small", 3, 300, 640, 64, 8),
+    ("tscale_ragged_pairs", 2, 64, 1536, 16, 4),
+]
+
+
+@pytest.mark.parametrize("name,R,T,H,E,K", TSCALE, ids=[c[0] for c in TSCALE])
+def test_fp8_transposed_scales(name, R, T, H, E, K):
+    """PAYLOAD_FP8_E4M3_TSCALE (scales [E, H/128, cap], as a grouped GEMM
+    reads them), through moe_plan + moe_dispatch and through
+    moe_plan_dispatch: the same bytes and scales as the oracle."""
+    idx, x, w = _rand_case(zlib.crc32(name.encode()), R, T, H, E, K)
+    gpu_check.run_case(R, T, H, E, K, R * T, idx, x, w, ("fp8t",))
+    gpu_check.run_case(R, T, H, E, K, R * T, idx, x, w, ("fp8t",), fused=True)
+
+
+def test_fp8_transposed_scales_full_size_dsv3_decode():
+    wl = WORKLOADS["dsv3_decode"]
+    d = inputs.make(wl, 0)
+    for fused in (False, True):
+        gpu_check.run_case(wl.R, wl.T, wl.H, wl.E, wl.K, wl.cap, d["topk_idx"], d["x"],
+                           d["topk_weights"], ("fp8t",), expert_y="device", fused=fused)
+    torch.cuda.empty_cache()
