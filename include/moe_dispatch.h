@@ -61,7 +61,8 @@ typedef enum {
   MOE_PAYLOAD_FP8_E4M3_TSCALE = 2  /* the same bytes; the scales transposed per expert,
                                       [E, H/128, cap], as a grouped GEMM loads them: the
                                       scales of one 128-column block of one expert's rows
-                                      are contiguous */
+                                      are contiguous.  Every scale is then a separate
+                                      4-byte store: slower than FP8_E4M3 */
 } moe_payload;
 
 /* Problem shape.  Limits: all sizes >= 1 except T, which may be 0 (an empty
