@@ -7,11 +7,14 @@
 // index first), and weights = softmax over those K logits, exp(l_k - l_max)
 // / sum in fp64, rounded once to fp32.  The indices feed moe_plan directly.
 //
-// How: one warp per token.  The E logits are spread over the lanes in
-// registers (coalesced loads); K rounds of a warp-wide arg-max (value, then
-// index) each remove one expert.  Lanes 0..K-1 keep the chosen (logit,
-// expert); every lane adds the K exponentials in ascending k, the same order
-// as a sequential sum, so the result does not depend on a reduction tree.
+// How: one warp per token, a block's 8 warps on 8 consecutive tokens.  The E
+// logits are spread over the lanes in registers (coalesced loads); K rounds
+// of a warp-wide arg-max (value, then index) each remove one expert.  The
+// chosen logits of the block's tokens then go to shared memory, where one
+// thread per value computes its exponential and one thread per token adds
+// its token's K exponentials in ascending k (a sequential sum, so the result
+// does not depend on a reduction tree); one thread per value divides and
+// stores, so the outputs of the block are written as one coalesced run.
 #include <math.h>
 #include <stdint.h>
 
@@ -25,22 +28,30 @@ constexpr unsigned kAll = 0xFFFFFFFFu;
 template <int VPL>
 __global__ void __launch_bounds__(kRouterThreads)
 router_kernel(RouterParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp0 = ((int64_t)blockIdx.x * kRouterThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * kRouterThreads) >> 5;
+  constexpr int kWarps = kRouterThreads / 32;
+  // the block's tokens' chosen logits minus their maximum, exponentials and
+  // ids, [warp][k]; K <= 32, so kWarps * K <= kRouterThreads
+  __shared__ double s_d[kWarps * kMaxTopK];
+  __shared__ double s_sum[kWarps];
+  __shared__ int32_t s_e[kWarps * kMaxTopK];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
+  const int K = p.K;
   pdl_wait_for_previous();
-  for (int64_t g = warp0; g < p.N; g += nwarps) {
-    const float *row = p.logits + g * p.E;
+  // One token per warp; the block's kWarps tokens are consecutive, and every
+  // warp runs every iteration (the barriers), idle past the last token.
+  for (int64_t base = (int64_t)blockIdx.x * kWarps; base < p.N; base += (int64_t)gridDim.x * kWarps) {
+    const int64_t g = base + warp;
+    const bool live = g < p.N;
     float v[VPL];
 #pragma unroll
     for (int j = 0; j < VPL; ++j) {
       const int e = j * 32 + lane;
-      v[j] = e < p.E ? __ldcs(row + e) : -INFINITY;
+      v[j] = (live && e < p.E) ? __ldcs(p.logits + g * p.E + e) : -INFINITY;
     }
     uint32_t taken = 0;
     float my_v = 0.0f;
     int my_e = 0;
-    for (int k = 0; k < p.K; ++k) {
+    for (int k = 0; k < K; ++k) {
       float bv = -INFINITY;
       int be = INT32_MAX;
 #pragma unroll
@@ -67,14 +78,29 @@ router_kernel(RouterParams p) {
         my_e = be;
       }
     }
-    const double m = __shfl_sync(kAll, (double)my_v, 0);
-    const double z = lane < p.K ? exp((double)my_v - m) : 0.0;
-    double sum = 0.0;
-    for (int k = 0; k < p.K; ++k) sum += __shfl_sync(kAll, z, k);
-    if (lane < p.K) {
-      p.topk_idx[g * p.K + lane] = my_e;
-      p.topk_weights[g * p.K + lane] = (float)(z / sum);
+    // The fp64 part runs once per value, not once per warp and token: this
+    // GPU's fp64 rate is low, and a warp-wide fp64 instruction costs the
+    // same with K lanes active as with 32.
+    const float m = __shfl_sync(kAll, my_v, 0);
+    if (lane < K) {
+      s_d[warp * K + lane] = (double)my_v - (double)m;
+      s_e[warp * K + lane] = my_e;
     }
+    __syncthreads();
+    const int nv = kWarps * K;                     // values of the block's tokens
+    if (tid < nv) s_d[tid] = exp(s_d[tid]);
+    __syncthreads();
+    if (tid < kWarps) {                            // the sum in ascending k, as a sequential sum
+      double sum = 0.0;
+      for (int k = 0; k < K; ++k) sum += s_d[tid * K + k];
+      s_sum[tid] = sum;
+    }
+    __syncthreads();
+    if (tid < nv && base + tid / K < p.N) {        // consecutive outputs: coalesced
+      p.topk_idx[base * K + tid] = s_e[tid];
+      p.topk_weights[base * K + tid] = (float)(s_d[tid] / s_sum[tid / K]);
+    }
+    __syncthreads();
   }
 }
 
