@@ -9,7 +9,9 @@
 //
 // How: one warp per token, a block's 8 warps on 8 consecutive tokens.  The E
 // logits are spread over the lanes in registers (coalesced loads); K rounds
-// of a warp-wide arg-max (value, then index) each remove one expert.  The
+// of a warp-wide arg-max each remove one expert: each lane's best (value,
+// then lowest index) among its logits, then two warp reductions, the
+// largest order-preserving key and the lowest expert holding it.  The
 // chosen logits of the block's tokens then go to shared memory, where one
 // thread per value computes its exponential and one thread per token adds
 // its token's K exponentials in ascending k (a sequential sum, so the result
@@ -24,6 +26,19 @@ namespace moe {
 
 constexpr int kRouterThreads = 256;
 constexpr unsigned kAll = 0xFFFFFFFFu;
+
+// An unsigned key whose order is the order of the floats: the sign bit set
+// for non-negative values, all bits flipped for negative ones, with -0
+// mapped to +0 (the two compare equal).  NaN logits are unspecified.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  uint32_t b = __float_as_uint(v);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+// The float of a key (+0 for a key of zero).
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 template <int VPL>
 __global__ void __launch_bounds__(kRouterThreads)
@@ -63,18 +78,14 @@ router_kernel(RouterParams p) {
           be = e;
         }
       }
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        const float ov = __shfl_xor_sync(kAll, bv, off);
-        const int oe = __shfl_xor_sync(kAll, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
+      // the warp's best: the largest key, then the lowest expert holding it
+      const uint32_t key = order_key(bv);
+      const uint32_t top = __reduce_max_sync(kAll, key);
+      const uint32_t win = __reduce_min_sync(kAll, key == top ? (uint32_t)be : 0xFFFFFFFFu);
+      be = (int)win;
       if (be != INT32_MAX && (be & 31) == lane) taken |= 1u << (be >> 5);
       if (lane == k) {
-        my_v = bv;
+        my_v = key_value(top);
         my_e = be;
       }
     }
