@@ -218,3 +218,12 @@ def test_fused_every_token_to_the_same_experts():
     # and the separate plan and dispatch on the same routing
     res = gpu_check.run_case(R, T, H, E, K, N, idx, x, w, ("bf16", "fp8"))
     assert res["not_bit_exact"] == 0
+
+
+def test_fused_empty_batch():
+    """T = 0: zero counts and offsets, status OK, nothing dispatched."""
+    R, T, H, E, K = 3, 0, 256, 8, 2
+    idx = np.zeros((0, K), np.int32)
+    x = np.zeros((0, H), np.uint16)
+    w = np.zeros((0, K), np.float32)
+    gpu_check.run_case(R, T, H, E, K, 4, idx, x, w, ("bf16", "fp8"), fused=True)
