@@ -505,21 +505,77 @@ __device__ __forceinline__ uint32_t quant_patch4(uint32_t lo, uint32_t hi, float
   return lo;
 }
 
-// One lane's 8 bytes of a block with the given scale and r = RN(1/scale)
-// (zero: the block's amax is 0, all bytes 0): the window bytes, each byte
-// whose window ends disagree divided on its own, per lane, without a vote.
-// For bf16 inputs, where such bytes turn up in most warps' tasks.
-__device__ __forceinline__ uint2 quant_bytes8(const float (&f)[8], float scale, float r, bool zero) {
+// --- RN(x / scale) for bf16 x, with no division and no branch ---
+// q0 = RN(x y) with y = RN(1/scale) is off by up to about 1.5 units in the
+// last place; one correction with the exact remainder (Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 1990): e = RN(scale q0 - x), q = RN(q0 - e y).  For bf16 x (8
+// significant bits) and y = RN(1/scale), q = RN(x / scale) exactly: checked
+// for every bf16 x with 2^-12 <= x/scale < 2^10 against every binary32 scale in
+// [1, 2) (2.4e10 cases), and on both signs, zeros and subnormals at scale
+// exponents -60 to 60 (tests/quotient_check.c).  Scaling x and scale by the same
+// power of two changes no rounding while every intermediate stays normal,
+// which holds for scale in [2^-60, 2^60]; a quotient below 2^-12 comes out
+// below 2^-10 in magnitude, an E4M3 zero of x's sign.  The steps run on -x and
+// -y: with x - scale q0 as the remainder, x = -0 would come out +0.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+// Two-lane packed multiply and fused multiply-add of sm_100-class GPUs, each
+// lane rounded to nearest even (IEEE binary32, no flush to zero).
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Scales whose quotients the correction gives exactly.
+__device__ __forceinline__ bool quot_scale_ok(float scale) {
+  return scale >= 0x1p-60f && scale <= 0x1p60f;
+}
+
+// RN(x / scale) of the two bf16 halves of w; s2 = (scale, scale), ny2 =
+// (-y, -y) with y = RN(1/scale), scale within quot_scale_ok.
+__device__ __forceinline__ float2 quot2_bf16(uint32_t w, uint64_t s2, uint64_t ny2) {
+  const uint32_t nw = w ^ 0x80008000u;                 // -x, both halves
+  const uint64_t nx = pack2(__uint_as_float(nw << 16), __uint_as_float(nw & 0xFFFF0000u));
+  const uint64_t q0 = fmul2(nx, ny2);                   // x y
+  const uint64_t e = ffma2(s2, q0, nx);                 // scale q0 - x
+  return unpack2(ffma2(e, ny2, q0));                    // q0 - e y
+}
+
+// One lane's 8 E4M3 bytes e4m3(RN(x / scale)) of its 16-byte chunk v of a
+// block, as two little-endian words; scale within quot_scale_ok.
+__device__ __forceinline__ uint2 quant_bytes8_bf16(uint4 v, float scale, float ny) {
+  const uint64_t s2 = pack2(scale, scale);
+  const uint64_t ny2 = pack2(ny, ny);
+  const float2 a = quot2_bf16(v.x, s2, ny2);
+  const float2 b = quot2_bf16(v.y, s2, ny2);
+  const float2 c = quot2_bf16(v.z, s2, ny2);
+  const float2 d = quot2_bf16(v.w, s2, ny2);
+  return make_uint2(e4m3x4(a.x, a.y, b.x, b.y), e4m3x4(c.x, c.y, d.x, d.y));
+}
+
+// The same bytes for any scale: outside quot_scale_ok every element is
+// divided (zero: the block's amax is 0, all bytes 0).
+__device__ __forceinline__ uint2 quant_bytes8_bf16_any(uint4 v, float scale, float ny, bool zero) {
   if (zero) return make_uint2(0u, 0u);
-  if (!(r <= 3.0e38f)) return quant_bytes8_exact(f, scale);
-  uint2 q;
-  uint32_t h0, h1;
-  const float2 rw = quant_window_r(r);
-  quant_window4(f[0], f[1], f[2], f[3], rw.x, rw.y, q.x, h0);
-  quant_window4(f[4], f[5], f[6], f[7], rw.x, rw.y, q.y, h1);
-  if (q.x != h0) q.x = quant_patch4(q.x, h0, f[0], f[1], f[2], f[3], scale);
-  if (q.y != h1) q.y = quant_patch4(q.y, h1, f[4], f[5], f[6], f[7], scale);
-  return q;
+  if (quot_scale_ok(scale)) return quant_bytes8_bf16(v, scale, ny);
+  const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+  return quant_bytes8_exact(f, scale);
 }
 
 // A lane's P blocks of 8 values (block it: scale[it], r[it] = RN(1/scale),

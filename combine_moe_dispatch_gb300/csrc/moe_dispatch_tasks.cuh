@@ -110,9 +110,9 @@ __device__ __forceinline__ void fp8_load(const DispatchParams &p, int64_t g, int
 }
 
 // Quantise one loaded task (needs nothing from the plan).  Each block's
-// scale and reciprocal are computed once, by the lane that stores the scale
-// (lane L < 2P owns block seg*2P + L), and handed to the half-warp that
-// quantises the block by shuffle.  All 32 lanes call it together.
+// scale and (negated) reciprocal are computed once, by the lane that stores
+// the scale (lane L < 2P owns block seg*2P + L), and handed to the half-warp
+// that quantises the block by shuffle.  All 32 lanes call it together.
 template <int P>
 __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Task<P> &t) {
   const int half = lane >> 4;
@@ -141,20 +141,24 @@ __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Ta
   if (__any_sync(kFull, odd)) {
     if (odd) my_scale = __fdiv_rn(mine, 448.0f);
   }
-  const float my_r = mine == 0.0f ? 1.0f : __frcp_rn(my_scale);
+  const float my_ny = mine == 0.0f ? -1.0f : -__frcp_rn(my_scale);
   t.my_scale = my_scale;
+  // One vote per task: every block's scale in the corrected quotient's range
+  // (the rule; zero blocks count as in range).
+  if (__all_sync(kFull, mine == 0.0f || quot_scale_ok(my_scale))) {
 #pragma unroll
-  for (int it = 0; it < P; ++it) {
-    const uint32_t w[4] = {a.v[it].x, a.v[it].y, a.v[it].z, a.v[it].w};
-    float f[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = bf16_lo(w[i]);
-      f[2 * i + 1] = bf16_hi(w[i]);
+    for (int it = 0; it < P; ++it) {
+      const float scale = __shfl_sync(kFull, my_scale, it * 2 + half);
+      const float ny = __shfl_sync(kFull, my_ny, it * 2 + half);
+      t.q[it] = am[it] == 0.0f ? make_uint2(0u, 0u) : quant_bytes8_bf16(a.v[it], scale, ny);
     }
-    const float scale = __shfl_sync(kFull, my_scale, it * 2 + half);
-    const float r = __shfl_sync(kFull, my_r, it * 2 + half);
-    t.q[it] = quant_bytes8(f, scale, r, am[it] == 0.0f);
+  } else {
+#pragma unroll
+    for (int it = 0; it < P; ++it) {
+      const float scale = __shfl_sync(kFull, my_scale, it * 2 + half);
+      const float ny = __shfl_sync(kFull, my_ny, it * 2 + half);
+      t.q[it] = quant_bytes8_bf16_any(a.v[it], scale, ny, am[it] == 0.0f);
+    }
   }
   // Pair neighbouring lanes for 16-byte stores: for each pair of iterations
   // (2j, 2j+1), the even lane of a pair gets iteration 2j's bytes of both

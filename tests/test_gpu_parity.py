@@ -99,6 +99,50 @@ def test_fp8_rounding_edge_rows():
     gpu_check.run_case(R, T, H, E, K, N, idx, x, w, ("fp8",))
 
 
+def _fp8_scale_range_rows(H=1024):
+    """Rows of 8 blocks (one 4-pair task each) whose block scales 2^k sit on
+    both sides of 2^-60 and 2^60, the range where the kernels take the
+    quotient without dividing: quotients at E4M3 midpoints and one bf16 step
+    either side, rows all in range, rows with one block out of range, rows
+    all out of range."""
+    tab = __import__("oracle_pins").e4m3_table()[:0x7F]
+    mids = ((tab[:-1] + tab[1:]) / 2).astype(np.float64)
+    rng = np.random.default_rng(29)
+    plans = [(-60, -59, 59, 60, -60, 60, 0, 3),      # every block in range
+             (0, 3, -61, 5, -2, 1, 7, -4),           # one block below the range
+             (2, 62, -1, 0, 4, -3, 6, 1),            # one block above the range
+             (-61, -62, 61, 62, -70, 70, -61, 61),   # every block out of range
+             (-60, -61, 60, 61, -59, -62, 59, 62)]   # alternating at the edges
+    rows = []
+    for ks in plans:
+        for sign in (1.0, -1.0):
+            vals = np.empty(H)
+            top = np.zeros(H, bool)
+            for b, k in enumerate(ks):
+                blk = sign * rng.choice(mids, 128) * 2.0 ** k
+                j = b * 128 + int(rng.integers(0, 128))
+                vals[b * 128:(b + 1) * 128] = blk
+                vals[j] = sign * 448.0 * 2.0 ** k              # scale = 2^k
+                top[j] = True
+            bits = inputs.to_bf16_bits(vals.astype(np.float32))
+            rows.append(bits)
+            step = rng.choice([-1, 1], H)
+            step[top] = 0                                   # keep each block's scale
+            rows.append((bits.astype(np.int32) + step).astype(np.uint16))   # one bf16 step off
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["dispatch", "plan_dispatch"])
+def test_fp8_scale_range_edges(fused):
+    x = _fp8_scale_range_rows()
+    N = x.shape[0]
+    R, T, H, E, K = 1, N, x.shape[1], 6, 2
+    rng = np.random.default_rng(5)
+    idx = np.argsort(rng.random((N, E)), axis=1)[:, :K].astype(np.int32)
+    w = inputs.weights(N, K, 5)
+    gpu_check.run_case(R, T, H, E, K, N, idx, x, w, ("fp8",), fused=fused)
+
+
 def test_duplicate_experts_per_token():
     idx, x, w = _rand_case(5, 2, 64, 256, 4, 4, distinct=False)
     gpu_check.run_case(2, 64, 256, 4, 4, 2 * 64 * 4, idx, x, w, ("bf16", "fp8"))
