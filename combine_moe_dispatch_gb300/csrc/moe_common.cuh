@@ -433,6 +433,26 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return r;
 }
 
+// max(|a|, |b|) of each bf16 half of two packed words (the result's sign
+// bits are the XOR of the inputs' and carry nothing); a NaN half loses to a
+// number, as in fmaxf.
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Largest |x| of a 128-element block held by a half-warp as raw bf16, 4
+// words per lane (lanes 0-15 one block, 16-31 the next), NaN ignored and 0 for
+// a block of NaNs, as fmaxf from 0 gives.  The tree and the butterfly run on
+// packed pairs; the two halves meet at the end.  All 32 lanes call it together.
+__device__ __forceinline__ float half_warp_amax_bf16(uint4 v) {
+  uint32_t m = bf16x2_max_abs(bf16x2_max_abs(v.x, v.y), bf16x2_max_abs(v.z, v.w));
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) m = bf16x2_max_abs(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  return fmaxf(fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m))), 0.0f);
+}
+
 // Largest |x| of a 128-element block held by a half-warp, 8 values per lane
 // (lanes 0-15 one block, 16-31 the next); all 32 lanes call it together.
 __device__ __forceinline__ float half_warp_amax(const float (&f)[8]) {

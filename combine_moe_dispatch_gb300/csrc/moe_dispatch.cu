@@ -27,14 +27,12 @@
 // store is 16 bytes.  The first task is read and quantised before waiting
 // for the plan, which it does not need.
 //
-// Exact division, cheaply: q must be e4m3(RN(x / scale)).  With r =
-// RN(1/scale), x * RN(r * (1 - 2^-20)) and x * RN(r * (1 + 2^-20)), rounded,
-// bracket RN(x / scale) (three roundings of at most 2^-24 each cannot close
-// a 2^-20 gap).  Rounding to E4M3 is monotone, so where both give the same
-// byte, that byte is e4m3(RN(x / scale)); otherwise (a quotient next to an
-// E4M3 midpoint, about 1 element in 200 for bf16 inputs) that element alone
-// is divided with IEEE __fdiv_rn.  The result is bit-identical to dividing
-// every element.
+// Exact division, cheaply: q must be e4m3(RN(x / scale)).  With y =
+// RN(1/scale), RN(x y) corrected once with the exact remainder is RN(x /
+// scale) for every bf16 x and every scale in [2^-60, 2^60] (quot2_bf16 in
+// moe_common.cuh; checked exhaustively on the CPU).  Blocks with scales
+// outside that range divide every element.  The result is bit-identical to
+// dividing every element.
 #include <cuda_bf16.h>
 
 #include "moe_dispatch_tasks.cuh"

@@ -120,16 +120,7 @@ __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Ta
   t.seg = a.seg;
   float am[P];
 #pragma unroll
-  for (int it = 0; it < P; ++it) {
-    const uint32_t w[4] = {a.v[it].x, a.v[it].y, a.v[it].z, a.v[it].w};
-    float f[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = bf16_lo(w[i]);
-      f[2 * i + 1] = bf16_hi(w[i]);
-    }
-    am[it] = half_warp_amax(f);
-  }
+  for (int it = 0; it < P; ++it) am[it] = half_warp_amax_bf16(a.v[it]);
   float mine = 0.0f;
 #pragma unroll
   for (int it = 0; it < P; ++it) {
