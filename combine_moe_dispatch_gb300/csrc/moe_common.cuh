@@ -464,13 +464,13 @@ __device__ __forceinline__ float half_warp_amax(const float (&f)[8]) {
   return amax;
 }
 
-// The 8 E4M3 bytes e4m3(RN(x / scale)) of one lane as two little-endian
-// words, exact, from r = RN(1 / scale) and an IEEE division only where
-// needed: x is multiplied by r scaled down and up by 2^-20 (quant_window4),
-// which brackets RN(x / scale); where both ends give the same byte, that
-// byte is exact.  Where the two ends differ -- a quotient next to an E4M3 midpoint, which bf16 inputs hit
-// for about 1 element in 200 -- that element alone is divided with IEEE
-// __fdiv_rn.  If 1/scale overflows (r > 3e38) every element is divided.
+// --- E4M3 bytes e4m3(RN(x / scale)) of fp32 x by a bracketing window ---
+// (the activation's values; bf16 x takes the corrected quotient below).
+// With r = RN(1 / scale), x is multiplied by r scaled down and up by 2^-20
+// (quant_window4), which brackets RN(x / scale); where both ends give the
+// same byte, that byte is exact.  Where they differ -- a quotient next to an
+// E4M3 midpoint, rare for fp32 values -- that element alone is divided with
+// IEEE __fdiv_rn.  If 1/scale overflows (r > 3e38) every element is divided.
 __device__ __forceinline__ uint32_t e4m3_byte(float v) { return e4m3x4(v, 0.0f, 0.0f, 0.0f) & 0xFFu; }
 
 // The bytes by IEEE division of every element.
