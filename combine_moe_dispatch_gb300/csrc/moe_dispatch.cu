@@ -97,8 +97,10 @@ dispatch_bf16_kernel(DispatchParams p) {
   }
 }
 
-template <int P>
-__global__ void __launch_bounds__(kDispatchThreads, P >= 4 ? 3 : 1)
+// MINB: resident blocks per SM the registers are held to (3: 80 registers,
+// 4: 64; see launch_dispatch_fp8).
+template <int P, int MINB>
+__global__ void __launch_bounds__(kDispatchThreads, MINB)
 dispatch_fp8_kernel(DispatchParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * kDispatchThreads + threadIdx.x) >> 5;
@@ -164,8 +166,14 @@ cudaError_t launch_dispatch_fp8(const DispatchParams &p, cudaStream_t stream) {
   const int nb = p.H / 128;
   const int P = (nb % 2 == 0) ? pick_units(nb / 2, kFp8MaxPairs) : kFp8MaxPairs;
   const int64_t tasks = (int64_t)p.N * ((nb + 2 * P - 1) / (2 * P));
-  if (P == 1) return launch_tasks(dispatch_fp8_kernel<1>, tasks, p, stream);
-  return launch_tasks(dispatch_fp8_kernel<kFp8MaxPairs>, tasks, p, stream);
+  if (P == 1) return launch_tasks(dispatch_fp8_kernel<1, 1>, tasks, p, stream);
+  // More than 3 tasks per warp at 3 blocks per SM: 4 blocks per SM (64
+  // registers, no spills).  Measured on GB300: 15.2 -> 14.1 us at the
+  // Mixtral-shaped layer (4.5 tasks per warp), 52.6 -> 52.1 us at Kimi-K2
+  // decode (7.9), but 13.45 -> 13.6 us at DeepSeek-V3 decode (2.0).
+  const int64_t warps3 = (int64_t)device_sm_count() * 3 * (kDispatchThreads / 32);
+  if (tasks > 3 * warps3) return launch_tasks(dispatch_fp8_kernel<kFp8MaxPairs, 4>, tasks, p, stream);
+  return launch_tasks(dispatch_fp8_kernel<kFp8MaxPairs, 3>, tasks, p, stream);
 }
 
 }  // namespace moe

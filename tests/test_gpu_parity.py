@@ -143,6 +143,15 @@ def test_fp8_scale_range_edges(fused):
     gpu_check.run_case(R, T, H, E, K, N, idx, x, w, ("fp8",), fused=fused)
 
 
+def test_fp8_long_task_list():
+    """More than 3 tasks per warp of the 3-blocks-per-SM grid (12000 tasks of
+    1024 elements against 3648 warps on 152 SMs): the fp8 dispatch runs at 4
+    blocks per SM.  Whole outputs compared."""
+    R, T, H, E, K = 4, 750, 4096, 16, 2
+    idx, x, w = _rand_case(41, R, T, H, E, K)
+    gpu_check.run_case(R, T, H, E, K, R * T, idx, x, w, ("fp8",))
+
+
 def test_duplicate_experts_per_token():
     idx, x, w = _rand_case(5, 2, 64, 256, 4, 4, distinct=False)
     gpu_check.run_case(2, 64, 256, 4, 4, 2 * 64 * 4, idx, x, w, ("bf16", "fp8"))
