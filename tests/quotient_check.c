@@ -5,7 +5,7 @@
    -y (so that x = -0 keeps its sign); this program does the same, in binary32
    with fmaf.
 
-   Usage: quotient_check STEP [nocorr|unsigned]
+   Usage: quotient_check STEP [exact|nocorr|unsigned] [K]
      Runs over b = B * 2^k for k in {-60, -59, -40, -1, 0, 1, 40, 59, 60} and
      every STEP-th binary32 significand B in [1, 2), and over every finite bf16
      x (both signs, zeros, subnormals) with |x / b| < 1024.  Requires
@@ -19,7 +19,10 @@
      result: "nocorr" takes q0 itself (no correction); "unsigned" runs the
      steps on x and y, with e = RN(x - b q0) and q = RN(q0 + e y), where x = -0
      comes out +0.
+     K, if given, replaces the nine exponents by that one.
    Prints "cases N exact_mismatches A small_failures B" and exits 0.
+   Built with OpenMP (-fopenmp) the scale significands are split over threads;
+   without it the pragma is ignored.
 
    With STEP 1 and k = 0 this is every binary32 b in [1, 2); scaling x and b
    by the same power of two changes no rounding while every intermediate stays
@@ -46,10 +49,21 @@ int main(int argc, char **argv) {
   const long step = argc > 1 ? atol(argv[1]) : 4096;
   const int nocorr = argc > 2 && strcmp(argv[2], "nocorr") == 0;
   const int unsig = argc > 2 && strcmp(argv[2], "unsigned") == 0;
-  static const int ks[] = {-60, -59, -40, -1, 0, 1, 40, 59, 60};
+  static const int all_ks[] = {-60, -59, -40, -1, 0, 1, 40, 59, 60};
+  int one_k[1];
+  const int *ks = all_ks;
+  unsigned nk = sizeof all_ks / sizeof all_ks[0];
+  if (argc > 3) {
+    one_k[0] = atoi(argv[3]);
+    ks = one_k;
+    nk = 1;
+  }
+  const long nm = ((1L << 23) + step - 1) / step;
   long long n = 0, bad_exact = 0, bad_small = 0;
-  for (unsigned ki = 0; ki < sizeof ks / sizeof ks[0]; ++ki) {
-    for (uint32_t m = 0; m < (1u << 23); m += (uint32_t)step) {
+  for (unsigned ki = 0; ki < nk; ++ki) {
+#pragma omp parallel for schedule(dynamic, 16) reduction(+ : n, bad_exact, bad_small)
+    for (long mi = 0; mi < nm; ++mi) {
+      const uint32_t m = (uint32_t)(mi * step);
       const float b = ldexpf(u2f(0x3F800000u | m), ks[ki]);
       const float y = 1.0f / b, ny = -y;
       for (uint32_t xb = 0; xb < 0x10000u; ++xb) {
