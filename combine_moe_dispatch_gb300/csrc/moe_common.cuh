@@ -531,9 +531,9 @@ __device__ __forceinline__ uint32_t quant_patch4(uint32_t lo, uint32_t hi, float
 // of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
 // Dev. 1990): e = RN(scale q0 - x), q = RN(q0 - e y).  For bf16 x (8
 // significant bits) and y = RN(1/scale), q = RN(x / scale) exactly: checked
-// for every bf16 x with 2^-12 <= x/scale < 2^10 against every binary32 scale in
-// [1, 2) (2.4e10 cases), and on both signs, zeros and subnormals at scale
-// exponents -60 to 60 (tests/quotient_check.c).  Scaling x and scale by the same
+// for every finite bf16 x with |x/scale| < 1024 against every binary32 scale
+// in [1, 2) (2.95e11 cases), and at scale exponents -60 to 60 on every 64th
+// significand (tests/quotient_check.c).  Scaling x and scale by the same
 // power of two changes no rounding while every intermediate stays normal,
 // which holds for scale in [2^-60, 2^60]; a quotient below 2^-12 comes out
 // below 2^-10 in magnitude, an E4M3 zero of x's sign.  The steps run on -x and
