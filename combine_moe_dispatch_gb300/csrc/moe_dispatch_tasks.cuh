@@ -134,8 +134,8 @@ __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Ta
   }
   const float my_ny = mine == 0.0f ? -1.0f : -__frcp_rn(my_scale);
   t.my_scale = my_scale;
-  // One vote per task: every block's scale in the corrected quotient's range
-  // (the rule; zero blocks count as in range).
+  // One vote per task: when every block's scale is within quot_scale_ok
+  // (a zero block counts as within), no block needs the division path.
   if (__all_sync(kFull, mine == 0.0f || quot_scale_ok(my_scale))) {
 #pragma unroll
     for (int it = 0; it < P; ++it) {
