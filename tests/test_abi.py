@@ -122,6 +122,46 @@ def test_host_rejections_enqueue_nothing(lib):
     assert lib.moe_workspace_set_debug(None, 1, 0, None) == Status.INVALID_ARG
 
 
+@pytest.mark.parametrize("fields,over,under", [
+    # (R, T, H, E, K, cap, payload) of a shape just over a limit, and just under it
+    ("N*K < 2^31", (1, 1 << 28, 256, 8, 8, 8, 0), (1, (1 << 28) - 1, 256, 8, 8, 8, 0)),
+    ("E*cap < 2^31", (1, 4, 256, 2048, 2, 1 << 20, 0), (1, 4, 256, 2048, 2, (1 << 20) - 1, 0)),
+    ("E <= 2048", (1, 4, 256, 2049, 2, 8, 0), (1, 4, 256, 2048, 2, 8, 0)),
+    ("K <= 32", (1, 4, 256, 64, 33, 8, 0), (1, 4, 256, 64, 32, 8, 0)),
+    ("H % 8 == 0", (1, 4, 260, 8, 2, 8, 0), (1, 4, 264, 8, 2, 8, 0)),
+    ("fp8: H % 128 == 0", (1, 4, 264, 8, 2, 8, 1), (1, 4, 256, 8, 2, 8, 1)),
+    ("fp8, transposed scales: H % 128 == 0", (1, 4, 264, 8, 2, 8, 2), (1, 4, 384, 8, 2, 8, 2)),
+])
+def test_shape_limits(lib, fields, over, under):
+    """Each limit of the shape check, from both sides: just over it the
+    limit's own code; just under it the shape passes and the call fails at
+    the next check (a null x).  No pointer is dereferenced."""
+    A = 0x100000
+    s = Shape(*over)
+    assert lib.moe_dispatch(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None) \
+        == Status.UNSUPPORTED, fields
+    s = Shape(*under)
+    assert lib.moe_dispatch(ctypes.byref(s), None, _p(A), _p(A), _p(A), _p(A), _p(A), None) \
+        == Status.INVALID_ARG, fields
+
+
+def test_shape_values_out_of_range(lib):
+    A = 0x100000
+    for bad in [(0, 4, 256, 8, 2, 8, 0), (1, -1, 256, 8, 2, 8, 0), (1, 4, 0, 8, 2, 8, 0),
+                (1, 4, 256, 0, 2, 8, 0), (1, 4, 256, 8, 0, 8, 0), (1, 4, 256, 8, 2, 0, 0),
+                (1, 4, 256, 8, 2, 8, 3), (1, 4, 256, 8, 2, 8, -1)]:
+        s = Shape(*bad)
+        assert lib.moe_dispatch(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None) \
+            == Status.INVALID_ARG, bad
+
+
+def test_empty_batch_touches_nothing(lib):
+    # T = 0: the shape is valid and there is nothing to read or write, so even
+    # null buffers are accepted and nothing is enqueued
+    s = Shape(3, 0, 256, 8, 2, 4, 1)
+    assert lib.moe_dispatch(ctypes.byref(s), None, None, None, None, None, None, None) == Status.OK
+
+
 def test_missing_library_fails_loudly(tmp_path):
     saved = moe._lib
     moe._lib = None
