@@ -62,7 +62,8 @@ extern "C" moe_status moe_plan_noalloc(const moe_shape *shape, const int32_t *to
   if (need == 0)
     return (shape->num_ranks <= 0 || shape->tokens_per_rank < 0 || shape->hidden <= 0 ||
             shape->num_experts <= 0 || shape->top_k <= 0 || shape->capacity <= 0 ||
-            (shape->payload != MOE_PAYLOAD_BF16 && shape->payload != MOE_PAYLOAD_FP8_E4M3))
+            (shape->payload != MOE_PAYLOAD_BF16 && shape->payload != MOE_PAYLOAD_FP8_E4M3 &&
+             shape->payload != MOE_PAYLOAD_FP8_E4M3_TSCALE))
                ? MOE_ERR_INVALID_ARG
                : MOE_ERR_UNSUPPORTED;
   if (need > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;

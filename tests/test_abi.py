@@ -162,6 +162,51 @@ def test_empty_batch_touches_nothing(lib):
     assert lib.moe_dispatch(ctypes.byref(s), None, None, None, None, None, None, None) == Status.OK
 
 
+def test_router_limits(lib):
+    A = 0x100000
+    r = lib.moe_router_topk
+    for over, code in [((1, 4, 256, 8, 9, 8, 0), Status.UNSUPPORTED),        # K > E
+                       ((1, 4, 256, 1025, 8, 8, 0), Status.UNSUPPORTED)]:    # E above 1024
+        s = Shape(*over)
+        assert r(ctypes.byref(s), _p(A), _p(A), _p(A), None) == code, over
+    for under in [(1, 4, 256, 8, 8, 8, 0), (1, 4, 256, 1024, 8, 8, 0)]:
+        s = Shape(*under)
+        assert r(ctypes.byref(s), None, _p(A), _p(A), None) == Status.INVALID_ARG, under
+    s = Shape(1, 4, 256, 64, 8, 8, 0)
+    assert r(ctypes.byref(s), _p(A + 2), _p(A), _p(A), None) == Status.ALIGNMENT
+    s = Shape(2, 0, 256, 64, 8, 8, 0)
+    assert r(ctypes.byref(s), None, None, None, None) == Status.OK      # empty batch
+
+
+def test_activation_size_limit(lib):
+    # E * cap * 2I elements of expert_h must stay below 2^46
+    A = 0x100000
+    act = lib.moe_silu_mul_quant
+    s = Shape(1, 4, 256, 2048, 2, 1 << 20, 0)          # E * cap = 2^31 - too large for the shape check
+    assert act(ctypes.byref(s), 128, _p(A), _p(A), _p(A), _p(A), _p(A), _p(A)) == Status.UNSUPPORTED
+    s = Shape(1, 4, 256, 1024, 2, 1 << 20, 0)          # E * cap = 2^30: 2^31 * I >= 2^46 from I = 2^15
+    assert act(ctypes.byref(s), 1 << 15, _p(A), _p(A), _p(A), _p(A), _p(A), _p(A)) == Status.UNSUPPORTED
+    assert act(ctypes.byref(s), (1 << 15) - 128, None, _p(A), _p(A), _p(A), _p(A), _p(A)) \
+        == Status.INVALID_ARG
+
+
+@pytest.mark.parametrize("payload", [0, 1, 2])
+def test_plan_noalloc_host_checks(lib, payload):
+    A = 0x100000
+    na = lib.moe_plan_noalloc
+    assert na(None, _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None) == Status.INVALID_ARG
+    s = Shape(1, 4, 256, 0, 2, 8, payload)               # no experts
+    assert na(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None) == Status.INVALID_ARG
+    s = Shape(1, 4, 256, 4096, 2, 8, payload)            # more experts than supported
+    assert na(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None) == Status.UNSUPPORTED
+    s = Shape(64, 4096, 256, 256, 8, 8, payload)         # a workspace above the 1 MiB scratch
+    assert moe.workspace_size(s) > (1 << 20)
+    assert na(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None) == Status.WORKSPACE
+    s = Shape(1, 4, 256, 8, 2, 8, payload)
+    assert na(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A), None, None) == Status.INVALID_ARG
+    assert na(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A + 2), None) == Status.ALIGNMENT
+
+
 def test_missing_library_fails_loudly(tmp_path):
     saved = moe._lib
     moe._lib = None
