@@ -207,6 +207,33 @@ def test_plan_noalloc_host_checks(lib, payload):
     assert na(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A + 2), None) == Status.ALIGNMENT
 
 
+def test_masked_plan_and_shared_combine_host_checks(lib):
+    A = 0x100000
+    s = Shape(2, 4, 256, 8, 2, 8, 0)
+    ws = moe.workspace_size(s)
+    pm = lib.moe_plan_masked
+    # num_tokens may be null (every token valid) but, if given, 4-byte aligned
+    assert pm(ctypes.byref(s), _p(A), _p(A + 2), _p(A), _p(A), _p(A), _p(A), _p(A), ws, None) \
+        == Status.ALIGNMENT
+    assert pm(ctypes.byref(s), None, None, _p(A), _p(A), _p(A), _p(A), _p(A), ws, None) \
+        == Status.INVALID_ARG
+    cs = lib.moe_combine_shared
+    # the shared expert's output is required, 16-byte aligned
+    assert cs(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), None, _p(A), _p(A), None) \
+        == Status.INVALID_ARG
+    assert cs(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A + 8), _p(A), _p(A), None) \
+        == Status.ALIGNMENT
+    # the rest as moe_combine: y aligned, shape checked
+    assert cs(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A + 8), _p(A), None) \
+        == Status.ALIGNMENT
+    big_k = Shape(2, 4, 256, 64, 40, 8, 0)
+    assert cs(ctypes.byref(big_k), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None) \
+        == Status.UNSUPPORTED
+    # an empty batch needs nothing
+    e = Shape(2, 0, 256, 8, 2, 8, 0)
+    assert cs(ctypes.byref(e), None, None, None, None, None, None, None, None) == Status.OK
+
+
 def test_missing_library_fails_loudly(tmp_path):
     saved = moe._lib
     moe._lib = None
