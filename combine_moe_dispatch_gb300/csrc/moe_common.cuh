@@ -640,8 +640,9 @@ __device__ __forceinline__ void quantise_blocks(const float (&f)[P][8], const fl
 // amax / 448 rounded to nearest: q0 = RN(amax * RN(1/448)), then one
 // correction with the exact remainder (the method for divisors known in
 // advance of Brisebarre, Muller and Raina, IEEE Trans. Computers 2004).
-// Checked against IEEE division for every binary32 amax in [2^-120, FLT_MAX];
-// smaller and non-finite amax (subnormal quotients, inf) take __fdiv_rn.
+// Checked against IEEE division for every binary32 amax in [2^-120, FLT_MAX]
+// (tests/div448_check.c); smaller and non-finite amax (subnormal quotients,
+// inf) take __fdiv_rn.
 __device__ __forceinline__ float div448_fast(float amax) {
   const float y = 1.0f / 448.0f;
   const float q0 = __fmul_rn(amax, y);
