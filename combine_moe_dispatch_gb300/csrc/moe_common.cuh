@@ -468,9 +468,10 @@ __device__ __forceinline__ float half_warp_amax(const float (&f)[8]) {
 // (the activation's values; bf16 x takes the corrected quotient below).
 // With r = RN(1 / scale), x is multiplied by r scaled down and up by 2^-20
 // (quant_window4), which brackets RN(x / scale); where both ends give the
-// same byte, that byte is exact.  Where they differ -- a quotient next to an
-// E4M3 midpoint, rare for fp32 values -- that element alone is divided with
-// IEEE __fdiv_rn.  If 1/scale overflows (r > 3e38) every element is divided.
+// same byte, that byte is exact (sampled in tests/window_check.c).  Where
+// they differ -- a quotient next to an E4M3 midpoint, rare for fp32 values --
+// that element alone is divided with IEEE __fdiv_rn.  If 1/scale overflows
+// (r > 3e38) every element is divided.
 __device__ __forceinline__ uint32_t e4m3_byte(float v) { return e4m3x4(v, 0.0f, 0.0f, 0.0f) & 0xFFu; }
 
 // The bytes by IEEE division of every element.
