@@ -111,8 +111,45 @@ def step_calls(wl) -> list:
 
 def step_sequence(wl) -> list:
     """The calls one step makes: the plan fused with the bf16 dispatch, the
-    fp8 dispatch on that plan, the combine."""
-    return ["plan_dispatch_bf16"] + (["dispatch_fp8"] if wl.H % 128 == 0 else []) + ["combine"]
+    fp8 dispatch on that plan, the combine.  The fp8 dispatch reads x early
+    (MOE_DISPATCH_EARLY_X): the kernel before it, the fused call, began only
+    after x was written and never writes x."""
+    return ["plan_dispatch_bf16"] + (["dispatch_fp8_early"] if wl.H % 128 == 0 else []) + ["combine"]
+
+
+def base_call(name: str) -> str:
+    """The call a timed name stands for: "dispatch_fp8_early" is
+    moe_dispatch_ex(MOE_DISPATCH_EARLY_X) of the fp8 payload, which moves the
+    bytes of "dispatch_fp8"."""
+    return name[:-len("_early")] if name.endswith("_early") else name
+
+
+def dispatch_incl_plan(calls, means: dict, cb: dict, peak: float) -> dict:
+    """"Dispatch" as the target counts it: the plan and the dispatch.  ``us``
+    is moe_plan_dispatch (one launch up to FUSED_MAX_ENTRIES routed entries);
+    ``two_launches_us`` is moe_plan then moe_dispatch_ex(MOE_DISPATCH_EARLY_X),
+    as moe_plan_dispatch runs them beyond that; ``two_launches_default_us``
+    the same with the default moe_dispatch, which waits for the plan before
+    its first read of x.  ``means`` in ms."""
+    disp = {}
+    for p_ in ("bf16", "fp8"):
+        c = f"dispatch_{p_}"
+        if c in calls and "plan_" + c in means:
+            us = 1e3 * means["plan_" + c]
+            two = 1e3 * means["plan+" + c + "_early"]
+            two_d = 1e3 * means["plan+" + c]
+            b_ = cb["plan"] + cb[c]
+            disp[p_] = {"us": us, "gbs": b_ / (us * 1e-6) / 1e9,
+                        "frac_of_peak": b_ / (us * 1e-6) / 1e9 / peak,
+                        "two_launches_us": two,
+                        "two_launches_frac_of_peak": b_ / (two * 1e-6) / 1e9 / peak,
+                        "two_launches_default_us": two_d,
+                        "two_launches_default_frac_of_peak": b_ / (two_d * 1e-6) / 1e9 / peak,
+                        "note": ("us: moe_plan_dispatch (one launch when N*K <= "
+                                 f"{FUSED_MAX_ENTRIES}); two_launches: moe_plan then "
+                                 "moe_dispatch_ex(EARLY_X), back to back in one graph; "
+                                 "two_launches_default: moe_plan then moe_dispatch")}
+    return disp
 
 
 def launches_per_step(wl) -> int:
@@ -300,7 +337,7 @@ def run_reference(args, wl):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**workload_config(wl, wl.cap), "sample": desc},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": desc, "host": f"{os.cpu_count()} cores, {cpu_model()}"},
@@ -359,14 +396,16 @@ class BufferSet:
 
     def do(self, name, stream):
         moe, b16, b8 = self.moe, self.b16, self.b8
+        early = name.endswith("_early")
+        name = base_call(name)
         if name == "plan":
             b16.plan(self.idx, stream)
         elif name == "dispatch_bf16":
             moe.dispatch(self.sh16, self.x, self.idx, b16.slot_of, b16.expert_x, None,
-                         b16.workspace, stream)
+                         b16.workspace, stream, early_x=early)
         elif name == "dispatch_fp8":
             moe.dispatch(self.sh8, self.x, self.idx, b16.slot_of, b8.expert_x, b8.expert_x_scale,
-                         b16.workspace, stream)
+                         b16.workspace, stream, early_x=early)
         elif name == "combine":
             moe.combine(self.sh16, self.ey, self.idx, b16.slot_of, self.w, b16.y, b16.workspace,
                         stream)
@@ -495,6 +534,91 @@ def measure_next_rows(moe, torch, wl, d, device, stream, l2, peak, seed, warmup)
     return out
 
 
+# The other workloads the path is measured on, besides the headline one; each
+# is timed call by call in the same run (no step, e2e or cold calls).
+EXTRA_WORKLOADS = ("mixtral", "dsv3_prefill", "kimi_decode")
+
+
+def measure_workload(moe, torch, wl, device, stream, l2, peak, seed, warmup):
+    """Per-call device times of one more workload at its full size and
+    capacity: every row of the step as its own call, the early-reading fp8
+    and bf16 dispatches, moe_plan_dispatch of both payloads, and the plan
+    followed by each dispatch.  Timed as the headline's per-call figures:
+    graphs of back-to-back launches over rotating buffer sets (enough that
+    one rotation of each call but the plan moves twice L2, up to 6, within
+    half of the free device memory), median of 5 replays.  The buffers are
+    freed before returning."""
+    d = inputs.make(wl, seed)
+    cap = wl.cap
+    calls = step_calls(wl)
+    disp_calls = [c for c in calls if c.startswith("dispatch_")]
+    timed = (calls + [c + "_early" for c in disp_calls]
+             + [c.replace("dispatch_", "plan_dispatch_") for c in disp_calls])
+    cb = call_bytes(wl)
+    smallest = min(cb[base_call(c)] for c in timed if c != "plan")
+    nsets = max(2, min(6, -(-2 * l2 // max(1, smallest))))
+    free = torch.cuda.mem_get_info(device)[0]
+    while nsets > 1 and nsets * BufferSet.nbytes(wl, cap, timed) > free // 2:
+        nsets -= 1
+    if BufferSet.nbytes(wl, cap, timed) > free * 0.9:
+        return {"skipped": f"needs {BufferSet.nbytes(wl, cap, timed) / 1e9:.1f} GB, "
+                           f"{free / 1e9:.1f} GB free"}
+    sets = [BufferSet(moe, torch, wl, d, device, timed, cap, seed + i) for i in range(nsets)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            for bs in sets:
+                for c in timed:
+                    bs.do(c, stream)
+    stream.synchronize()
+    assert all(moe.read_status(bs.b16.workspace, stream) == moe.Status.OK for bs in sets)
+    reps = max(1, 24 // nsets)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn(torch.cuda.current_stream(device))
+        return g
+
+    graphs = {c: capture(lambda st, c=c: [bs.do(c, st) for _ in range(reps) for bs in sets])
+              for c in timed}
+    for c in disp_calls:
+        for v in (c, c + "_early"):
+            graphs["plan+" + v] = capture(
+                lambda st, v=v: [(bs.do("plan", st), bs.do(v, st)) for _ in range(reps)
+                                 for bs in sets])
+    means = {}
+    with torch.cuda.stream(stream):
+        for c, g in graphs.items():
+            for _ in range(warmup):
+                g.replay()
+            ts = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b) / (reps * nsets))
+            means[c] = statistics.median(ts)
+    assert all(moe.read_status(bs.b16.workspace, stream) == moe.Status.OK for bs in sets)
+    out_calls = {}
+    for c in timed:
+        us = 1e3 * means[c]
+        b_ = cb[base_call(c)]
+        out_calls[c] = {"us": us, "bytes": b_, "gbs": b_ / (us * 1e-6) / 1e9,
+                        "frac_of_peak": b_ / (us * 1e-6) / 1e9 / peak}
+    out = {"config": {**workload_config(wl, cap), "sets": nsets,
+                      "launches_per_timed_replay": reps * nsets,
+                      "payloads_of_the_workload": list(wl.payloads)},
+           "calls": out_calls,
+           "dispatch_incl_plan": dispatch_incl_plan(calls, means, cb, peak)}
+    del graphs, sets
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args, wl):
     import torch
     import combine_moe_dispatch_gb300 as moe
@@ -520,7 +644,8 @@ def run_gpu(args, wl):
     N, H, E, K, R, T, cap = wl.N, wl.H, wl.E, wl.K, wl.R, wl.T, wl.cap
     calls = step_calls(wl)
     seq = step_sequence(wl)
-    timed = calls + [c.replace("dispatch_", "plan_dispatch_") for c in calls if c.startswith("dispatch_")]
+    timed = (calls + [c + "_early" for c in calls if c.startswith("dispatch_")]
+             + [c.replace("dispatch_", "plan_dispatch_") for c in calls if c.startswith("dispatch_")])
     if args.only:
         calls = [c for c in calls if c in ("plan", args.only)]
         seq = timed = calls if args.only in calls else [args.only]
@@ -529,10 +654,13 @@ def run_gpu(args, wl):
     cb = call_bytes(wl)
     step_bytes = sum(cb[c] for c in calls)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    seq_bytes = sum(cb[base_call(c)] for c in seq)
+    assert args.only or seq_bytes == step_bytes, "the step's calls move the bytes of every row"
 
     # Enough buffer sets that one rotation moves >= 2x L2 in its smallest call,
     # within half of the free device memory.
-    smallest = min(cb[c] for c in timed if c != "plan") if len(timed) > 1 else cb[timed[0]]
+    smallest = (min(cb[base_call(c)] for c in timed if c != "plan") if len(timed) > 1
+                else cb[base_call(timed[0])])
     nsets = max(2, min(6, -(-2 * l2 // max(1, smallest))))
     free = torch.cuda.mem_get_info(device)[0]
     while nsets > 1 and nsets * BufferSet.nbytes(wl, cap, timed) > free // 2:
@@ -563,11 +691,14 @@ def run_gpu(args, wl):
     call_graphs = {c: capture(lambda st, c=c: [bs.do(c, st) for _ in range(reps) for bs in sets])
                    for c in timed}
     # the plan and the dispatch as two calls: the plan, then the dispatch
-    # that may start while the plan finishes
+    # that may start while the plan finishes, reading x early (as
+    # moe_plan_dispatch does when it runs as two launches) and by default
     for c in calls:
         if c.startswith("dispatch_"):
-            call_graphs["plan+" + c] = capture(
-                lambda st, c=c: [(bs.do("plan", st), bs.do(c, st)) for _ in range(reps) for bs in sets])
+            for v in (c, c + "_early"):
+                call_graphs["plan+" + v] = capture(
+                    lambda st, v=v: [(bs.do("plan", st), bs.do(v, st)) for _ in range(reps)
+                                     for bs in sets])
     with torch.cuda.stream(stream):
         for g in step_graphs + list(call_graphs.values()):
             for _ in range(args.warmup):
@@ -693,33 +824,29 @@ def run_gpu(args, wl):
     if not args.no_next_rows:
         next_rows = measure_next_rows(moe, torch, wl, d, device, stream, l2, peak, args.seed,
                                       args.warmup)
+    workloads = None
+    if not args.no_workloads and not args.only:
+        workloads = {}
+        for name in EXTRA_WORKLOADS:
+            if name != wl.name:
+                workloads[name] = measure_workload(moe, torch, WORKLOADS[name], device, stream, l2,
+                                                   peak, args.seed, args.warmup)
     means = {c: statistics.median(v) for c, v in per_call.items()}
     dom = max((c for c in seq), key=means.get)
-    achieved = cb[dom] / (means[dom] * 1e-3) / 1e9
+    dom_b = base_call(dom)
+    achieved = cb[dom_b] / (means[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "peak_source": f"{peak_kind} hbm_gbs", "unit": UNIT, "frac": achieved / peak,
-                "traffic": recorded_traffic(dom, wl.name),
-                "algorithmic_bytes": cb[dom]}
+                "traffic": recorded_traffic(dom_b, wl.name),
+                "algorithmic_bytes": cb[dom_b]}
     calls_out = {}
     for c in timed:
         us = 1e3 * means[c]
-        calls_out[c] = {"us": us, "bytes": cb[c], "gbs": cb[c] / (us * 1e-6) / 1e9,
-                        "frac_of_peak": cb[c] / (us * 1e-6) / 1e9 / peak,
-                        "cold_call_us_median": statistics.median(cold[c])}
-    disp = {}
-    for p_ in ("bf16", "fp8"):
-        c = f"dispatch_{p_}"
-        if c in calls and "plan_" + c in means:
-            us = 1e3 * means["plan_" + c]
-            two = 1e3 * means["plan+" + c]
-            b_ = cb["plan"] + cb[c]
-            disp[p_] = {"us": us, "gbs": b_ / (us * 1e-6) / 1e9,
+        b_ = cb[base_call(c)]
+        calls_out[c] = {"us": us, "bytes": b_, "gbs": b_ / (us * 1e-6) / 1e9,
                         "frac_of_peak": b_ / (us * 1e-6) / 1e9 / peak,
-                        "two_launches_us": two,
-                        "two_launches_frac_of_peak": b_ / (two * 1e-6) / 1e9 / peak,
-                        "note": ("us: moe_plan_dispatch (one launch when N*K <= "
-                                 f"{FUSED_MAX_ENTRIES}); two_launches: moe_plan then moe_dispatch, "
-                                 "back to back in one graph")}
+                        "cold_call_us_median": statistics.median(cold[c])}
+    disp = dispatch_incl_plan(calls, means, cb, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -730,7 +857,7 @@ def run_gpu(args, wl):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": "bf16", "data": "synthetic",
             "config": {**workload_config(wl, cap), "calls_per_step": seq,
                        "io": "bf16 activations and expert outputs, e4m3 + fp32 scales for the fp8 payload",
                        "l2": (f"no flush: inputs larger than L2 -- each step moves {step_bytes / 1e6:.0f} MB "
@@ -745,6 +872,7 @@ def run_gpu(args, wl):
             "calls": calls_out,
             "dispatch_incl_plan": disp,
             "next_rows": next_rows,
+            "workloads": workloads,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
@@ -777,6 +905,9 @@ def main():
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the per-call timing of the masked plan, combine with the shared "
                          "expert, activation and router")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-call timing of the other workloads (" +
+                         ", ".join(EXTRA_WORKLOADS) + ")")
     ap.add_argument("--only", default=None,
                     help="profiling: time only this call (plus the plan it needs); no e2e")
     ap.add_argument("--tight-capacity", action="store_true",

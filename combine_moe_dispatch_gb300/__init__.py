@@ -20,6 +20,8 @@ from . import buildlib as _build
 PAYLOAD_BF16 = 0
 PAYLOAD_FP8_E4M3 = 1
 PAYLOAD_FP8_E4M3_TSCALE = 2   # E4M3 bytes, scales [E, H/128, cap]
+# moe_dispatch_ex flag: x was final before the kernel preceding the dispatch began
+DISPATCH_EARLY_X = 1
 
 
 class Status(enum.IntEnum):
@@ -78,6 +80,7 @@ SIGNATURES = {
     "moe_workspace_init": ([_P, _S, _P], ctypes.c_int),
     "moe_plan": ([_SP, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
     "moe_dispatch": ([_SP, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "moe_dispatch_ex": ([_SP, _P, _P, _P, _P, _P, _P, _P, _U32], ctypes.c_int),
     "moe_combine": ([_SP, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_read_status": ([_P, _P, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -173,11 +176,26 @@ def plan_masked(shape: Shape, topk_idx, num_tokens, expert_num_tokens, expert_ra
 
 
 def dispatch(shape: Shape, x, topk_idx, slot_of, expert_x, expert_x_scale, workspace,
-             stream=None, check=True) -> Status:
+             stream=None, check=True, early_x=False) -> Status:
+    """moe_dispatch; with ``early_x`` moe_dispatch_ex(MOE_DISPATCH_EARLY_X),
+    for callers whose x was final before the preceding kernel began."""
+    if early_x:
+        st = load_library().moe_dispatch_ex(ctypes.byref(shape), _ptr(x), _ptr(topk_idx),
+                                            _ptr(slot_of), _ptr(expert_x), _ptr(expert_x_scale),
+                                            _ptr(workspace), _stream(stream), DISPATCH_EARLY_X)
+        return _check(st, "moe_dispatch_ex", check)
     st = load_library().moe_dispatch(ctypes.byref(shape), _ptr(x), _ptr(topk_idx), _ptr(slot_of),
                                      _ptr(expert_x), _ptr(expert_x_scale), _ptr(workspace),
                                      _stream(stream))
     return _check(st, "moe_dispatch", check)
+
+
+def dispatch_ex(shape: Shape, x, topk_idx, slot_of, expert_x, expert_x_scale, workspace,
+                flags: int, stream=None, check=True) -> Status:
+    st = load_library().moe_dispatch_ex(ctypes.byref(shape), _ptr(x), _ptr(topk_idx),
+                                        _ptr(slot_of), _ptr(expert_x), _ptr(expert_x_scale),
+                                        _ptr(workspace), _stream(stream), flags)
+    return _check(st, "moe_dispatch_ex", check)
 
 
 def plan_dispatch(shape: Shape, x, topk_idx, expert_num_tokens, expert_rank_offsets, slot_of,
@@ -291,9 +309,9 @@ class Buffers:
                            self.expert_rank_offsets, self.slot_of, self.src_of, self.workspace,
                            stream, check)
 
-    def dispatch(self, x, topk_idx, stream=None, check=True):
+    def dispatch(self, x, topk_idx, stream=None, check=True, early_x=False):
         return dispatch(self.shape, x, topk_idx, self.slot_of, self.expert_x, self.expert_x_scale,
-                        self.workspace, stream, check)
+                        self.workspace, stream, check, early_x)
 
     def plan_dispatch(self, x, topk_idx, stream=None, check=True):
         return plan_dispatch(self.shape, x, topk_idx, self.expert_num_tokens,

@@ -173,6 +173,13 @@ static moe_status plan_common(const moe_shape *shape, const int32_t *topk_idx,
 moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *topk_idx,
                         const int32_t *slot_of, void *expert_x, float *expert_x_scale,
                         void *workspace, void *stream) {
+  return moe_dispatch_ex(shape, x, topk_idx, slot_of, expert_x, expert_x_scale, workspace, stream, 0u);
+}
+
+moe_status moe_dispatch_ex(const moe_shape *shape, const void *x, const int32_t *topk_idx,
+                           const int32_t *slot_of, void *expert_x, float *expert_x_scale,
+                           void *workspace, void *stream, uint32_t flags) {
+  if ((flags & ~(uint32_t)MOE_DISPATCH_EARLY_X) != 0u) return MOE_ERR_INVALID_ARG;
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   if (shape->tokens_per_rank == 0) return MOE_OK;   // empty batch: nothing to read or write
@@ -196,6 +203,7 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *to
   p.K = shape->top_k;
   p.cap = shape->capacity;
   p.scale_t = shape->payload == MOE_PAYLOAD_FP8_E4M3_TSCALE;
+  p.early_x = (flags & MOE_DISPATCH_EARLY_X) ? 1 : 0;
   cudaStream_t s = (cudaStream_t)stream;
   return from_cuda(fp8 ? launch_dispatch_fp8(p, s) : launch_dispatch_bf16(p, s));
 }
@@ -218,7 +226,11 @@ moe_status moe_plan_dispatch(const moe_shape *shape, const void *x, const int32_
     st = plan_common(shape, topk_idx, nullptr, 0, expert_num_tokens, expert_rank_offsets, slot_of,
                      src_of, workspace, workspace_bytes, stream);
     if (st != MOE_OK || empty) return st;
-    return moe_dispatch(shape, x, topk_idx, slot_of, expert_x, expert_x_scale, workspace, stream);
+    // The kernel before the dispatch is this call's own plan, an ordinary
+    // launch that began after every earlier kernel (whatever wrote x) had
+    // completed, and that never writes x: the dispatch may read x early.
+    return moe_dispatch_ex(shape, x, topk_idx, slot_of, expert_x, expert_x_scale, workspace,
+                           stream, MOE_DISPATCH_EARLY_X);
   }
   if (!topk_idx || !slot_of || !expert_num_tokens || !expert_rank_offsets || !src_of)
     return MOE_ERR_INVALID_ARG;
@@ -238,6 +250,7 @@ moe_status moe_plan_dispatch(const moe_shape *shape, const void *x, const int32_
   f.d.K = shape->top_k;
   f.d.cap = shape->capacity;
   f.d.scale_t = shape->payload == MOE_PAYLOAD_FP8_E4M3_TSCALE;
+  f.d.early_x = 1;   // unused: the fused kernel is an ordinary launch
   f.topk_idx = topk_idx;
   f.expert_num_tokens = expert_num_tokens;
   f.expert_rank_offsets = expert_rank_offsets;

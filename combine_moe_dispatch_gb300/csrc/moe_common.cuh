@@ -127,6 +127,8 @@ struct DispatchParams {
   WsHeader *hdr;
   int N, H, E, K, cap;
   int scale_t;                 // fp8: scales [E, H/128, cap] instead of [E, cap, H/128]
+  int early_x;                 // 1: x is read before waiting for the previous kernel
+                               // (the caller asserts it was final before that kernel began)
 };
 
 // Plan and dispatch in one launch (moe_plan_dispatch.cu): taken up to

@@ -11,8 +11,13 @@
 //
 // How: work is cut by token, never by expert, so a skewed routing costs the
 // same as a uniform one.  The kernel may start while moe_plan is still
-// running (programmatic dependent launch): each warp loads its first task
-// and only then waits for the plan's slots.  Tasks are software-pipelined:
+// running (programmatic dependent launch).  By default each warp waits for
+// that kernel to complete before its first read of anything, x included:
+// the kernel before this one in the stream may be the one writing x.  When
+// the caller asserts that x was final before that kernel began (early_x:
+// it is moe_plan, or another kernel that leaves x alone), each warp loads
+// (fp8: and quantises) its first task first and only then waits for the
+// plan's slots.  Tasks are software-pipelined:
 // the next task's row and routing loads are in flight while this task's
 // stores are issued (and, for fp8, while it is quantised).  A warp takes
 // one (token, segment) task at a time from a grid sized to fill every SM;
@@ -24,8 +29,7 @@
 // butterfly over 16 lanes, and the block's scale (amax/448, exactly rounded)
 // and its reciprocal are computed once, by the lane that stores the scale,
 // and shared by all K copies; neighbouring lanes swap 8-byte halves so every
-// store is 16 bytes.  The first task is read and quantised before waiting
-// for the plan, which it does not need.
+// store is 16 bytes.
 //
 // Exact division, cheaply: q must be e4m3(RN(x / scale)).  With y =
 // RN(1/scale), RN(x y) corrected once with the exact remainder is RN(x /
@@ -70,9 +74,11 @@ dispatch_bf16_kernel(DispatchParams p) {
   const int tpr = (cpr + 32 * U - 1) / (32 * U);         // tasks per row
   const int64_t ntasks = (int64_t)p.N * tpr;
 
-  // The first task's read of x needs nothing from the plan: issue it before
-  // waiting for the plan to finish.
+  // The first task's read of x needs nothing from the plan: with early_x it
+  // is issued before waiting for the plan to finish.  Without, the previous
+  // kernel may still be writing x, and the wait comes first.
   if (warp0 >= ntasks) return;
+  if (!p.early_x) pdl_wait_for_previous();
   TaskCursor cur(warp0, nwarps, tpr);
   Bf16Task<U> t;
   bf16_load<U>(p, cur.g, cur.seg, lane, t);
@@ -110,12 +116,15 @@ dispatch_fp8_kernel(DispatchParams p) {
   const int64_t ntasks = (int64_t)p.N * tpr;
 
   // The first task's read and quantisation of x need nothing from the plan:
-  // they run before waiting for the plan to finish.  Then software-pipeline
+  // with early_x they run before waiting for the plan to finish.  Then software-pipeline
   // the tasks: the next task's x and routing loads are issued before this
   // task's stores, and it is quantised while those stores drain.
   // (The token and segment of a task come from a division here: a
   // TaskCursor's registers would make this kernel spill at its 80.)
+  // Without early_x the previous kernel may still be writing x: wait for it
+  // before the first read.
   if (warp0 >= ntasks) return;
+  if (!p.early_x) pdl_wait_for_previous();
   Fp8Raw<P> a;
   fp8_load<P>(p, warp0 / tpr, (int)(warp0 % tpr), lane, a);
   Fp8Task<P> t;

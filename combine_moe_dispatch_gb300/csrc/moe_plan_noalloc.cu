@@ -25,24 +25,31 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_plan_scratch[kNoAllocScratchBytes];
 
-// Device address of g_plan_scratch, looked up once per device with that
-// device current.  In host code the symbol itself is only a host-side
-// stand-in, so kernels must be given this address, never the symbol.
-std::once_flag g_once[kMaxDevices];
+// Device address of g_plan_scratch, looked up with that device current.  In
+// host code the symbol itself is only a host-side stand-in, so kernels must
+// be given this address, never the symbol.  Only a successful lookup is
+// kept: a lookup that failed (for example one made while the stream was
+// being captured) is tried again by the next call.
+std::mutex g_mutex;
 void *g_addr[kMaxDevices];
-cudaError_t g_err[kMaxDevices];
 
 cudaError_t scratch_address(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_addr[dev]) {
     void *p = nullptr;
-    g_err[dev] = cudaGetSymbolAddress(&p, g_plan_scratch);
+    e = cudaGetSymbolAddress(&p, g_plan_scratch);
+    if (e != cudaSuccess) {
+      // clear the error the failed lookup recorded, so that the next
+      // launch check of this thread does not mistake it for its own
+      (void)cudaGetLastError();
+      return e;
+    }
     g_addr[dev] = p;
-  });
-  if (g_err[dev] != cudaSuccess) return g_err[dev];
+  }
   *out = g_addr[dev];
   return cudaSuccess;
 }
@@ -67,7 +74,11 @@ extern "C" moe_status moe_plan_noalloc(const moe_shape *shape, const int32_t *to
                ? MOE_ERR_INVALID_ARG
                : MOE_ERR_UNSUPPORTED;
   if (need > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
-  if (!topk_idx || !expert_num_tokens || !expert_rank_offsets || !slot_of || !src_of || !status_out)
+  // An empty batch (T = 0) reads no routes and writes no slots: topk_idx and
+  // slot_of may then be NULL, as for moe_plan.
+  const bool empty = shape->tokens_per_rank == 0;
+  if ((!empty && (!topk_idx || !slot_of)) || !expert_num_tokens || !expert_rank_offsets ||
+      !src_of || !status_out)
     return MOE_ERR_INVALID_ARG;
   if (((uintptr_t)status_out & 3u) != 0) return MOE_ERR_ALIGNMENT;
 

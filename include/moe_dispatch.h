@@ -166,17 +166,38 @@ moe_status moe_plan_masked(const moe_shape *shape, const int32_t *topk_idx,
  *       and sets the status word (BAD_EXPERT / CAPACITY); an entry with
  *       slot_of = -1 (not routed, see moe_plan_masked) is skipped silently.
  * Ordering: the kernel is launched as a programmatic dependent of the
- *       previous kernel in the stream (normally moe_plan's) and starts
- *       loading x before that kernel has completed; it reads slot_of, the
- *       routes and the status only after.  So x must not be written by the
- *       kernel just before this call in the stream if that kernel lets its
- *       dependents start early (griddepcontrol.launch_dependents); moe_plan
- *       itself waits for every earlier kernel.
+ *       previous kernel in the stream (normally moe_plan's), so its blocks
+ *       may start before that kernel has completed; each waits for it to
+ *       complete before its first read of any input, x included.  Any
+ *       kernel may therefore produce x just before this call, even one that
+ *       lets its dependents start early (griddepcontrol.launch_dependents).
+ *       moe_dispatch_ex with MOE_DISPATCH_EARLY_X reads x sooner.
  * Host errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA. */
 moe_status moe_dispatch(const moe_shape *shape, const void *x,
                         const int32_t *topk_idx, const int32_t *slot_of,
                         void *expert_x, float *expert_x_scale,
                         void *workspace, void *stream);
+
+/* Flags of moe_dispatch_ex. */
+enum {
+  /* The caller asserts that x was final before the kernel that precedes this
+   * call in the stream began: that kernel is moe_plan (an ordinary launch,
+   * which starts only after every earlier kernel has completed, and which
+   * never writes x) or another kernel that leaves x alone.  The dispatch
+   * then loads (fp8: and quantises) the first rows of x while that kernel
+   * is still finishing, and waits for it only before reading slot_of, the
+   * routes and the status.  Without the assertion holding, rows may be
+   * dispatched from stale x. */
+  MOE_DISPATCH_EARLY_X = 1u
+};
+
+/* moe_dispatch with flags (0 = moe_dispatch).  Same inputs, outputs and
+ * errors; an unknown flag bit is INVALID_ARG.  moe_plan_dispatch, when it
+ * runs as two launches, dispatches this way after its own plan. */
+moe_status moe_dispatch_ex(const moe_shape *shape, const void *x,
+                           const int32_t *topk_idx, const int32_t *slot_of,
+                           void *expert_x, float *expert_x_scale,
+                           void *workspace, void *stream, uint32_t flags);
 
 /* Plan and dispatch in one call: the outputs of moe_plan followed by
  * moe_dispatch, bit for bit, from a single kernel launch where the shape

@@ -120,6 +120,15 @@ def test_host_rejections_enqueue_nothing(lib):
     assert lib.moe_workspace_init(None, 256, None) == Status.INVALID_ARG
     assert lib.moe_workspace_init(_p(A + 4), 256, None) == Status.ALIGNMENT
     assert lib.moe_workspace_set_debug(None, 1, 0, None) == Status.INVALID_ARG
+    # moe_dispatch_ex: moe_dispatch's checks, and no flag bit but EARLY_X
+    dx = lib.moe_dispatch_ex
+    assert dx(sp, None, _p(A), _p(A), _p(A), None, _p(A), None, 1) == Status.INVALID_ARG
+    assert dx(sp, _p(A + 8), _p(A), _p(A), _p(A), None, _p(A), None, 1) == Status.ALIGNMENT
+    assert dx(sp, _p(A), _p(A), _p(A), _p(A), None, None, None, 0) == Status.WORKSPACE
+    for flags in (2, 4, 1 | 8, 0x80000000):
+        assert dx(sp, _p(A), _p(A), _p(A), _p(A), None, _p(A), None, flags) == Status.INVALID_ARG
+    assert dx(ctypes.byref(Shape(3, 0, 256, 8, 2, 4, 1)), None, None, None, None, None, None, None,
+              moe.DISPATCH_EARLY_X) == Status.OK
 
 
 @pytest.mark.parametrize("fields,over,under", [
@@ -205,6 +214,9 @@ def test_plan_noalloc_host_checks(lib, payload):
     s = Shape(1, 4, 256, 8, 2, 8, payload)
     assert na(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A), None, None) == Status.INVALID_ARG
     assert na(ctypes.byref(s), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A + 2), None) == Status.ALIGNMENT
+    # routes and slots are required unless the batch is empty (T = 0, tested on the GPU)
+    assert na(ctypes.byref(s), None, _p(A), _p(A), _p(A), _p(A), _p(A), None) == Status.INVALID_ARG
+    assert na(ctypes.byref(s), _p(A), _p(A), _p(A), None, _p(A), _p(A), None) == Status.INVALID_ARG
 
 
 def test_masked_plan_and_shared_combine_host_checks(lib):

@@ -45,3 +45,27 @@ def test_recorded_traffic_lines_parse():
         lines = [l.split() for l in f if l.strip().startswith("traffic ")]
     assert lines and all(len(l) == 5 and l[1] in calls and l[2] in WORKLOADS and int(l[3]) > 0
                          for l in lines)
+
+
+def test_step_moves_the_bytes_of_every_row():
+    # the step's calls (fused plan + bf16 dispatch, the early-reading fp8
+    # dispatch, combine) move exactly the bytes of the rows a1-a6
+    for wl in WORKLOADS.values():
+        cb = bench.call_bytes(wl)
+        assert (sum(cb[bench.base_call(c)] for c in bench.step_sequence(wl))
+                == sum(cb[c] for c in bench.step_calls(wl)))
+    assert bench.base_call("dispatch_fp8_early") == "dispatch_fp8"
+    assert bench.base_call("combine") == "combine"
+
+
+def test_dispatch_incl_plan_reports_both_two_launch_orders():
+    wl = WORKLOADS["dsv3_decode"]
+    cb = bench.call_bytes(wl)
+    ms = {"plan_dispatch_fp8": 0.016, "plan+dispatch_fp8": 0.018, "plan+dispatch_fp8_early": 0.017}
+    d = bench.dispatch_incl_plan(["plan", "dispatch_fp8"], ms, cb, 6782.4)
+    b = cb["plan"] + cb["dispatch_fp8"]
+    assert abs(d["fp8"]["us"] - 16.0) < 1e-9
+    assert abs(d["fp8"]["frac_of_peak"] - b / 16e-6 / 1e9 / 6782.4) < 1e-12
+    assert abs(d["fp8"]["two_launches_us"] - 17.0) < 1e-9
+    assert abs(d["fp8"]["two_launches_default_us"] - 18.0) < 1e-9
+    assert set(bench.EXTRA_WORKLOADS) <= set(WORKLOADS)

@@ -86,14 +86,10 @@ def test_fused_workload_full_size(name):
     wl = WORKLOADS[name]
     d = inputs.make(wl, 0)
     big = wl.E * wl.cap * wl.H > (1 << 28)
-    sample = None
-    if big and wl.N > 1024:
-        sample = np.sort(np.random.default_rng(0).choice(wl.N, 1024, replace=False))
-        sample[0], sample[-1] = 0, wl.N - 1
     payloads = ("bf16", "fp8")
     res = gpu_check.run_case(wl.R, wl.T, wl.H, wl.E, wl.K, wl.cap, d["topk_idx"], d["x"],
                              d["topk_weights"], payloads, fused=True,
-                             expert_y="device" if big else "host", combine_tokens=sample)
+                             expert_y="device" if big else "host", combine_tokens=None)
     print(name, res)
     torch.cuda.empty_cache()
 

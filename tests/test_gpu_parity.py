@@ -211,17 +211,18 @@ def test_both_plan_paths_share_one_workspace():
 
 @pytest.mark.parametrize("name", ["tiny", "mixtral", "dsv3_decode", "dsv3_prefill", "kimi_decode"])
 def test_workload_full_size(name):
+    """Every workload at its full size, in the bench's launch configuration:
+    every plan output, every dispatched row, and the combine of every token.
+    Where expert_y is too large for the host (E*cap*H > 2^28) it is drawn on
+    the device, and only the N*K routed rows (at most 0.94 GB, at prefill)
+    come back for the oracle."""
     wl = WORKLOADS[name]
     d = inputs.make(wl, 0)
     big = wl.E * wl.cap * wl.H > (1 << 28)
-    sample = None
-    if big and wl.N > 1024:
-        sample = np.sort(np.random.default_rng(0).choice(wl.N, 1024, replace=False))
-        sample[0], sample[-1] = 0, wl.N - 1
     payloads = wl.payloads
     res = gpu_check.run_case(wl.R, wl.T, wl.H, wl.E, wl.K, wl.cap, d["topk_idx"], d["x"],
                              d["topk_weights"], payloads,
-                             expert_y="device" if big else "host", combine_tokens=sample)
+                             expert_y="device" if big else "host", combine_tokens=None)
     print(name, res)
     torch.cuda.empty_cache()
 
