@@ -27,6 +27,7 @@
 namespace moe {
 
 constexpr int kCombineThreads = 256;
+
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 
 __device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4 &v) {
@@ -65,16 +66,19 @@ combine_kernel(CombineParams p) {
 
   if (warp0 >= ntasks) return;
   TaskCursor cur(warp0, nwarps, tpr);
-  for (int64_t task = warp0; task < ntasks; task += nwarps, cur = cur.next()) {
+  // The routing of a warp's next task is loaded while the current task's
+  // rows are read, so each task waits for one memory round trip (its rows),
+  // not two (its routing, then its rows).
+  int e_l = -1, s_l = -1;
+  float w_l = 0.0f;
+  if (lane < p.K) {
+    e_l = __ldg(p.topk_idx + (int64_t)cur.g * p.K + lane);
+    s_l = __ldg(p.slot_of + (int64_t)cur.g * p.K + lane);
+    w_l = __ldg(p.topk_weights + (int64_t)cur.g * p.K + lane);
+  }
+  for (int64_t task = warp0; task < ntasks; task += nwarps) {
     const int64_t g = cur.g;
     const int seg = cur.seg;
-    int e_l = -1, s_l = -1;
-    float w_l = 0.0f;
-    if (lane < p.K) {
-      e_l = __ldg(p.topk_idx + g * p.K + lane);
-      s_l = __ldg(p.slot_of + g * p.K + lane);
-      w_l = __ldg(p.topk_weights + g * p.K + lane);
-    }
     // slot -1: an entry the plan did not route (skipped; a token with no
     // routed entry gets y = +0).  Other out-of-range entries are reported.
     const bool routed = lane < p.K && s_l != -1;
@@ -83,6 +87,10 @@ combine_kernel(CombineParams p) {
     if (seg == 0 && routed && !ok)
       report_status(p.hdr, e_ok ? MOE_ERR_CAPACITY : MOE_ERR_BAD_EXPERT);
     const unsigned okmask = __ballot_sync(kFullMask, ok);
+    const int ce_l = e_l, cs_l = s_l;
+    const float cw_l = w_l;
+    cur = cur.next();
+    const bool more = task + nwarps < ntasks;
 
     const int c0 = seg * cpt + lane;
     float acc[U][8];
@@ -112,8 +120,8 @@ combine_kernel(CombineParams p) {
 #pragma unroll
       for (int kk = 0; kk < KG; ++kk) {
         const int k = kb + kk;
-        const int e = __shfl_sync(kFullMask, e_l, k & 31);
-        const int s = __shfl_sync(kFullMask, s_l, k & 31);
+        const int e = __shfl_sync(kFullMask, ce_l, k & 31);
+        const int s = __shfl_sync(kFullMask, cs_l, k & 31);
         const bool use = k < p.K && ((okmask >> (k & 31)) & 1u);
         const uint16_t *row = p.expert_y + ((int64_t)(use ? e : 0) * p.cap + (use ? s : 0)) * p.H;
 #pragma unroll
@@ -123,10 +131,15 @@ combine_kernel(CombineParams p) {
                                       : make_uint4(0, 0, 0, 0);
         }
       }
+      if (kb == 0 && more && lane < p.K) {   // the next task's routing, behind this task's first rows
+        e_l = __ldg(p.topk_idx + (int64_t)cur.g * p.K + lane);
+        s_l = __ldg(p.slot_of + (int64_t)cur.g * p.K + lane);
+        w_l = __ldg(p.topk_weights + (int64_t)cur.g * p.K + lane);
+      }
 #pragma unroll
       for (int kk = 0; kk < KG; ++kk) {
         const int k = kb + kk;
-        const float w = __shfl_sync(kFullMask, w_l, k & 31);
+        const float w = __shfl_sync(kFullMask, cw_l, k & 31);
         if (k < p.K && ((okmask >> (k & 31)) & 1u)) {
 #pragma unroll
           for (int u = 0; u < U; ++u) fma8(acc[u], w, v[kk][u]);

@@ -149,12 +149,14 @@ struct FusedParams {
   int units;                   // bf16: 16-byte chunks per lane per task; fp8: block pairs
   int tpr;                     // tasks per token row
   int64_t ntasks;              // N * tpr
-  int q_tasks;                 // tasks per block (a contiguous run)
+  int q_tasks;                 // tasks per block, at most (block b: [b*ntasks/grid, (b+1)*ntasks/grid))
   int grid;                    // blocks, one per SM at most
   int owned;                   // experts per block for counts and offsets
   int max_run;                 // routed entries of one block's tokens, at most
   int ebits;                   // bits of the largest expert id
   int vec_idx;                 // topk_idx is 16-byte aligned (16-byte loads)
+  int task_elems;              // x elements of one whole task
+  size_t stage_off;            // dynamic shared memory offset of the staged second tasks
   size_t smem_bytes;
 };
 
@@ -273,6 +275,23 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *flag, uint32_t want, u
     __nanosleep(32);
   }
   return false;
+}
+
+// Barrier `id` (1..15) over the first `n` threads of the block (n a
+// multiple of 32; every thread that takes part passes the same id and n).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// named_sync that also returns the AND of `pred` over the n threads.
+__device__ __forceinline__ bool named_sync_and(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p, q;\n\t"
+               "setp.ne.u32 p, %1, 0;\n\t"
+               "bar.red.and.pred q, %2, %3, p;\n\t"
+               "selp.u32 %0, 1, 0, q;\n\t}"
+               : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(n) : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ uint32_t cluster_cta_rank() {

@@ -45,6 +45,7 @@ namespace moe {
 
 constexpr int kDispatchThreads = 256;
 
+
 __device__ __forceinline__ Routes load_routes(const DispatchParams &p, int64_t g, int lane) {
   Routes r{-1, -1};
   if (lane < p.K) {
@@ -134,6 +135,10 @@ dispatch_fp8_kernel(DispatchParams p) {
   for (int64_t task = warp0; task < ntasks; task += nwarps) {
     const int64_t next = task + nwarps;
     const bool more = next < ntasks;
+    // The next kernel may start launching once every warp is on its last
+    // task (measured: 13.5 -> 13.1 us alone, 12.5 us when reading x early,
+    // at DeepSeek-V3 decode; the bf16 kernel measured slower with it).
+    if (!more) pdl_allow_dependents();
     Routes rn;
     if (more) {
       const int64_t g = next / tpr;

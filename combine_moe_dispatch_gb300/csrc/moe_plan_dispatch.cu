@@ -12,36 +12,48 @@
 // boundary after it, is a third of plan + dispatch.  Here no block waits for
 // another: each finds the slots it needs from the routing table itself.
 //
-// How: block b takes the contiguous run of Q (token, segment) tasks
-// [b*Q, (b+1)*Q), so its tokens form one range [g_lo, g_hi] and its routed
-// entries the run [g_lo*K, (g_hi+1)*K).  The slot of an entry (g, k) with
-// expert e is the number of entries of e before the run plus the number of
-// entries of e inside the run before (g, k).  Block b also owns the experts
-// [b*O, (b+1)*O) and writes their counts and offsets rows.
+// How: block b takes the contiguous run of (token, segment) tasks
+// [b*n/G, (b+1)*n/G) (n tasks, G blocks, one per SM), so its tokens form one
+// range [g_lo, g_hi] and its routed entries the run [g_lo*K, (g_hi+1)*K).
+// The slot of an entry (g, k) with expert e is the number of entries of e
+// before the run plus the number of entries of e inside the run before
+// (g, k).  Block b also owns the experts [b*O, (b+1)*O) and writes their
+// counts and offsets rows.  The kernel is a programmatic dependent of the
+// previous kernel: its blocks may be scheduled while that kernel drains, and
+// wait for it before reading anything.
 //   1. Thread 0 starts one bulk copy (cp.async.bulk, completed on an
 //      mbarrier, waited for with a time limit) of the whole routing table
 //      into shared memory, and every warp issues the loads of its first
 //      task's x segment.  The copy engine leaves the SM's load pipeline to
 //      the x loads; when the table went through that pipeline as plain
 //      loads, it waited behind them (about 2 us at DeepSeek-V3 decode).
-//   2. The block marks the experts of its run in a shared byte table.
+//      bf16: each warp's second task is bulk-copied into shared memory too.
+//   2-4 are the planner warps' work (all warps for bf16, 12 of 24 for fp8);
+//      for fp8 the other warps quantise their first task meanwhile, so the
+//      first stores wait for the longer of the plan and the quantisation,
+//      not for their sum.
+//   2. The planners mark the experts of the run in a shared byte table.
 //   3. Warp 0 ranks the run stably (one ballot per bit of the expert id finds
 //      the lanes with the same expert; a shared per-expert counter carries
-//      the count across 32-entry batches).  Meanwhile the other warps scan
-//      the table in shared memory: an entry before the run whose expert is
-//      marked adds one to that expert's count, and an entry of an owned
-//      expert adds one to that expert's count for its rank.
-//   4. slot = count before the run + rank in the run, kept in shared memory.
-//   5. The warps run their tasks as moe_dispatch does, software-pipelined,
-//      with the routes read from shared memory.  Each warp quantises (fp8)
-//      its first task at the end of step 3, after its share of the scan.
+//      the count across 32-entry batches).  Meanwhile the other planners
+//      scan the entries before the run in shared memory: one whose expert is
+//      marked adds one to that expert's count.
+//   4. slot = count before the run + rank in the run, kept in shared memory;
+//      a slot at or beyond cap is the capacity error (every entry is in some
+//      block's run, so the runs see every expert that overflows).
+//   5. After one block barrier the warps run their tasks as moe_dispatch
+//      does, software-pipelined, with the routes read from shared memory
+//      (the planners first quantise their own first task).  A warp starting
+//      its last task lets the next kernel in the stream begin to launch.
 //   6. The block's first warp to run out of tasks adds the block's arrival
 //      and error bits to one workspace word; the last block to arrive writes
 //      the status word (no block waits for another).  Issued by a warp with
 //      stores still to make, that contended atomic delayed it by ~0.8 us.
 //   7. After its tasks the block writes slot_of and src_of for the tokens
-//      whose first segment it holds, and each owner its experts' counts and
-//      offsets rows: stores issued earlier would wait behind the x loads.
+//      whose first segment it holds (stores issued earlier would wait behind
+//      the x loads); then it counts its owned experts' entries per rank over
+//      the whole table and writes their counts and offsets rows.  Off the
+//      path to the first store, that scan overlaps the drain of the stores.
 // Every block copies and scans all N*K routes, which pays only while the
 // table is small: the fused path is taken up to kFusedMaxEntries routed
 // entries (at Kimi-K2 decode, 32768 entries, two launches measured faster);
@@ -62,29 +74,63 @@ namespace moe {
 
 // bf16 and fp8 tasks behind one interface: load (no routing needed), prep
 // (fp8: quantise; bf16: nothing), store to the K rows.
+// Warps of a block that make the plan (the rest quantise meanwhile): all of
+// them for bf16, which has nothing to quantise; a part for fp8.
+#ifndef MOE_FUSED_PLAN_WARPS
+#define MOE_FUSED_PLAN_WARPS 12
+#endif
+
 template <int U>
 struct Bf16Path {
   using Raw = Bf16Task<U>;
   using Out = Bf16Task<U>;
+  static constexpr int kPlanWarps = 0;   // all
+  static constexpr bool kStage2 = true;
   static __device__ __forceinline__ void load(const DispatchParams &p, const TaskCursor &c,
                                               int lane, Raw &a) {
     bf16_load<U>(p, c.g, c.seg, lane, a);
+  }
+  // the task from its copy in shared memory (s: the task's first element)
+  static __device__ __forceinline__ void load_staged(const DispatchParams &p, const TaskCursor &c,
+                                                     int lane, const uint16_t *s, Raw &a) {
+    const int cpr = p.H / 8;
+    a.g = c.g;
+    a.seg = c.seg;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c16 = c.seg * 32 * U + lane + u * 32;
+      a.v[u] = c16 < cpr ? *reinterpret_cast<const uint4 *>(s + (lane + u * 32) * 8)
+                         : make_uint4(0, 0, 0, 0);
+    }
   }
   static __device__ __forceinline__ void prep(const Raw &a, int, Out &t) { t = a; }
   static __device__ __forceinline__ void store(const DispatchParams &p, int lane, const Out &t,
                                                const Routes &r) {
     bf16_store<U>(p, lane, t, r);
   }
-  static __device__ __forceinline__ int64_t token(const Out &t) { return t.g; }
 };
 
 template <int P>
 struct Fp8Path {
   using Raw = Fp8Raw<P>;
   using Out = Fp8Task<P>;
+  static constexpr int kPlanWarps = MOE_FUSED_PLAN_WARPS;
+  static constexpr bool kStage2 = false;
   static __device__ __forceinline__ void load(const DispatchParams &p, const TaskCursor &c,
                                               int lane, Raw &a) {
     fp8_load<P>(p, c.g, c.seg, lane, a);
+  }
+  static __device__ __forceinline__ void load_staged(const DispatchParams &p, const TaskCursor &c,
+                                                     int lane, const uint16_t *s, Raw &a) {
+    const int half = lane >> 4, sub = lane & 15, nb = p.H / 128;
+    a.g = c.g;
+    a.seg = c.seg;
+#pragma unroll
+    for (int it = 0; it < P; ++it) {
+      const int blk = c.seg * 2 * P + it * 2 + half;
+      a.v[it] = blk < nb ? *reinterpret_cast<const uint4 *>(s + (it * 2 + half) * 128 + sub * 8)
+                         : make_uint4(0, 0, 0, 0);
+    }
   }
   static __device__ __forceinline__ void prep(const Raw &a, int lane, Out &t) {
     fp8_quantise<P>(a, lane, t);
@@ -93,7 +139,6 @@ struct Fp8Path {
                                                const Routes &r) {
     fp8_store<P>(p, lane, t, r);
   }
-  static __device__ __forceinline__ int64_t token(const Out &t) { return t.g; }
 };
 
 // Routes of token g from the block's run: lane k < K holds (expert, slot);
@@ -131,14 +176,23 @@ __device__ __forceinline__ void finish_status(WsHeader *hdr, uint32_t arrived) {
   hdr->arrivals = 0;
 }
 
+
 template <class Path, int THREADS>
 __global__ void __launch_bounds__(THREADS, 1)
 plan_dispatch_kernel(FusedParams p) {
+  // a programmatic dependent of the previous kernel: nothing is read before
+  // that kernel has completed
+  pdl_wait_for_previous();
   constexpr int kWarps = THREADS / 32;
-  constexpr int kScanners = THREADS - 32;   // warps 1.. scan, warp 0 ranks
+  // planner warps: warp 0 ranks the run, the others scan the prefix
+  constexpr int kPlanWarps = (Path::kPlanWarps > 0 && Path::kPlanWarps < kWarps) ? Path::kPlanWarps : kWarps;
+  static_assert(kPlanWarps >= 2, "one warp ranks, at least one scans");
+  constexpr int kPlanThreads = kPlanWarps * 32;
+  constexpr int kScanThreads = kPlanThreads - 32;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t s_bar;
-  __shared__ uint32_t s_err, s_fin;
+  __shared__ uint32_t s_err, s_fin, s_fail;
+  __shared__ __align__(8) uint64_t s_xbar[Path::kStage2 ? kWarps : 1];   // per warp: its staged second task
   const int E = p.d.E, K = p.d.K, R = p.R, cap = p.d.cap;
   const int total = p.d.N * K;
   const size_t tab_bytes = ((size_t)total * 4 + 15) & ~(size_t)15;
@@ -151,8 +205,11 @@ plan_dispatch_kernel(FusedParams p) {
   int32_t *s_rslot = s_rexp + p.max_run;                                   // [run] rank, then slot
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t t0 = (int64_t)blockIdx.x * p.q_tasks;
-  const int64_t t1 = min(t0 + (int64_t)p.q_tasks, p.ntasks);
+  const bool planner = warp < kPlanWarps;
+  // block b: tasks [b * ntasks / grid, (b + 1) * ntasks / grid), so that the
+  // runs differ by one task at most and every SM gets a block
+  const int64_t t0 = (int64_t)blockIdx.x * p.ntasks / p.grid;
+  const int64_t t1 = ((int64_t)blockIdx.x + 1) * p.ntasks / p.grid;
   const int64_t g_lo = t0 / p.tpr, g_hi = (t1 - 1) / p.tpr;
   const int lo_ent = (int)(g_lo * K);
   const int run = (int)(g_hi - g_lo + 1) * K;
@@ -174,6 +231,24 @@ plan_dispatch_kernel(FusedParams p) {
   TaskCursor cur(my0, kWarps, p.tpr);
   typename Path::Raw a;
   if (has0) Path::load(p.d, cur, lane, a);
+  // bf16: the warp's second task is copied into shared memory now, by the
+  // copy engine, so x is read while the plan runs, before the stores start,
+  // instead of between them.  (For fp8 it measured slower: the copies delay
+  // the routing table, and the quantisers wait for the first task's x.)
+  const uint16_t *s_x2 = reinterpret_cast<const uint16_t *>(smem + p.stage_off) +
+                         (size_t)warp * p.task_elems;
+  const bool has1 = Path::kStage2 && my0 + kWarps < t1;
+  if (Path::kStage2 && lane == 0) {
+    mbar_init(&s_xbar[warp], 1);
+    if (has1) {
+      const TaskCursor c1 = cur.next();
+      const int64_t e0 = (int64_t)c1.seg * p.task_elems;
+      const int64_t n = min((int64_t)p.task_elems, (int64_t)p.d.H - e0);
+      bulk_copy_g2s(const_cast<uint16_t *>(s_x2), p.d.x + (int64_t)c1.g * p.d.H + e0,
+                    (uint32_t)(n * 2), &s_xbar[warp]);
+    }
+  }
+  bool stage_pending = has1;   // the copy may still be in flight
   for (int i = tid; i < E; i += THREADS) {
     s_code[i] = 0;
     s_pre[i] = 0;
@@ -183,13 +258,89 @@ plan_dispatch_kernel(FusedParams p) {
   if (tid == 0) {
     s_err = 0;
     s_fin = 0;
+    s_fail = 0;
   }
-  __syncthreads();   // also publishes the barrier's initialisation
-  const bool tab_ok = nbulk == 0 || mbar_wait_bounded(&s_bar, 0, global_timer_ns() + kDefaultTimeoutNs);
-  if (!__syncthreads_and(tab_ok)) {
-    // the copy did not land in time: wait once more (bounded) so that no
-    // copy into this block's shared memory is left in flight, report, and
-    // write nothing
+  __syncthreads();   // also publishes the barrier's initialisation and the zeroed tables
+
+  // 2-4 run on the planner warps alone (named barrier 1); the other warps
+  // quantise their first task (fp8) meanwhile, as soon as its x lands, so
+  // that the first stores wait for the plan or the quantisation, whichever
+  // ends later, instead of for both one after the other.
+  typename Path::Out t;
+  uint32_t err = 0;
+  if (planner) {
+    const bool ok = nbulk == 0 || mbar_wait_bounded(&s_bar, 0, global_timer_ns() + kDefaultTimeoutNs);
+    const bool tab_ok = named_sync_and(1, kPlanThreads, ok);
+    if (tid == 0) s_fail = tab_ok ? 0u : 1u;
+    if (tab_ok) {
+      // 2. mark the run's experts
+      for (int i = tid; i < run; i += kPlanThreads) {
+        const int e = s_tab[lo_ent + i];
+        const bool in = (unsigned)e < (unsigned)E;
+        s_rexp[i] = in ? e : -1;
+        if (in) s_code[e] = 1;   // every writer stores the same value
+        else err |= kErrBadExpert;
+      }
+      named_sync(1, kPlanThreads);
+
+      // 3. rank the run (warp 0) / count the entries before the run (the
+      //    other planner warps)
+      if (warp == 0) {
+        const unsigned lt = (1u << lane) - 1u;
+        for (int i0 = 0; i0 < run; i0 += 32) {
+          const int i = i0 + lane;
+          const int e = i < run ? s_rexp[i] : -1;
+          const unsigned same = peers_with_same_key(e, p.ebits);
+          const int before = __popc(same & lt);
+          const int base = e >= 0 ? s_loc[e] : 0;
+          __syncwarp();
+          if (e >= 0 && before == 0) s_loc[e] = base + __popc(same);
+          __syncwarp();
+          if (i < run) s_rslot[i] = base + before;
+        }
+      } else {
+        // An entry before the run whose expert the run uses adds one to
+        // that expert's count before the run.  Only the prefix is read, and
+        // nothing else is counted here: the owned experts' per-rank counts
+        // are needed only for the offsets rows, written after the tasks.  A
+        // bad id is reported by its own run's block.
+        auto count_pre = [&](int e) {
+          if ((unsigned)e < (unsigned)E && s_code[e]) atomicAdd(&s_pre[e], 1);
+        };
+        const int4 *t4 = reinterpret_cast<const int4 *>(s_tab);
+        const int n4 = lo_ent >> 2;
+        for (int j = tid - 32; j < n4; j += kScanThreads) {
+          const int4 w = t4[j];
+          count_pre(w.x);
+          count_pre(w.y);
+          count_pre(w.z);
+          count_pre(w.w);
+        }
+        for (int q = 4 * n4 + tid - 32; q < lo_ent; q += kScanThreads) count_pre(s_tab[q]);
+      }
+      named_sync(1, kPlanThreads);
+
+      // 4. slots (in shared memory only: the plan outputs are written after
+      //    the tasks, so no store here waits behind the x loads in flight);
+      //    errors.  An expert over capacity has an entry with slot cap, in
+      //    some block's run: the runs' slots alone find every capacity error.
+      for (int i = tid; i < run; i += kPlanThreads) {
+        const int e = s_rexp[i];
+        const int slot = e >= 0 ? s_pre[e] + s_rslot[i] : -1;
+        if (e >= 0 && slot >= cap) err |= kErrCapacity;
+        s_rslot[i] = slot;
+      }
+      if (err) atomicOr(&s_err, err);
+    }
+  } else if (has0) {
+    Path::prep(a, lane, t);
+  }
+  __syncthreads();
+  if (s_fail) {
+    // the table copy did not land in time: wait once more (bounded) so that
+    // no copy into this block's shared memory is left in flight, report,
+    // and write nothing
+    if (stage_pending) mbar_wait_bounded(&s_xbar[warp], 0, global_timer_ns() + kDefaultTimeoutNs);
     if (tid == 0) {
       mbar_wait_bounded(&s_bar, 0, global_timer_ns() + kDefaultTimeoutNs);
       const uint32_t code = arrival_code(kErrTimeout);
@@ -197,105 +348,45 @@ plan_dispatch_kernel(FusedParams p) {
     }
     return;
   }
-
-  // 2. mark the run's experts
-  uint32_t err = 0;
-  for (int i = tid; i < run; i += THREADS) {
-    const int e = s_tab[lo_ent + i];
-    const bool ok = (unsigned)e < (unsigned)E;
-    s_rexp[i] = ok ? e : -1;
-    if (ok) s_code[e] = 1;   // every writer stores the same value
-    else err |= kErrBadExpert;
-  }
-  __syncthreads();
-
-  // 3. rank the run (warp 0) / count entries before the run and of owned
-  //    experts (the other warps)
-  if (warp == 0) {
-    const unsigned lt = (1u << lane) - 1u;
-    for (int i0 = 0; i0 < run; i0 += 32) {
-      const int i = i0 + lane;
-      const int e = i < run ? s_rexp[i] : -1;
-      const unsigned same = peers_with_same_key(e, p.ebits);
-      const int before = __popc(same & lt);
-      const int base = e >= 0 ? s_loc[e] : 0;
-      __syncwarp();
-      if (e >= 0 && before == 0) s_loc[e] = base + __popc(same);
-      __syncwarp();
-      if (i < run) s_rslot[i] = base + before;
-    }
-  } else {
-    const int tk = p.T * K;      // entries per rank
-    // entry q of expert e: before the run and marked -> s_pre; owned -> its
-    // rank's counter.  The rank r = q / tk is computed once per 16 bytes.
-    auto visit = [&](int q, int e, int r) {
-      const bool ok = (unsigned)e < (unsigned)E;   // a bad id is reported by its run's block
-      const int ec = ok ? e : 0;
-      if (ok && q < lo_ent && s_code[ec]) atomicAdd(&s_pre[ec], 1);
-      const unsigned o = (unsigned)(e - own0);
-      if (ok && o < (unsigned)p.owned) atomicAdd(&s_ocnt[o * R + r], 1);
-    };
-    const int4 *t4 = reinterpret_cast<const int4 *>(s_tab);
-    const int n4 = total >> 2;
-    for (int j = tid - 32; j < n4; j += kScanners) {
-      const int4 w = t4[j];
-      const int q = 4 * j;
-      // q is a multiple of 4, so with tk >= 2 the 4 entries cross at most
-      // one rank boundary after q's own rank; tk = 1 divides each entry
-      const int r = q / tk;
-      const int nxt = (r + 1) * tk;
-      const bool one = tk >= 2;
-      visit(q, w.x, r);
-      visit(q + 1, w.y, one ? r + (q + 1 >= nxt) : (q + 1) / tk);
-      visit(q + 2, w.z, one ? r + (q + 2 >= nxt) : (q + 2) / tk);
-      visit(q + 3, w.w, one ? r + (q + 3 >= nxt) : (q + 3) / tk);
-    }
-    for (int q = 4 * n4 + tid - 32; q < total; q += kScanners) visit(q, s_tab[q], q / tk);
-  }
-  // Each warp quantises (fp8) its first task once its share of the plan is
-  // done: the scan waits on shared-memory atomics, and the quantisation
-  // fills the issue slots the slowest scanners leave.  Before the scan it
-  // measured slower (17.2 against 16.6 us at DeepSeek-V3 decode), after the
-  // plan's last barrier 16.6 against 16.5 us.
-  typename Path::Out t;
-  if (has0) Path::prep(a, lane, t);
-  __syncthreads();
-
-  // 4. slots (in shared memory only: the plan outputs are written after the
-  //    tasks, so no store here waits behind the x loads in flight); errors
-  for (int i = tid; i < run; i += THREADS) {
-    const int e = s_rexp[i];
-    const int slot = e >= 0 ? s_pre[e] + s_rslot[i] : -1;
-    if (e >= 0 && slot >= cap) err |= kErrCapacity;
-    s_rslot[i] = slot;
-  }
-  for (int j = warp; j < p.owned; j += kWarps) {
-    if (own0 + j >= E) break;
-    int sum = 0;
-    for (int r = lane; r < R; r += 32) sum += s_ocnt[j * R + r];
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-    if (sum > cap) err |= kErrCapacity;
-  }
-  if (err) atomicOr(&s_err, err);
-  __syncthreads();
+  if (planner && has0) Path::prep(a, lane, t);   // the planners' first task, after the plan
 
   // 5. the tasks, software-pipelined as in moe_dispatch, starting from the
   //    first task quantised above.
   if (has0) {
-    Routes r = run_routes(s_rexp, s_rslot, Path::token(t), g_lo, K, cap, lane);
-    for (int64_t task = my0; task < t1; task += kWarps) {
+    Routes r = run_routes(s_rexp, s_rslot, a.g, g_lo, K, cap, lane);
+    int64_t task = my0;
+    for (; task < t1; task += kWarps) {
       const int64_t next = task + kWarps;
       const bool more = next < t1;
+      if (!more) pdl_allow_dependents();   // the next kernel may start launching
       cur = cur.next();
       typename Path::Raw an;
-      if (more) Path::load(p.d, cur, lane, an);
+      const bool staged = has1 && task == my0;   // the next task is the one in shared memory
+      if (more && !staged) Path::load(p.d, cur, lane, an);
       Path::store(p.d, lane, t, r);
       if (more) {
+        if (staged) {
+          // every lane waits for the copy (bounded); if any lane's wait ran
+          // out, the warp reads x from global memory instead
+          const bool in = mbar_wait_bounded(&s_xbar[warp], 0, global_timer_ns() + kDefaultTimeoutNs);
+          if (__all_sync(kFull, in)) {
+            stage_pending = false;
+            Path::load_staged(p.d, cur, lane, s_x2, an);
+          } else {
+            Path::load(p.d, cur, lane, an);
+          }
+        }
         Path::prep(an, lane, t);
         r = run_routes(s_rexp, s_rslot, cur.g, g_lo, K, cap, lane);
       }
     }
+  }
+  // A copy not seen to complete (a wait that ran out): wait for it again,
+  // bounded, so that none is left in flight when the block exits; report a
+  // copy that still has not landed.
+  if (stage_pending) {
+    const bool in = mbar_wait_bounded(&s_xbar[warp], 0, global_timer_ns() + kDefaultTimeoutNs);
+    if (!__all_sync(kFull, in) && lane == 0) report_status(p.d.hdr, MOE_ERR_TIMEOUT);
   }
 
   // One atomic per block carries its arrival and its errors, issued by the
@@ -307,7 +398,8 @@ plan_dispatch_kernel(FusedParams p) {
   }
 
   // 6. the plan outputs: slot_of and src_of of the tokens whose segment 0
-  //    is in this block; each owner's counts and offsets rows
+  //    is in this block; each owner's counts and offsets rows, from a count
+  //    of its experts' entries per rank over the whole table
   const int64_t gw0 = (t0 + p.tpr - 1) / p.tpr;
   const int64_t gw1 = (t1 + p.tpr - 1) / p.tpr;
   for (int i = tid; i < run; i += THREADS) {
@@ -318,6 +410,30 @@ plan_dispatch_kernel(FusedParams p) {
       if (e >= 0 && slot < cap) p.src_of[(int64_t)e * cap + slot] = q;
     }
   }
+  {
+    const int tk = p.T * K;      // entries per rank
+    auto visit = [&](int e, int r) {
+      const unsigned o = (unsigned)(e - own0);
+      if ((unsigned)e < (unsigned)E && o < (unsigned)p.owned) atomicAdd(&s_ocnt[o * R + r], 1);
+    };
+    const int4 *t4 = reinterpret_cast<const int4 *>(s_tab);
+    const int n4 = total >> 2;
+    for (int j = tid; j < n4; j += THREADS) {
+      const int4 w = t4[j];
+      const int q = 4 * j;
+      // q is a multiple of 4, so with tk >= 2 the 4 entries cross at most
+      // one rank boundary after q's own rank; tk = 1 divides each entry
+      const int r = q / tk;
+      const int nxt = (r + 1) * tk;
+      const bool one = tk >= 2;
+      visit(w.x, r);
+      visit(w.y, one ? r + (q + 1 >= nxt) : (q + 1) / tk);
+      visit(w.z, one ? r + (q + 2 >= nxt) : (q + 2) / tk);
+      visit(w.w, one ? r + (q + 3 >= nxt) : (q + 3) / tk);
+    }
+    for (int q = 4 * n4 + tid; q < total; q += THREADS) visit(s_tab[q], q / tk);
+  }
+  __syncthreads();
   for (int j = warp; j < p.owned; j += kWarps) {
     const int e = own0 + j;
     if (e >= E) break;
@@ -355,11 +471,24 @@ cudaError_t launch_fused(const FusedParams &p, cudaStream_t stream) {
                                          (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
   }
-  // An ordinary launch: as a programmatic dependent (waiting before its
-  // first read of the routes and x) it measured slower, 25.4 against 24.0 us
-  // for bf16 at DeepSeek-V3 decode.
-  kern<<<p.grid, THREADS, p.smem_bytes, stream>>>(p);
-  return cudaGetLastError();
+  // A programmatic dependent of the previous kernel: its blocks may be
+  // scheduled while that kernel drains (the previous kernels of this library
+  // let their dependents launch when their warps start their last task),
+  // and wait for it to complete before reading anything.  Measured at
+  // DeepSeek-V3 decode in graphs of back-to-back calls, with the other
+  // kernels' late trigger: fp8 16.6 -> 15.5 us, bf16 24.0 -> 23.3 us.
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -395,13 +524,17 @@ bool plan_dispatch_geometry(const moe_shape &s, FusedParams &p) {
   }
   const int64_t ntasks = N * tpr;
   const int64_t sms = device_sm_count() < kFusedMaxGrid ? device_sm_count() : kFusedMaxGrid;
-  const int64_t q = (ntasks + sms - 1) / sms;
-  const int grid = (int)((ntasks + q - 1) / q);
+  const int grid = (int)(ntasks < sms ? ntasks : sms);
+  const int64_t q = (ntasks + grid - 1) / grid;   // tasks of a block, at most
   const int owned = (s.num_experts + grid - 1) / grid;
   const int64_t max_run = (q / tpr + 2) * s.top_k;
   const size_t tab = ((size_t)(N * s.top_k) * 4 + 15) & ~(size_t)15;
-  const size_t smem = tab + (size_t)((s.num_experts + 15) & ~15) + 8 * (size_t)s.num_experts +
-                      4 * (size_t)owned * s.num_ranks + 8 * (size_t)max_run;
+  size_t smem = tab + (size_t)((s.num_experts + 15) & ~15) + 8 * (size_t)s.num_experts +
+                4 * (size_t)owned * s.num_ranks + 8 * (size_t)max_run;
+  // one whole task of x per warp, for the staged second tasks
+  p.task_elems = fp8 ? 2 * p.units * 128 : 256 * p.units;
+  p.stage_off = (smem + 15) & ~(size_t)15;
+  if (!fp8) smem = p.stage_off + (size_t)(kFusedBf16Threads / 32) * p.task_elems * 2;
   if (smem > kFusedMaxSmem) return false;
   p.R = s.num_ranks;
   p.T = s.tokens_per_rank;
