@@ -838,6 +838,10 @@ def run_gpu(args, wl):
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "peak_source": f"{peak_kind} hbm_gbs", "unit": UNIT, "frac": achieved / peak,
                 "traffic": recorded_traffic(dom_b, wl.name),
+                "traffic_counters": ("ncu, per launch: dram__bytes_read.sum plus the L2 write sectors "
+                                     "from the SMs (lts__t_sectors_op_write minus its die-to-die fabric "
+                                     "part, x 32 B); dram__bytes_write misses lines still dirty in the "
+                                     "write-back L2 when a replayed launch ends (profiles/dram_traffic.md)"),
                 "algorithmic_bytes": cb[dom_b]}
     calls_out = {}
     for c in timed:

@@ -49,11 +49,14 @@
 //      and error bits to one workspace word; the last block to arrive writes
 //      the status word (no block waits for another).  Issued by a warp with
 //      stores still to make, that contended atomic delayed it by ~0.8 us.
-//   7. After its tasks the block writes slot_of and src_of for the tokens
-//      whose first segment it holds (stores issued earlier would wait behind
-//      the x loads); then it counts its owned experts' entries per rank over
-//      the whole table and writes their counts and offsets rows.  Off the
-//      path to the first store, that scan overlaps the drain of the stores.
+//      The same warp writes slot_of and src_of for the tokens whose first
+//      segment the block holds (stores issued before the tasks would wait
+//      behind the x loads).
+//   7. The warps that run out of tasks claim 128-entry chunks of the table
+//      and count the owned experts' entries per rank; the warp that
+//      completes the last chunk writes the owners' counts and offsets rows.
+//      The block's slowest warp, which sets its end, mostly finds no chunk
+//      left.
 // Every block copies and scans all N*K routes, which pays only while the
 // table is small: the fused path is taken up to kFusedMaxEntries routed
 // entries (at Kimi-K2 decode, 32768 entries, two launches measured faster);
@@ -78,6 +81,9 @@ namespace moe {
 // them for bf16, which has nothing to quantise; a part for fp8.
 #ifndef MOE_FUSED_PLAN_WARPS
 #define MOE_FUSED_PLAN_WARPS 12
+#endif
+#ifndef MOE_FUSED_OWN_VEC
+#define MOE_FUSED_OWN_VEC 1
 #endif
 
 template <int U>
@@ -191,7 +197,7 @@ plan_dispatch_kernel(FusedParams p) {
   constexpr int kScanThreads = kPlanThreads - 32;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t s_bar;
-  __shared__ uint32_t s_err, s_fin, s_fail;
+  __shared__ uint32_t s_err, s_fin, s_fail, s_chunk, s_chunk_done;
   __shared__ __align__(8) uint64_t s_xbar[Path::kStage2 ? kWarps : 1];   // per warp: its staged second task
   const int E = p.d.E, K = p.d.K, R = p.R, cap = p.d.cap;
   const int total = p.d.N * K;
@@ -259,6 +265,8 @@ plan_dispatch_kernel(FusedParams p) {
     s_err = 0;
     s_fin = 0;
     s_fail = 0;
+    s_chunk = 0;
+    s_chunk_done = 0;
   }
   __syncthreads();   // also publishes the barrier's initialisation and the zeroed tables
 
@@ -389,71 +397,92 @@ plan_dispatch_kernel(FusedParams p) {
     if (!__all_sync(kFull, in) && lane == 0) report_status(p.d.hdr, MOE_ERR_TIMEOUT);
   }
 
-  // One atomic per block carries its arrival and its errors, issued by the
-  // block's first warp to run out of tasks, so that its round trip (all
-  // blocks add to one word) delays no warp that still has stores to issue.
-  if (lane == 0 && atomicAdd(&s_fin, 1u) == 0u) {
-    const uint32_t code = arrival_code(s_err);
-    finish_status(p.d.hdr, atomicAdd(&p.d.hdr->arrivals, code) + code);
+  // 6-7 are shared out among the warps that finish their tasks first, so
+  // that the block's slowest warp, which sets its end, does none of it: a
+  // share per thread (with a block barrier before the offsets rows) cost
+  // 1.1 us of the fp8 call at DeepSeek-V3 decode.
+  //
+  // 6. The block's first warp to run out of tasks carries its arrival and
+  //    errors in one atomic (all blocks add to one word, so its round trip
+  //    delays no warp that still has stores to issue), and writes slot_of
+  //    and src_of of the tokens whose segment 0 is in this block.
+  const unsigned first = __shfl_sync(kFull, lane == 0 ? atomicAdd(&s_fin, 1u) : 0u, 0);
+  if (first == 0u) {
+    if (lane == 0) {
+      const uint32_t code = arrival_code(s_err);
+      finish_status(p.d.hdr, atomicAdd(&p.d.hdr->arrivals, code) + code);
+    }
+    const int64_t gw0 = (t0 + p.tpr - 1) / p.tpr;
+    const int64_t gw1 = (t1 + p.tpr - 1) / p.tpr;
+    for (int i = lane; i < run; i += 32) {
+      const int64_t g = g_lo + i / K;
+      if (g >= gw0 && g < gw1) {
+        const int e = s_rexp[i], slot = s_rslot[i], q = lo_ent + i;
+        p.slot_of[q] = slot;
+        if (e >= 0 && slot < cap) p.src_of[(int64_t)e * cap + slot] = q;
+      }
+    }
   }
 
-  // 6. the plan outputs: slot_of and src_of of the tokens whose segment 0
-  //    is in this block; each owner's counts and offsets rows, from a count
-  //    of its experts' entries per rank over the whole table
-  const int64_t gw0 = (t0 + p.tpr - 1) / p.tpr;
-  const int64_t gw1 = (t1 + p.tpr - 1) / p.tpr;
-  for (int i = tid; i < run; i += THREADS) {
-    const int64_t g = g_lo + i / K;
-    if (g >= gw0 && g < gw1) {
-      const int e = s_rexp[i], slot = s_rslot[i], q = lo_ent + i;
-      p.slot_of[q] = slot;
-      if (e >= 0 && slot < cap) p.src_of[(int64_t)e * cap + slot] = q;
-    }
-  }
-  {
-    const int tk = p.T * K;      // entries per rank
-    auto visit = [&](int e, int r) {
-      const unsigned o = (unsigned)(e - own0);
-      if ((unsigned)e < (unsigned)E && o < (unsigned)p.owned) atomicAdd(&s_ocnt[o * R + r], 1);
-    };
-    const int4 *t4 = reinterpret_cast<const int4 *>(s_tab);
-    const int n4 = total >> 2;
-    for (int j = tid; j < n4; j += THREADS) {
-      const int4 w = t4[j];
-      const int q = 4 * j;
-      // q is a multiple of 4, so with tk >= 2 the 4 entries cross at most
-      // one rank boundary after q's own rank; tk = 1 divides each entry
-      const int r = q / tk;
-      const int nxt = (r + 1) * tk;
-      const bool one = tk >= 2;
-      visit(w.x, r);
-      visit(w.y, one ? r + (q + 1 >= nxt) : (q + 1) / tk);
-      visit(w.z, one ? r + (q + 2 >= nxt) : (q + 2) / tk);
-      visit(w.w, one ? r + (q + 3 >= nxt) : (q + 3) / tk);
-    }
-    for (int q = 4 * n4 + tid; q < total; q += THREADS) visit(s_tab[q], q / tk);
-  }
-  __syncthreads();
-  for (int j = warp; j < p.owned; j += kWarps) {
-    const int e = own0 + j;
-    if (e >= E) break;
-    int32_t *row = p.expert_rank_offsets + (int64_t)e * (R + 1);
-    int sum = 0;
-    for (int r0 = 0; r0 < R; r0 += 32) {
-      const int r = r0 + lane;
-      const int c = r < R ? s_ocnt[j * R + r] : 0;
-      int incl = c;
+  // 7. The owned experts' entries per rank, over the whole table, in
+  //    chunks (128 entries per 16-byte load of a lane) that the warps claim as they run out of
+  //    tasks; the warp that completes the last chunk writes the owners'
+  //    counts and offsets rows.
+  const int tk = p.T * K;      // entries per rank
+  constexpr int kChunk = 32 * 4 * MOE_FUSED_OWN_VEC;   // entries per chunk: MOE_FUSED_OWN_VEC 16-byte loads per lane
+  const int nchunks = (total + kChunk - 1) / kChunk;
+  for (;;) {
+    const unsigned c = __shfl_sync(kFull, lane == 0 ? atomicAdd(&s_chunk, 1u) : 0u, 0);
+    if (c >= (unsigned)nchunks) break;
+    int ev[MOE_FUSED_OWN_VEC][4];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(kFull, incl, off);
-        if (lane >= off) incl += v;
+    for (int v = 0; v < MOE_FUSED_OWN_VEC; ++v) {
+      const int q0 = (int)c * kChunk + v * 128 + 4 * lane;   // this lane's 4 entries
+      if (q0 + 4 <= total) {
+        const int4 w = *reinterpret_cast<const int4 *>(s_tab + q0);
+        ev[v][0] = w.x; ev[v][1] = w.y; ev[v][2] = w.z; ev[v][3] = w.w;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ev[v][u] = q0 + u < total ? s_tab[q0 + u] : -1;
       }
-      if (r < R) row[r] = sum + incl - c;
-      sum += __shfl_sync(kFull, incl, 31);
     }
-    if (lane == 0) {
-      row[R] = sum;
-      p.expert_num_tokens[e] = sum;
+#pragma unroll
+    for (int v = 0; v < MOE_FUSED_OWN_VEC; ++v) {
+      const int q0 = (int)c * kChunk + v * 128 + 4 * lane;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = ev[v][u];
+        const unsigned o = (unsigned)(e - own0);
+        if ((unsigned)e < (unsigned)E && o < (unsigned)p.owned) atomicAdd(&s_ocnt[o * R + (q0 + u) / tk], 1);
+      }
+    }
+    __threadfence_block();   // this chunk's counts before its completion
+    __syncwarp();
+    const unsigned done = __shfl_sync(kFull, lane == 0 ? atomicAdd(&s_chunk_done, 1u) + 1u : 0u, 0);
+    if (done == (unsigned)nchunks) {
+      __threadfence_block();   // every chunk's counts are in
+      for (int j = 0; j < p.owned; ++j) {
+        const int e = own0 + j;
+        if (e >= E) break;
+        int32_t *row = p.expert_rank_offsets + (int64_t)e * (R + 1);
+        int sum = 0;
+        for (int r0 = 0; r0 < R; r0 += 32) {
+          const int r = r0 + lane;
+          const int cnt = r < R ? atomicAdd(&s_ocnt[j * R + r], 0) : 0;
+          int incl = cnt;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += v;
+          }
+          if (r < R) row[r] = sum + incl - cnt;
+          sum += __shfl_sync(kFull, incl, 31);
+        }
+        if (lane == 0) {
+          row[R] = sum;
+          p.expert_num_tokens[e] = sum;
+        }
+      }
     }
   }
 }
