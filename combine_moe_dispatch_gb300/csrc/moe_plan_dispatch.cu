@@ -431,6 +431,7 @@ plan_dispatch_kernel(FusedParams p) {
   const int tk = p.T * K;      // entries per rank
   constexpr int kChunk = 32 * 4 * MOE_FUSED_OWN_VEC;   // entries per chunk: MOE_FUSED_OWN_VEC 16-byte loads per lane
   const int nchunks = (total + kChunk - 1) / kChunk;
+  unsigned mine = 0;   // chunks this warp counted
   for (;;) {
     const unsigned c = __shfl_sync(kFull, lane == 0 ? atomicAdd(&s_chunk, 1u) : 0u, 0);
     if (c >= (unsigned)nchunks) break;
@@ -456,33 +457,36 @@ plan_dispatch_kernel(FusedParams p) {
         if ((unsigned)e < (unsigned)E && o < (unsigned)p.owned) atomicAdd(&s_ocnt[o * R + (q0 + u) / tk], 1);
       }
     }
-    __threadfence_block();   // this chunk's counts before its completion
-    __syncwarp();
-    const unsigned done = __shfl_sync(kFull, lane == 0 ? atomicAdd(&s_chunk_done, 1u) + 1u : 0u, 0);
-    if (done == (unsigned)nchunks) {
-      __threadfence_block();   // every chunk's counts are in
-      for (int j = 0; j < p.owned; ++j) {
-        const int e = own0 + j;
-        if (e >= E) break;
-        int32_t *row = p.expert_rank_offsets + (int64_t)e * (R + 1);
-        int sum = 0;
-        for (int r0 = 0; r0 < R; r0 += 32) {
-          const int r = r0 + lane;
-          const int cnt = r < R ? atomicAdd(&s_ocnt[j * R + r], 0) : 0;
-          int incl = cnt;
+    ++mine;
+  }
+  if (mine == 0u) return;
+  // One fence per warp: its counts are in before its chunks are reported
+  // done.  The warp whose report completes the last chunk has every count.
+  __threadfence_block();
+  __syncwarp();
+  const unsigned done = __shfl_sync(kFull, lane == 0 ? atomicAdd(&s_chunk_done, mine) + mine : 0u, 0);
+  if (done != (unsigned)nchunks) return;
+  __threadfence_block();
+  for (int j = 0; j < p.owned; ++j) {
+    const int e = own0 + j;
+    if (e >= E) break;
+    int32_t *row = p.expert_rank_offsets + (int64_t)e * (R + 1);
+    int sum = 0;
+    for (int r0 = 0; r0 < R; r0 += 32) {
+      const int r = r0 + lane;
+      const int cnt = r < R ? atomicAdd(&s_ocnt[j * R + r], 0) : 0;
+      int incl = cnt;
 #pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(kFull, incl, off);
-            if (lane >= off) incl += v;
-          }
-          if (r < R) row[r] = sum + incl - cnt;
-          sum += __shfl_sync(kFull, incl, 31);
-        }
-        if (lane == 0) {
-          row[R] = sum;
-          p.expert_num_tokens[e] = sum;
-        }
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += v;
       }
+      if (r < R) row[r] = sum + incl - cnt;
+      sum += __shfl_sync(kFull, incl, 31);
+    }
+    if (lane == 0) {
+      row[R] = sum;
+      p.expert_num_tokens[e] = sum;
     }
   }
 }
