@@ -62,7 +62,8 @@
 // entries (at Kimi-K2 decode, 32768 entries, two launches measured faster);
 // larger shapes run moe_plan and moe_dispatch as two launches.  One block per
 // SM, as many threads as the dispatch kernels keep resident per SM (768 for
-// fp8, 1024 for bf16).
+// fp8, or 1024 when that would give a warp more than two tasks; 1024 for
+// bf16).
 //
 // Data errors: the status word ends up exactly as moe_plan would set it, and
 // the plan outputs are those of moe_plan.  But no block waits for the
@@ -494,6 +495,10 @@ plan_dispatch_kernel(FusedParams p) {
 namespace {
 
 constexpr int kFusedFp8Threads = 768;    // 3 x 256: the fp8 dispatch's residency per SM
+// fp8 with more than two tasks per warp at 768 threads: 1024 threads (64
+// registers, 4 bytes of spill).  Measured: Mixtral-shaped layer (108 tasks
+// per block) 16.5 -> 16.0 us; DeepSeek-V3 decode (48) 15.9 against 15.95 us.
+constexpr int kFusedFp8ThreadsWide = 1024;
 constexpr int kFusedBf16Threads = 1024;  // 4 x 256: the bf16 dispatch's residency per SM
 
 template <class Path, int THREADS>
@@ -589,10 +594,14 @@ cudaError_t launch_plan_dispatch(const FusedParams &p, bool fp8, cudaStream_t st
   // tasks per row (p.tpr) come from it, and the kernel indexes the blocks
   // of a task with its own size.
   if (fp8) {
+    const bool wide = p.q_tasks > 2 * (kFusedFp8Threads / 32);
     switch (p.units) {
-      case 1: return launch_fused<Fp8Path<1>, kFusedFp8Threads>(p, stream);
-      case 2: return launch_fused<Fp8Path<2>, kFusedFp8Threads>(p, stream);
-      case 4: return launch_fused<Fp8Path<4>, kFusedFp8Threads>(p, stream);
+      case 1: return wide ? launch_fused<Fp8Path<1>, kFusedFp8ThreadsWide>(p, stream)
+                          : launch_fused<Fp8Path<1>, kFusedFp8Threads>(p, stream);
+      case 2: return wide ? launch_fused<Fp8Path<2>, kFusedFp8ThreadsWide>(p, stream)
+                          : launch_fused<Fp8Path<2>, kFusedFp8Threads>(p, stream);
+      case 4: return wide ? launch_fused<Fp8Path<4>, kFusedFp8ThreadsWide>(p, stream)
+                          : launch_fused<Fp8Path<4>, kFusedFp8Threads>(p, stream);
       default: return cudaErrorInvalidValue;
     }
   }
