@@ -83,9 +83,6 @@ namespace moe {
 #ifndef MOE_FUSED_PLAN_WARPS
 #define MOE_FUSED_PLAN_WARPS 12
 #endif
-#ifndef MOE_FUSED_OWN_VEC
-#define MOE_FUSED_OWN_VEC 1
-#endif
 
 template <int U>
 struct Bf16Path {
@@ -426,37 +423,33 @@ plan_dispatch_kernel(FusedParams p) {
   }
 
   // 7. The owned experts' entries per rank, over the whole table, in
-  //    chunks (128 entries per 16-byte load of a lane) that the warps claim as they run out of
+  //    128-entry chunks (4 per lane) that the warps claim as they run out of
   //    tasks; the warp that completes the last chunk writes the owners'
-  //    counts and offsets rows.
+  //    counts and offsets rows.  Few entries belong to the owned experts,
+  //    so an entry costs a compare; only those take an atomic.
   const int tk = p.T * K;      // entries per rank
-  constexpr int kChunk = 32 * 4 * MOE_FUSED_OWN_VEC;   // entries per chunk: MOE_FUSED_OWN_VEC 16-byte loads per lane
-  const int nchunks = (total + kChunk - 1) / kChunk;
+  const int nchunks = (total + 127) / 128;
   unsigned mine = 0;   // chunks this warp counted
   for (;;) {
     const unsigned c = __shfl_sync(kFull, lane == 0 ? atomicAdd(&s_chunk, 1u) : 0u, 0);
     if (c >= (unsigned)nchunks) break;
-    int ev[MOE_FUSED_OWN_VEC][4];
+    const int q0 = (int)c * 128 + 4 * lane;   // this lane's 4 entries
+    int ev[4];
+    if (q0 + 4 <= total) {
+      const int4 w = *reinterpret_cast<const int4 *>(s_tab + q0);
+      ev[0] = w.x;
+      ev[1] = w.y;
+      ev[2] = w.z;
+      ev[3] = w.w;
+    } else {
 #pragma unroll
-    for (int v = 0; v < MOE_FUSED_OWN_VEC; ++v) {
-      const int q0 = (int)c * kChunk + v * 128 + 4 * lane;   // this lane's 4 entries
-      if (q0 + 4 <= total) {
-        const int4 w = *reinterpret_cast<const int4 *>(s_tab + q0);
-        ev[v][0] = w.x; ev[v][1] = w.y; ev[v][2] = w.z; ev[v][3] = w.w;
-      } else {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) ev[v][u] = q0 + u < total ? s_tab[q0 + u] : -1;
-      }
+      for (int u = 0; u < 4; ++u) ev[u] = q0 + u < total ? s_tab[q0 + u] : -1;
     }
 #pragma unroll
-    for (int v = 0; v < MOE_FUSED_OWN_VEC; ++v) {
-      const int q0 = (int)c * kChunk + v * 128 + 4 * lane;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = ev[v][u];
-        const unsigned o = (unsigned)(e - own0);
-        if ((unsigned)e < (unsigned)E && o < (unsigned)p.owned) atomicAdd(&s_ocnt[o * R + (q0 + u) / tk], 1);
-      }
+    for (int u = 0; u < 4; ++u) {
+      const unsigned o = (unsigned)(ev[u] - own0);
+      if ((unsigned)ev[u] < (unsigned)E && o < (unsigned)p.owned)
+        atomicAdd(&s_ocnt[o * R + (q0 + u) / tk], 1);
     }
     ++mine;
   }
