@@ -388,9 +388,9 @@ class BufferSet:
         self.x = torch.from_numpy(d["x"].view(np.int16)).to(device).view(torch.bfloat16)
         self.w = torch.from_numpy(d["topk_weights"]).to(device)
         self.b16 = moe.Buffers(self.sh16, device=device, expert_y=False,
-                               expert_x=any(c.endswith("dispatch_bf16") for c in calls))
+                               expert_x=any(base_call(c).endswith("dispatch_bf16") for c in calls))
         self.b8 = (moe.Buffers(self.sh8, device=device, expert_y=False, expert_x=True)
-                   if any(c.endswith("dispatch_fp8") for c in calls) else None)
+                   if any(base_call(c).endswith("dispatch_fp8") for c in calls) else None)
         self.ey = inputs.expert_outputs_device(E, cap, H, seed, device=device)
         self.moe = moe
 
@@ -417,9 +417,9 @@ class BufferSet:
     @staticmethod
     def nbytes(wl, cap, calls):
         per = wl.N * wl.H * 2 * 2 + wl.E * cap * wl.H * 2           # x, y, expert_y
-        if any(c.endswith("dispatch_bf16") for c in calls):
+        if any(base_call(c).endswith("dispatch_bf16") for c in calls):
             per += wl.E * cap * wl.H * 2
-        if any(c.endswith("dispatch_fp8") for c in calls):
+        if any(base_call(c).endswith("dispatch_fp8") for c in calls):
             per += wl.E * cap * wl.H + wl.E * cap * (wl.H // 128) * 4
         return per
 

@@ -72,14 +72,15 @@ class Result(dict):
 def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
              payloads=("bf16", "fp8"), expert_y="host", combine_tokens=None, seed=0,
              expect_status=None, masked=False, num_tokens=None, fused=False,
-             idx_device=None) -> Result:
+             idx_device=None, early_x=False) -> Result:
     """Run plan/dispatch/combine on the GPU and compare with the oracle.
     ``expert_y``: "host" (seeded numpy, full [E,cap,H]) or "device" (seeded
     torch generator on the GPU, for shapes too large for the host).
     ``combine_tokens``: token ids the oracle recomputes (None = all).
     ``fused``: plan and dispatch through moe_plan_dispatch.
     ``idx_device``: the device copy of ``idx`` to pass (e.g. a view that is
-    not 16-byte aligned); default a fresh tensor."""
+    not 16-byte aligned); default a fresh tensor.
+    ``early_x``: dispatch through moe_dispatch_ex(MOE_DISPATCH_EARLY_X)."""
     N = R * T
     res = Result(mismatch={}, max_ulp=0, not_bit_exact=0)
     if masked:
@@ -122,7 +123,7 @@ def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
         if expect_status == moe.Status.BAD_EXPERT and fused:
             return res
         if expect_status == moe.Status.BAD_EXPERT:
-            buf.dispatch(x_d, idx_d)
+            buf.dispatch(x_d, idx_d, early_x=early_x)
             torch.cuda.synchronize()
             assert not rows_touched(buf.expert_x, E, cap).any(), "dispatch wrote after BAD_EXPERT"
             return res
@@ -135,7 +136,7 @@ def run_case(R, T, H, E, K, cap, idx: np.ndarray, x: np.ndarray, w: np.ndarray,
             n = min(int(cnt[e]), cap)
             assert np.array_equal(g_src[e, :n], src_o[e, :n]), f"src_of row {e}"
         if not fused:
-            buf.dispatch(x_d, idx_d)
+            buf.dispatch(x_d, idx_d, early_x=early_x)
         torch.cuda.synchronize()
         touched = rows_touched(buf.expert_x, E, cap)
         if expect_status == moe.Status.CAPACITY and fused:

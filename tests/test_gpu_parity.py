@@ -227,6 +227,22 @@ def test_workload_full_size(name):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("R,T,H,E,K,status", [
+    (2, 96, 512, 16, 4, "ok"), (3, 300, 1536, 64, 8, "ok"), (8, 128, 7168, 256, 8, "ok"),
+    (2, 64, 256, 8, 2, "capacity"), (2, 64, 256, 8, 2, "bad_expert")])
+def test_dispatch_early_x(R, T, H, E, K, status):
+    """moe_dispatch_ex with MOE_DISPATCH_EARLY_X right after moe_plan (the
+    order it is meant for): the same rows, bytes and scales as the oracle,
+    and nothing written after a failed plan."""
+    idx, x, w = _rand_case(91, R, T, H, E, K)
+    cap = R * T
+    if status == "capacity":
+        cap = int(np.bincount(idx.ravel(), minlength=E).max()) - 1
+    if status == "bad_expert":
+        idx[R * T // 2, 0] = E
+    gpu_check.run_case(R, T, H, E, K, cap, idx, x, w, ("bf16", "fp8"), early_x=True)
+
+
 def test_fp8_scales_offset_by_4_bytes():
     """A scale array 4 bytes past a 16-byte boundary: the scales must still
     land exactly (bulk copies need 16-byte alignment, so they are not used)."""
