@@ -50,12 +50,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int KG, int U, int MINB>
 __global__ void __launch_bounds__(kCombineThreads, MINB)
 combine_kernel(CombineParams p) {
-  __shared__ int32_t s_status;
-  pdl_wait_for_previous();
-  if (threadIdx.x == 0) s_status = read_status(p.hdr);
-  __syncthreads();
-  if (s_status != MOE_OK) return;
-
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kCombineThreads) >> 5;
@@ -63,19 +57,26 @@ combine_kernel(CombineParams p) {
   constexpr int cpt = 32 * U;        // chunks per task
   const int tpr = (cpr + cpt - 1) / cpt;
   const int64_t ntasks = (int64_t)p.N * tpr;
-
-  if (warp0 >= ntasks) return;
   TaskCursor cur(warp0, nwarps, tpr);
-  // The routing of a warp's next task is loaded while the current task's
-  // rows are read, so each task waits for one memory round trip (its rows),
-  // not two (its routing, then its rows).
+  // After the wait, thread 0 reads the status word while every warp's first
+  // routing loads are in flight (before, one round trip after the other:
+  // 22.1 -> 21.9 us at DeepSeek-V3 decode, 18.5 -> 18.1 us at the
+  // Mixtral-shaped layer).
+  __shared__ int32_t s_status;
+  pdl_wait_for_previous();
+  if (threadIdx.x == 0) s_status = read_status(p.hdr);
   int e_l = -1, s_l = -1;
   float w_l = 0.0f;
-  if (lane < p.K) {
+  if (warp0 < ntasks && lane < p.K) {
     e_l = __ldg(p.topk_idx + (int64_t)cur.g * p.K + lane);
     s_l = __ldg(p.slot_of + (int64_t)cur.g * p.K + lane);
     w_l = __ldg(p.topk_weights + (int64_t)cur.g * p.K + lane);
   }
+  __syncthreads();
+  if (s_status != MOE_OK || warp0 >= ntasks) return;
+  // The routing of a warp's next task is loaded while the current task's
+  // rows are read, so each task waits for one memory round trip (its rows),
+  // not two (its routing, then its rows).
   for (int64_t task = warp0; task < ntasks; task += nwarps) {
     const int64_t g = cur.g;
     const int seg = cur.seg;

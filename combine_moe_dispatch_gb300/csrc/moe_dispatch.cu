@@ -64,6 +64,18 @@ __device__ __forceinline__ bool wait_plan_ok(const WsHeader *hdr, int lane) {
   if (lane == 0) st = read_status(hdr);
   return __shfl_sync(0xFFFFFFFFu, st, 0) == MOE_OK;
 }
+// The same, with the warp's first routes loaded together with the status
+// word, so that the two loads are in flight at once (fp8 at DeepSeek-V3
+// decode, x read early: 12.55 -> 12.15 us; the bf16 kernel measured 0.7 us
+// slower with it and reads the routes after the status).
+__device__ __forceinline__ bool wait_plan_ok_routes(const DispatchParams &p, int64_t g, int lane,
+                                                    Routes &r) {
+  pdl_wait_for_previous();
+  int32_t st = 0;
+  if (lane == 0) st = read_status(p.hdr);
+  r = load_routes(p, g, lane);
+  return __shfl_sync(0xFFFFFFFFu, st, 0) == MOE_OK;
+}
 
 template <int U>
 __global__ void __launch_bounds__(kDispatchThreads)
@@ -130,8 +142,8 @@ dispatch_fp8_kernel(DispatchParams p) {
   fp8_load<P>(p, warp0 / tpr, (int)(warp0 % tpr), lane, a);
   Fp8Task<P> t;
   fp8_quantise<P>(a, lane, t);
-  if (!wait_plan_ok(p.hdr, lane)) return;
-  Routes r = load_routes(p, a.g, lane);
+  Routes r;
+  if (!wait_plan_ok_routes(p, a.g, lane, r)) return;
   for (int64_t task = warp0; task < ntasks; task += nwarps) {
     const int64_t next = task + nwarps;
     const bool more = next < ntasks;

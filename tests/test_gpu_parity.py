@@ -355,8 +355,9 @@ def test_combine_shared(R, T, H, E, K):
                                    (33, 7, 7), (300, 64, 1)])
 def test_router_topk(N, E, K):
     """moe_router_topk against the oracle: indices bit for bit (including
-    many exact ties), weights within 1 fp32 ulp (the two sides' fp64 exp may
-    differ in the last bit); then the router's output through moe_plan."""
+    many exact ties), weights within 1 fp32 ulp (the kernel computes them in
+    float-float, the oracle in fp64: the two round the same value to
+    neighbouring floats at most); then the router's output through moe_plan."""
     import combine_moe_dispatch_gb300 as moe
     import oracle
     rng = np.random.default_rng(N + E + K)
@@ -376,6 +377,28 @@ def test_router_topk(N, E, K):
     st, cnt, off, slot, src = oracle.plan(1, N, E, K, N, idx_o)
     assert moe.read_status(b.workspace) == moe.Status.OK
     assert np.array_equal(b.slot_of.cpu().numpy(), slot)
+
+
+def test_router_topk_unaligned_logits():
+    """Logits that start 4 bytes past a 16-byte boundary (the kernel's
+    16-byte loads are skipped for them): the same result as the oracle."""
+    import combine_moe_dispatch_gb300 as moe
+    import oracle
+    N, E, K = 257, 256, 8
+    rng = np.random.default_rng(7)
+    lg = rng.standard_normal((N, E)).astype(np.float32)
+    flat = torch.empty(N * E + 4, dtype=torch.float32, device="cuda")
+    flat[1:1 + N * E] = torch.from_numpy(lg.ravel()).cuda()
+    lg_d = flat[1:1 + N * E].view(N, E)
+    assert lg_d.data_ptr() % 16 == 4
+    shape = moe.make_shape(1, N, 256, E, K, N)
+    idx_d = torch.empty((N, K), dtype=torch.int32, device="cuda")
+    w_d = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    moe.router_topk(shape, lg_d, idx_d, w_d)
+    idx_o, w_o = oracle.router_topk(lg, K)
+    assert np.array_equal(idx_d.cpu().numpy(), idx_o)
+    d = np.abs(w_d.cpu().numpy().view(np.int32).astype(np.int64) - w_o.view(np.int32).astype(np.int64))
+    assert d.max() <= 1
 
 
 TSCALE = [
