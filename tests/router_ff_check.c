@@ -7,26 +7,29 @@
    round-to-nearest (build with -ffp-contract=off so that no product and sum
    are fused behind the code's back):
      d = l_k - l_max as a float-float (TwoSum, exact);
-     e^d for d >= -64: n = rint(d_h / ln 2), r = d - n (L1 + L2 + L3) as a
-       float-float, e^r = 1 + r (1 + r (1/2 + r (1/6 + r Q(r)))) with Q (the
-       terms r^4/4! .. r^9/9! over r^3) in binary32, the product r Q exact,
-       and the outer steps in float-float, times 2^n; below -64 (and for
-       -inf) in binary64;
+     e^d for d >= -64: N = rint(32 d_h / ln 2) = 32 m + j, r = d - N (L1 +
+       L2 + L3) as a float-float (L1 + L2 + L3 = ln 2 / 32), e^r = 1 + r +
+       r^2 (1/2 + r/6 + r^2/24 + r^3/120) with the part after r in binary32
+       and the two additions in float-float, times the float-float 2^(j/32)
+       and 2^m; below -64 (and for -inf) in binary64;
      the sum of the K exponentials by a butterfly of float-float additions;
-     w = RN(q + RN(rem / S_h)), q = RN(e_h / S_h), rem = e - q S.
+     w = RN(q + RN(rem y)), y ~ 1 / S_h, q = RN(e_h y), rem = e - q S.
 
-   Usage: router_ff_check STEP ROWS [full|noL2|f32sum]
+   Usage: router_ff_check STEP ROWS [full|noL2|f32sum|rcpU]
      exp: every STEP-th binary32 d in [-64, 0] (bit patterns of -0 .. -64),
        plus ROWS * 8 differences of random logit pairs (non-zero low parts);
        reports the largest relative error of e_h + e_l against exp() in
-       binary64, as a power of two (about 2^-34; the test requires below
-       2^-33.5).
+       binary64, as a power of two (about 2^-36; the test requires below
+       2^-35).
      softmax: ROWS random rows of K = 1..32 logits (N(0, s), s in {0.5, 1, 3,
        10}, some rounded to integers for exact ties), the weights against
        RN32 of the binary64 softmax; counts weights one ulp apart (the test
        allows 0.1% of them) and more than one ulp apart (must be none).
+     "rcpU" (U = -2 .. 2) moves y = RN(1/S_h) by U ulps: the kernel takes y
+       from the hardware's approximate reciprocal, and the corrected
+       quotient must come out the same within these bounds for any such y.
      Controls, which must fail, so that the check is seen to detect a wrong
-     result: "noL2" reduces by n L1 alone; "f32sum" adds the exponentials'
+     result: "noL2" reduces by N L1 alone; "f32sum" adds the exponentials'
      high parts in binary32.
    Prints "exp_cases N exp_err_log2 X ulp1 A ulp2plus B rows R" and exits 0. */
 #include <math.h>
@@ -39,7 +42,7 @@ typedef struct {
   float h, l;
 } ff;
 
-static int mode_nol2 = 0, mode_f32sum = 0;
+static int mode_nol2 = 0, mode_f32sum = 0, rcp_ulps = 0;
 
 static ff two_sum(float a, float b) {
   const float s = a + b;
@@ -63,35 +66,42 @@ static ff ff_mul(ff a, ff b) {
   e = fmaf(a.h, b.l, fmaf(a.l, b.h, e));
   return fast_two_sum(p, e);
 }
-static ff ff_horner(float c, ff r, ff t) {
-  ff cc = {c, 0.0f};
-  return ff_add(cc, ff_mul(r, t));
-}
+/* 2^(j/32) as float-float pairs (hi, lo), the kernel's table. */
+static const float exp2_32[64] = {
+    0x1p+0f, 0x0p+0f, 0x1.059b0ep+0f, -0x1.9d4f52p-25f, 0x1.0b5586p+0f, 0x1.9f3122p-25f,
+    0x1.11301ep+0f, -0x1.fdb496p-25f, 0x1.172b84p+0f, -0x1.c15742p-27f, 0x1.1d4874p+0f, -0x1.d2e8cap-25f,
+    0x1.2387a6p+0f, 0x1.ceac48p-25f, 0x1.29e9e0p+0f, -0x1.5c0424p-25f, 0x1.306fe0p+0f, 0x1.4636e2p-25f,
+    0x1.371a74p+0f, -0x1.18aac6p-25f, 0x1.3dea64p+0f, 0x1.824684p-25f, 0x1.44e086p+0f, 0x1.8624b4p-30f,
+    0x1.4bfdaep+0f, -0x1.593abcp-25f, 0x1.5342b6p+0f, -0x1.2c5610p-25f, 0x1.5ab07ep+0f, -0x1.5bd5ecp-27f,
+    0x1.6247ecp+0f, -0x1.f8b550p-25f, 0x1.6a09e6p+0f, 0x1.9fcef4p-26f, 0x1.71f75ep+0f, 0x1.1d8beep-25f,
+    0x1.7a1148p+0f, -0x1.829fd0p-25f, 0x1.82589ap+0f, -0x1.accc7cp-26f, 0x1.8ace54p+0f, 0x1.15506ep-27f,
+    0x1.93737cp+0f, -0x1.e64744p-25f, 0x1.9c4918p+0f, 0x1.51f848p-27f, 0x1.a5503cp+0f, -0x1.b83b54p-25f,
+    0x1.ae89fap+0f, -0x1.a94b14p-26f, 0x1.b7f770p+0f, -0x1.a09438p-25f, 0x1.c199bep+0f, -0x1.3d56b2p-27f,
+    0x1.cb720ep+0f, -0x1.8837ccp-27f, 0x1.d5818ep+0f, -0x1.822dbcp-27f, 0x1.dfc974p+0f, -0x1.908c94p-25f,
+    0x1.ea4afap+0f, 0x1.52486cp-27f, 0x1.f50766p+0f, -0x1.246eb0p-26f};
 
 static ff ff_exp_neg(float dh, float dl) {
-  const float kInvLn2 = 0x1.715476p+0f;
-  const float kL1 = 0x1.62e4p-1f, kL2 = 0x1.7f7d1cp-20f, kL3 = 0x1.ef357ap-45f;
-  const float n = rintf(dh * kInvLn2);
+  const float kInv = 0x1.715476p+5f;
+  const float kL1 = 0x1.62ep-6f, kL2 = 0x1.0bfbe8p-20f, kL3 = 0x1.cf79acp-45f;
+  const float n = rintf(dh * kInv);
+  const int ni = (int)n;
+  const int j = ni & 31, m = ni >> 5;
+  const float th = exp2_32[2 * j], tl = exp2_32[2 * j + 1];
   const float r1 = dh - n * kL1;
   float p2 = n * kL2, p2e = fmaf(n, kL2, -p2), l3 = n * kL3;
   if (mode_nol2) p2 = p2e = l3 = 0.0f;
   const ff s = two_sum(r1, -p2);
   const float low = ((s.l - p2e) + dl) - l3;
   const ff r = fast_two_sum(s.h, low);
-  float q = 0x1.71de3ap-19f;
-  q = fmaf(q, r.h, 0x1.a01a02p-16f);
-  q = fmaf(q, r.h, 0x1.a01a02p-13f);
-  q = fmaf(q, r.h, 0x1.6c16c2p-10f);
-  q = fmaf(q, r.h, 0x1.111112p-7f);
-  q = fmaf(q, r.h, 0x1.555556p-5f);
-  const float rqh = r.h * q;
-  ff c6 = {0x1.555556p-3f, -0x1.555556p-28f}, rq = {rqh, fmaf(r.l, q, fmaf(r.h, q, -rqh))};
-  ff t = ff_add(c6, rq);
-  t = ff_horner(0.5f, r, t);
-  t = ff_horner(1.0f, r, t);
-  t = ff_horner(1.0f, r, t);
-  const float two_n = ldexpf(1.0f, (int)n);
-  ff out = {t.h * two_n, t.l * two_n};
+  float q = fmaf(r.h, 0x1.111112p-7f, 0x1.555556p-5f);
+  q = fmaf(q, r.h, 0x1.555556p-3f);
+  q = fmaf(q, r.h, 0.5f);
+  const float pr = (r.h * r.h) * q;
+  ff one = {1.0f, 0.0f}, prf = {pr, 0.0f}, tt = {th, tl};
+  const ff t = ff_add(one, ff_add(r, prf));
+  const ff u = ff_mul(t, tt);
+  const float two_m = ldexpf(1.0f, m);
+  ff out = {u.h * two_m, u.l * two_m};
   return out;
 }
 
@@ -130,11 +140,14 @@ static void ff_softmax(int K, const float *v, float *w) {
   for (int k = 0; k < K; ++k) {
     const ff S = s[k];
     if (!slow[k]) {
-      const float q = e[k].h / S.h;
+      float y = 1.0f / S.h;
+      for (int u = 0; u < rcp_ulps; ++u) y = nextafterf(y, INFINITY);
+      for (int u = 0; u > rcp_ulps; --u) y = nextafterf(y, 0.0f);
+      const float q = e[k].h * y;
       const float pr = q * S.h;
       const float pe = fmaf(q, S.h, -pr);
       const float rem = ((e[k].h - pr) - pe) + (e[k].l - q * S.l);
-      w[k] = q + rem / S.h;
+      w[k] = q + rem * y;
     } else {
       w[k] = (float)(z[k] / ((double)S.h + (double)S.l));
     }
@@ -182,6 +195,7 @@ int main(int argc, char **argv) {
   if (argc > 3) {
     mode_nol2 = strcmp(argv[3], "noL2") == 0;
     mode_f32sum = strcmp(argv[3], "f32sum") == 0;
+    if (strncmp(argv[3], "rcp", 3) == 0) rcp_ulps = atoi(argv[3] + 3);
   }
   double worst = 0.0;
   long cases = 0;

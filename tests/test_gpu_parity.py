@@ -352,12 +352,14 @@ def test_combine_shared(R, T, H, E, K):
 
 
 @pytest.mark.parametrize("N,E,K", [(64, 8, 2), (1024, 256, 8), (4096, 384, 8), (500, 1024, 32),
-                                   (33, 7, 7), (300, 64, 1)])
+                                   (33, 7, 7), (300, 64, 1), (5000, 256, 8), (3000, 8, 2)])
 def test_router_topk(N, E, K):
     """moe_router_topk against the oracle: indices bit for bit (including
     many exact ties), weights within 1 fp32 ulp (the kernel computes them in
     float-float, the oracle in fp64: the two round the same value to
-    neighbouring floats at most); then the router's output through moe_plan."""
+    neighbouring floats at most); then the router's output through moe_plan.
+    Up to one token per warp of one block per SM the kernel keeps two
+    candidates per lane; the larger N here take the one-candidate variant."""
     import combine_moe_dispatch_gb300 as moe
     import oracle
     rng = np.random.default_rng(N + E + K)
