@@ -278,7 +278,10 @@ moe_status moe_combine_shared(const moe_shape *shape, const void *expert_y,
  * sort that tracks indices; sparse kernels consume the top-K indices and
  * scores directly).  Per token: the K largest logits in descending order,
  * ties to the lower expert index; weights = softmax over those K logits,
- * exp(l_k - l_max) / sum computed in fp64, rounded once to fp32.
+ * exp(l_k - l_max) / sum, rounded once to fp32.  The weights are computed in
+ * float-float arithmetic (pairs of fp32 values), within about 2^-36 of the
+ * exact value before that rounding: each is the correctly rounded weight or
+ * a neighbouring fp32 value (1 ulp).  The indices are exact.
  * In:   logits [N, E] fp32 (4-byte aligned).
  * Out:  topk_idx [N, K] int32, topk_weights [N, K] fp32.
  * Limits: K <= E <= 1024 (else UNSUPPORTED).  NaN logits: unspecified.
