@@ -381,6 +381,37 @@ def test_router_topk(N, E, K):
     assert np.array_equal(b.slot_of.cpu().numpy(), slot)
 
 
+def test_router_topk_wide_spread():
+    """Logit differences on both sides of -64, where the kernel leaves the
+    float-float exponential for fp64 (weights down to subnormal and zero),
+    and rows whose chosen logits are all equal: the same indices as the
+    oracle and weights within 1 ulp."""
+    import combine_moe_dispatch_gb300 as moe
+    import oracle
+    E, K = 256, 8
+    rng = np.random.default_rng(11)
+    offsets = np.array([0.0, -10.0, -63.9, -64.0, -64.1, -80.0, -100.0, -150.0], np.float32)
+    rows = []
+    for t in range(64):
+        lg = (rng.standard_normal(E) * 0.01 - 400.0).astype(np.float32)
+        top = rng.choice(E, size=K, replace=False)
+        lg[top] = np.float32(rng.standard_normal() * 3) + offsets * (1.0 + 0.01 * (t % 5))
+        rows.append(lg)
+    rows.append(np.full(E, 1.5, np.float32))               # every logit equal
+    rows.append(np.where(np.arange(E) % 2 == 0, -np.inf, 0.0).astype(np.float32))
+    lg = np.stack(rows)
+    N = lg.shape[0]
+    shape = moe.make_shape(1, N, 256, E, K, N)
+    idx_d = torch.empty((N, K), dtype=torch.int32, device="cuda")
+    w_d = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    moe.router_topk(shape, gpu_check.dev(lg), idx_d, w_d)
+    idx_o, w_o = oracle.router_topk(lg, K)
+    assert np.array_equal(idx_d.cpu().numpy(), idx_o)
+    d = np.abs(w_d.cpu().numpy().view(np.int32).astype(np.int64) - w_o.view(np.int32).astype(np.int64))
+    assert d.max() <= 1, f"router weights differ by {d.max()} ulp"
+    assert (w_o < np.float32(1.2e-38)).any() and (w_o == 0).any()   # subnormal and zero weights occur
+
+
 def test_router_topk_unaligned_logits():
     """Logits that start 4 bytes past a 16-byte boundary (the kernel's
     16-byte loads are skipped for them): the same result as the oracle."""
