@@ -157,7 +157,7 @@ class Oracle:
         r = _c(row_bits, np.uint16)
         H = r.shape[0]
         q = np.empty(H, np.uint8)
-        sc = np.empty(H // 128, np.float32)
+        sc = np.empty((H + 127) // 128, np.float32)
         self.lib.oracle_quant_row_e4m3(H, _ptr(r), _ptr(q), _ptr(sc))
         return q, sc
 
@@ -170,7 +170,7 @@ class Oracle:
         if out is None:
             out = np.zeros((E, cap, H), np.uint8)
         if out_scale is None:
-            out_scale = np.zeros((E, cap, H // 128), np.float32)
+            out_scale = np.zeros((E, cap, (H + 127) // 128), np.float32)
         self.lib.oracle_dispatch_fp8(N, H, E, idx.shape[1], cap, _ptr(x), _ptr(idx),
                                      _ptr(slot), _ptr(out), _ptr(out_scale))
         return out, out_scale

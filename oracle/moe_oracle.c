@@ -256,6 +256,9 @@ void oracle_dispatch_bf16(int N, int H, int E, int K, int cap,
  * absolute value of the block.
  *
  * Readings taken (the pages fix only "absmax per 128 elements" and fp8):
+ *   blocks  = ceil_div(H, 128); the last block holds the H % 128 elements
+ *             left over when H is not a multiple of 128 (the scale shape
+ *             M x ceil_div(K, 128) above)
  *   amax  = max |x_i| over the block (exact in fp32)
  *   scale = amax / 448   (IEEE binary32 division; 448 = largest E4M3)
  *   q_i   = e4m3(x_i / scale)   (binary32 division, then RNE + saturate)
@@ -263,15 +266,17 @@ void oracle_dispatch_bf16(int N, int H, int E, int K, int cap,
  */
 void oracle_quant_row_e4m3(int H, const uint16_t *row, uint8_t *q,
                            float *scale) {
-  for (int b = 0; b < H / 128; ++b) {
+  const int nb = (H + 127) / 128;   /* ceil_div(H, 128): the last block may be short */
+  for (int b = 0; b < nb; ++b) {
+    const int end = (b + 1) * 128 < H ? (b + 1) * 128 : H;
     float amax = 0.0f;
-    for (int i = b * 128; i < (b + 1) * 128; ++i) {
+    for (int i = b * 128; i < end; ++i) {
       float a = fabsf(oracle_bf16_to_f32(row[i]));
       if (a > amax) amax = a;
     }
     float s = amax / 448.0f;
     scale[b] = s;
-    for (int i = b * 128; i < (b + 1) * 128; ++i) {
+    for (int i = b * 128; i < end; ++i) {
       if (amax == 0.0f) q[i] = 0x00;
       else q[i] = oracle_f32_to_e4m3(oracle_bf16_to_f32(row[i]) / s);
     }
@@ -282,7 +287,7 @@ void oracle_dispatch_fp8(int N, int H, int E, int K, int cap,
                          const uint16_t *x, const int32_t *topk_idx,
                          const int32_t *slot_of, uint8_t *expert_x,
                          float *expert_x_scale) {
-  const int nb = H / 128;
+  const int nb = (H + 127) / 128;
   uint8_t *q = (uint8_t *)malloc((size_t)H);
   float *sc = (float *)malloc((size_t)nb * sizeof(float));
   if (!q || !sc) abort();

@@ -412,6 +412,35 @@ def check_fp8_properties(o):
             assert (err <= 0.5 * step + np.abs(t) * 2.0**-23).all(), "E4M3 rounding bound"
 
 
+def check_fp8_partial_block(o):
+    """A row whose length is not a multiple of 128 has ceil(H/128) blocks, the
+    last one short ("Lower latency and higher throughput with multi-node
+    DeepSeek deployment", Quantization: scales M x ceil_div(K, 128)).  The
+    short block must quantise exactly as the same elements followed by zeros
+    up to 128 (zeros change neither the maximum nor any other element's
+    byte), which is the full-block path pinned above; an all-zero short block
+    has scale 0."""
+    rng = np.random.default_rng(29)
+    for H in (16, 144, 400, 7200):
+        nb = (H + 127) // 128
+        for trial in range(6):
+            f = rng.standard_normal(H).astype(np.float32) * np.float32(10.0 ** rng.uniform(-3, 3))
+            if trial == 0:
+                f[(nb - 1) * 128:] = 0.0              # an all-zero short block
+            if trial == 1:
+                f[(nb - 1) * 128:] *= np.float32(1e4)  # the short block holds the row's maximum
+            row = torch_bf16_bits(f)
+            q, sc = o.quant_row_e4m3(row)
+            assert q.shape == (H,) and sc.shape == (nb,), "ceil(H/128) scales"
+            padded = np.zeros(nb * 128, np.uint16)
+            padded[:H] = row
+            qp, scp = o.quant_row_e4m3(padded)
+            assert np.array_equal(q, qp[:H]), f"H={H}: short block bytes as if zero-padded"
+            assert np.array_equal(sc.view(np.uint32), scp.view(np.uint32)), f"H={H}: scales"
+            if trial == 0:
+                assert sc[-1] == 0.0 and (q[(nb - 1) * 128:] == 0).all(), "zero short block"
+
+
 def check_dispatch_fp8(o):
     rng = np.random.default_rng(5)
     R, T, E, K, H = 3, 21, 5, 2, 384
@@ -635,7 +664,8 @@ ALL_CHECKS = [
     check_plan_exhaustive, check_plan_random, check_plan_empty, check_plan_masked,
     check_plan_errors,
     check_plan_golden,
-    check_dispatch_bf16, check_fp8_golden, check_fp8_properties, check_dispatch_fp8,
+    check_dispatch_bf16, check_fp8_golden, check_fp8_properties, check_fp8_partial_block,
+    check_dispatch_fp8,
     check_combine_golden, check_combine_identity, check_combine_bound, check_combine_shared,
     check_router, check_exp_silu, check_silu_mul_quant,
 ]

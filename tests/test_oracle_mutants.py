@@ -37,8 +37,11 @@ MUTANTS = [
     ("masked_routes_minus_one", "  return topk_idx[g * K + k] != -1;", "  return topk_idx[g * K + k] != -2;"),
     ("dispatch_bf16_swap_pairs", "dst[h] = x[g * H + h];", "dst[h] = x[g * H + (h ^ 1)];"),
     ("quant_scale_447", "float s = amax / 448.0f;", "float s = amax / 447.0f;"),
-    ("quant_amax_drops_last", "for (int i = b * 128; i < (b + 1) * 128; ++i) {\n      float a",
-     "for (int i = b * 128; i < (b + 1) * 128 - 1; ++i) {\n      float a"),
+    ("quant_amax_drops_last", "for (int i = b * 128; i < end; ++i) {\n      float a",
+     "for (int i = b * 128; i < end - 1; ++i) {\n      float a"),
+    ("quant_partial_block_dropped", "const int nb = (H + 127) / 128;", "const int nb = H / 128;"),
+    ("quant_partial_block_scale_128", "    float s = amax / 448.0f;\n    scale[b] = s;",
+     "    float s = (end - b * 128 < 128 ? amax * 0.5f : amax) / 448.0f;\n    scale[b] = s;"),
     ("quant_zero_block_one", "if (amax == 0.0f) q[i] = 0x00;", "if (amax == 0.0f) q[i] = 0x01;"),
     ("quant_reciprocal", "oracle_bf16_to_f32(row[i]) / s);", "oracle_bf16_to_f32(row[i]) * (448.0f / amax));"),
     ("dispatch_fp8_scale_index", "expert_x_scale[row * nb + b] = sc[b];", "expert_x_scale[row * nb] = sc[b];"),
