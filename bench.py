@@ -73,13 +73,13 @@ def call_bytes(wl) -> dict:
         # read x, topk_idx, slot_of; write K copies of every row
         "dispatch_bf16": N * H * 2 + 2 * maps + N * K * H * 2,
         # read x, topk_idx, slot_of; write K copies of the e4m3 row and its H/128 scales
-        "dispatch_fp8": N * H * 2 + 2 * maps + N * K * H + N * K * (H // 128) * 4,
+        "dispatch_fp8": N * H * 2 + 2 * maps + N * K * H + N * K * ((H + 127) // 128) * 4,
         # read K expert rows per token, topk_idx, slot_of, weights; write y
         "combine": N * K * H * 2 + 3 * maps + N * H * 2,
         # the plan and the dispatch in one call: the bytes of both
         "plan_dispatch_bf16": 3 * maps + E * 4 + E * (R + 1) * 4 + N * H * 2 + 2 * maps + N * K * H * 2,
         "plan_dispatch_fp8": (3 * maps + E * 4 + E * (R + 1) * 4 + N * H * 2 + 2 * maps + N * K * H
-                              + N * K * (H // 128) * 4),
+                              + N * K * ((H + 127) // 128) * 4),
     }
 
 
@@ -273,7 +273,7 @@ def oracle_sample(wl, seed=0):
     bufs = {
         "ex16": np.zeros((E, cap, H), np.uint16),
         "ex8": np.zeros((E, cap, H), np.uint8),
-        "sc": np.zeros((E, cap, H // 128), np.float32),
+        "sc": np.zeros((E, cap, (H + 127) // 128), np.float32),
         "ey": np.zeros((E, cap, H), np.uint16),
     }
 
@@ -420,7 +420,7 @@ class BufferSet:
         if any(base_call(c).endswith("dispatch_bf16") for c in calls):
             per += wl.E * cap * wl.H * 2
         if any(base_call(c).endswith("dispatch_fp8") for c in calls):
-            per += wl.E * cap * wl.H + wl.E * cap * (wl.H // 128) * 4
+            per += wl.E * cap * wl.H + wl.E * cap * ((wl.H + 127) // 128) * 4
         return per
 
 

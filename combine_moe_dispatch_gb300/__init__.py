@@ -19,7 +19,7 @@ from . import buildlib as _build
 
 PAYLOAD_BF16 = 0
 PAYLOAD_FP8_E4M3 = 1
-PAYLOAD_FP8_E4M3_TSCALE = 2   # E4M3 bytes, scales [E, H/128, cap]
+PAYLOAD_FP8_E4M3_TSCALE = 2   # E4M3 bytes, scales [E, ceil(H/128), cap]
 # moe_dispatch_ex flag: x was final before the kernel preceding the dispatch began
 DISPATCH_EARLY_X = 1
 
@@ -269,8 +269,8 @@ def workspace_set_debug(workspace, flags: int, timeout_ns: int = 0, stream=None,
 class Buffers:
     """Device buffers of one shape, allocated with torch (the library itself
     allocates nothing).  ``expert_x`` is uint8 [E, cap, H] for the fp8
-    payloads, bf16 otherwise; ``expert_x_scale`` is [E, cap, H/128], or
-    [E, H/128, cap] for PAYLOAD_FP8_E4M3_TSCALE, and None for bf16."""
+    payloads, bf16 otherwise; ``expert_x_scale`` is [E, cap, ceil(H/128)], or
+    [E, ceil(H/128), cap] for PAYLOAD_FP8_E4M3_TSCALE, and None for bf16."""
 
     def __init__(self, shape: Shape, device="cuda", expert_y: bool = True, expert_x: bool = True):
         import torch
@@ -291,7 +291,8 @@ class Buffers:
             self.expert_x = self.expert_x_scale = None
         elif shape.fp8:
             self.expert_x = torch.empty((E, cap, H), dtype=torch.uint8, device=device)
-            sdims = (E, H // 128, cap) if shape.payload == PAYLOAD_FP8_E4M3_TSCALE else (E, cap, H // 128)
+            nb = (H + 127) // 128                      # the last block is short when H % 128 != 0
+            sdims = (E, nb, cap) if shape.payload == PAYLOAD_FP8_E4M3_TSCALE else (E, cap, nb)
             self.expert_x_scale = torch.empty(sdims, dtype=torch.float32, device=device)
         else:
             self.expert_x = torch.empty((E, cap, H), dtype=torch.bfloat16, device=device)

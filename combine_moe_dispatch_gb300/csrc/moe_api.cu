@@ -71,7 +71,9 @@ moe_status check_shape(const moe_shape *s) {
   if (N * s->top_k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)s->num_experts * s->capacity >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if (s->hidden % 8 != 0) return MOE_ERR_UNSUPPORTED;
-  if (s->payload != MOE_PAYLOAD_BF16 && s->hidden % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  // fp8: rows of any multiple of 16 elements (the last 128-element scale
+  // block may be short); each 16-byte store is then all in or all past a row
+  if (s->payload != MOE_PAYLOAD_BF16 && s->hidden % 16 != 0) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 

@@ -117,14 +117,15 @@ dispatch_bf16_kernel(DispatchParams p) {
 }
 
 // MINB: resident blocks per SM the registers are held to (3: 80 registers,
-// 4: 64; see launch_dispatch_fp8).
-template <int P, int MINB>
+// 4: 64; see launch_dispatch_fp8).  SHORT: H % 128 != 0, the last block of a
+// row is short (fp8_load, fp8_store).
+template <int P, int MINB, bool SHORT = false>
 __global__ void __launch_bounds__(kDispatchThreads, MINB)
 dispatch_fp8_kernel(DispatchParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * kDispatchThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kDispatchThreads) >> 5;
-  const int nb = p.H / 128;                                  // blocks per row
+  const int nb = SHORT ? (p.H + 127) / 128 : p.H / 128;      // blocks per row
   const int tpr = (nb + 2 * P - 1) / (2 * P);
   const int64_t ntasks = (int64_t)p.N * tpr;
 
@@ -139,7 +140,7 @@ dispatch_fp8_kernel(DispatchParams p) {
   if (warp0 >= ntasks) return;
   if (!p.early_x) pdl_wait_for_previous();
   Fp8Raw<P> a;
-  fp8_load<P>(p, warp0 / tpr, (int)(warp0 % tpr), lane, a);
+  fp8_load<P, SHORT>(p, warp0 / tpr, (int)(warp0 % tpr), lane, a);
   Fp8Task<P> t;
   fp8_quantise<P>(a, lane, t);
   Routes r;
@@ -154,10 +155,10 @@ dispatch_fp8_kernel(DispatchParams p) {
     Routes rn;
     if (more) {
       const int64_t g = next / tpr;
-      fp8_load<P>(p, g, (int)(next - g * tpr), lane, a);
+      fp8_load<P, SHORT>(p, g, (int)(next - g * tpr), lane, a);
       rn = load_routes(p, g, lane);
     }
-    fp8_store<P>(p, lane, t, r);
+    fp8_store<P, SHORT>(p, lane, t, r);
     if (more) {
       fp8_quantise<P>(a, lane, t);
       r = rn;
@@ -189,8 +190,10 @@ cudaError_t launch_dispatch_bf16(const DispatchParams &p, cudaStream_t stream) {
 }
 
 cudaError_t launch_dispatch_fp8(const DispatchParams &p, cudaStream_t stream) {
-  const int nb = p.H / 128;
-  const int P = (nb % 2 == 0) ? pick_units(nb / 2, kFp8MaxPairs) : kFp8MaxPairs;
+  const bool short_blk = p.H % 128 != 0;
+  const int nb = (p.H + 127) / 128;
+  // a short last block: always kFp8MaxPairs block pairs per task
+  const int P = (nb % 2 == 0 && !short_blk) ? pick_units(nb / 2, kFp8MaxPairs) : kFp8MaxPairs;
   const int64_t tasks = (int64_t)p.N * ((nb + 2 * P - 1) / (2 * P));
   if (P == 1) return launch_tasks(dispatch_fp8_kernel<1, 1>, tasks, p, stream);
   // More than 3 tasks per warp at 3 blocks per SM: 4 blocks per SM (64
@@ -198,6 +201,9 @@ cudaError_t launch_dispatch_fp8(const DispatchParams &p, cudaStream_t stream) {
   // Mixtral-shaped layer (4.5 tasks per warp), 52.6 -> 52.1 us at Kimi-K2
   // decode (7.9), but 13.45 -> 13.6 us at DeepSeek-V3 decode (2.0).
   const int64_t warps3 = (int64_t)device_sm_count() * 3 * (kDispatchThreads / 32);
+  if (short_blk)
+    return tasks > 3 * warps3 ? launch_tasks(dispatch_fp8_kernel<kFp8MaxPairs, 4, true>, tasks, p, stream)
+                              : launch_tasks(dispatch_fp8_kernel<kFp8MaxPairs, 3, true>, tasks, p, stream);
   if (tasks > 3 * warps3) return launch_tasks(dispatch_fp8_kernel<kFp8MaxPairs, 4>, tasks, p, stream);
   return launch_tasks(dispatch_fp8_kernel<kFp8MaxPairs, 3>, tasks, p, stream);
 }

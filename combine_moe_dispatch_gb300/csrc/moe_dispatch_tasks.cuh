@@ -93,7 +93,7 @@ struct Fp8Task {     // one task's output
   float my_scale;   // lane L < 2P holds the scale of block seg*2P + L
 };
 
-template <int P>
+template <int P, bool SHORT = false>
 __device__ __forceinline__ void fp8_load(const DispatchParams &p, int64_t g, int seg, int lane,
                                          Fp8Raw<P> &a) {
   const int half = lane >> 4;
@@ -102,10 +102,15 @@ __device__ __forceinline__ void fp8_load(const DispatchParams &p, int64_t g, int
   a.g = g;
   a.seg = seg;
   const uint16_t *src = p.x + a.g * p.H;
+  // SHORT (H % 128 != 0; H % 16 == 0): a lane's 8 elements are all in the
+  // row or all past its end, and past it they read as 0.  The full-block
+  // build keeps the block test: the element test measured 0.3 us slower in
+  // the fused kernel at DeepSeek-V3 decode.
 #pragma unroll
   for (int it = 0; it < P; ++it) {
     const int blk = a.seg * 2 * P + it * 2 + half;
-    a.v[it] = blk < nb ? ld_stream16(src + (int64_t)blk * 128 + sub * 8) : make_uint4(0, 0, 0, 0);
+    const bool in = SHORT ? blk * 128 + sub * 8 < p.H : blk < nb;
+    a.v[it] = in ? ld_stream16(src + (int64_t)blk * 128 + sub * 8) : make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -169,12 +174,12 @@ __device__ __forceinline__ void fp8_quantise(const Fp8Raw<P> &a, int lane, Fp8Ta
 }
 
 // Write one quantised task to every (expert, slot) of its token.
-template <int P>
+template <int P, bool SHORT = false>
 __device__ __forceinline__ void fp8_store(const DispatchParams &p, int lane, const Fp8Task<P> &t,
                                           const Routes &r) {
   const int half = lane >> 4;
   const int sub = lane & 15;
-  const int nb = p.H / 128;
+  const int nb = SHORT ? (p.H + 127) / 128 : p.H / 128;   // SHORT: the last block is short
   constexpr int bpt = 2 * P;
   const unsigned okmask = check_routes(p, r, lane, t.seg == 0);
   const int nscale = min(bpt, nb - t.seg * bpt);
@@ -186,18 +191,20 @@ __device__ __forceinline__ void fp8_store(const DispatchParams &p, int lane, con
     uint8_t *dst = static_cast<uint8_t *>(p.expert_x) + row * p.H;
     if constexpr (P % 2 == 0) {
       // lane pair (sub & ~1, sub | 1) writes 16 bytes at (sub & ~1) * 8 of
-      // block 2j (even lane) or 2j + 1 (odd lane) of its half
+      // block 2j (even lane) or 2j + 1 (odd lane) of its half (SHORT: those
+      // 16 bytes are all in the row or all past its end, H % 16 == 0)
 #pragma unroll
       for (int j = 0; j < P / 2; ++j) {
         const int blk = t.seg * bpt + (2 * j + (lane & 1)) * 2 + half;
-        if (blk < nb)
-          *reinterpret_cast<uint4 *>(dst + (int64_t)blk * 128 + (sub & ~1) * 8) = t.w16[j];
+        const bool in = SHORT ? blk * 128 + (sub & ~1) * 8 < p.H : blk < nb;
+        if (in) *reinterpret_cast<uint4 *>(dst + (int64_t)blk * 128 + (sub & ~1) * 8) = t.w16[j];
       }
     } else {
 #pragma unroll
       for (int it = 0; it < P; ++it) {
         const int blk = t.seg * bpt + it * 2 + half;
-        if (blk < nb) *reinterpret_cast<uint2 *>(dst + (int64_t)blk * 128 + sub * 8) = t.q[it];
+        const bool in = SHORT ? blk * 128 + sub * 8 < p.H : blk < nb;
+        if (in) *reinterpret_cast<uint2 *>(dst + (int64_t)blk * 128 + sub * 8) = t.q[it];
       }
     }
     if (lane < nscale) {

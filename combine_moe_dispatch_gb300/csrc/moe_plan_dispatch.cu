@@ -114,7 +114,7 @@ struct Bf16Path {
   }
 };
 
-template <int P>
+template <int P, bool SHORT = false>   // SHORT: H % 128 != 0 (fp8_load, fp8_store)
 struct Fp8Path {
   using Raw = Fp8Raw<P>;
   using Out = Fp8Task<P>;
@@ -122,7 +122,7 @@ struct Fp8Path {
   static constexpr bool kStage2 = false;
   static __device__ __forceinline__ void load(const DispatchParams &p, const TaskCursor &c,
                                               int lane, Raw &a) {
-    fp8_load<P>(p, c.g, c.seg, lane, a);
+    fp8_load<P, SHORT>(p, c.g, c.seg, lane, a);
   }
   static __device__ __forceinline__ void load_staged(const DispatchParams &p, const TaskCursor &c,
                                                      int lane, const uint16_t *s, Raw &a) {
@@ -132,8 +132,9 @@ struct Fp8Path {
 #pragma unroll
     for (int it = 0; it < P; ++it) {
       const int blk = c.seg * 2 * P + it * 2 + half;
-      a.v[it] = blk < nb ? *reinterpret_cast<const uint4 *>(s + (it * 2 + half) * 128 + sub * 8)
-                         : make_uint4(0, 0, 0, 0);
+      const bool in = SHORT ? blk * 128 + sub * 8 < p.H : blk < nb;
+      a.v[it] = in ? *reinterpret_cast<const uint4 *>(s + (it * 2 + half) * 128 + sub * 8)
+                   : make_uint4(0, 0, 0, 0);
     }
   }
   static __device__ __forceinline__ void prep(const Raw &a, int lane, Out &t) {
@@ -141,7 +142,7 @@ struct Fp8Path {
   }
   static __device__ __forceinline__ void store(const DispatchParams &p, int lane, const Out &t,
                                                const Routes &r) {
-    fp8_store<P>(p, lane, t, r);
+    fp8_store<P, SHORT>(p, lane, t, r);
   }
 };
 
@@ -543,8 +544,10 @@ bool plan_dispatch_geometry(const moe_shape &s, FusedParams &p) {
   const bool fp8 = s.payload != MOE_PAYLOAD_BF16;
   int tpr;
   if (fp8) {
-    const int nb = s.hidden / 128;
-    const int P = (nb % 2 == 0) ? pick_units(nb / 2, kFusedFp8MaxPairs) : kFusedFp8MaxPairs;
+    // a short last block (H % 128 != 0): always kFusedFp8MaxPairs pairs per task
+    const int nb = (s.hidden + 127) / 128;
+    const int P = (nb % 2 == 0 && s.hidden % 128 == 0) ? pick_units(nb / 2, kFusedFp8MaxPairs)
+                                                        : kFusedFp8MaxPairs;
     tpr = (nb + 2 * P - 1) / (2 * P);
     p.units = P;
   } else {
@@ -588,6 +591,11 @@ cudaError_t launch_plan_dispatch(const FusedParams &p, bool fp8, cudaStream_t st
   // of a task with its own size.
   if (fp8) {
     const bool wide = p.q_tasks > 2 * (kFusedFp8Threads / 32);
+    if (p.d.H % 128 != 0) {   // a short last block: built for kFusedFp8MaxPairs only
+      if (p.units != kFusedFp8MaxPairs) return cudaErrorInvalidValue;
+      return wide ? launch_fused<Fp8Path<kFusedFp8MaxPairs, true>, kFusedFp8ThreadsWide>(p, stream)
+                  : launch_fused<Fp8Path<kFusedFp8MaxPairs, true>, kFusedFp8Threads>(p, stream);
+    }
     switch (p.units) {
       case 1: return wide ? launch_fused<Fp8Path<1>, kFusedFp8ThreadsWide>(p, stream)
                           : launch_fused<Fp8Path<1>, kFusedFp8Threads>(p, stream);

@@ -57,9 +57,10 @@ typedef enum {
 
 typedef enum {
   MOE_PAYLOAD_BF16 = 0,     /* expert_x rows are bf16 copies of x */
-  MOE_PAYLOAD_FP8_E4M3 = 1, /* expert_x rows are OCP E4M3 bytes + fp32 scales [E, cap, H/128] */
+  MOE_PAYLOAD_FP8_E4M3 = 1, /* expert_x rows are OCP E4M3 bytes + fp32 scales [E, cap, nb],
+                               nb = ceil(H / 128) */
   MOE_PAYLOAD_FP8_E4M3_TSCALE = 2  /* the same bytes; the scales transposed per expert,
-                                      [E, H/128, cap], as a grouped GEMM loads them: the
+                                      [E, nb, cap], as a grouped GEMM loads them: the
                                       scales of one 128-column block of one expert's rows
                                       are contiguous.  Every scale is then a separate
                                       4-byte store: slower than FP8_E4M3 */
@@ -68,7 +69,10 @@ typedef enum {
 /* Problem shape.  Limits: all sizes >= 1 except T, which may be 0 (an empty
  * batch: moe_plan writes zero counts and offsets, dispatch and combine do
  * nothing); K <= 32; E <= 2048; N*K < 2^31; E*cap < 2^31; H % 8 == 0
- * (H % 128 == 0 for the fp8 payload). */
+ * (H % 16 == 0 for the fp8 payloads, whose last 128-element scale block is
+ * short when H % 128 != 0: "Lower latency and higher throughput with
+ * multi-node DeepSeek deployment", Quantization, scale shape
+ * M x ceil_div(K, 128)). */
 typedef struct {
   int32_t num_ranks;        /* R */
   int32_t tokens_per_rank;  /* T */
@@ -155,9 +159,11 @@ moe_status moe_plan_masked(const moe_shape *shape, const int32_t *topk_idx,
  * Out:  expert_x     [E, cap, H]: bf16 (payload BF16) or E4M3 bytes (payload
  *                    FP8_E4M3), 16-byte aligned.  Row (e, s) is written only
  *                    for s < count[e]; other rows are not touched.
- *       expert_x_scale [E, cap, H/128] fp32 for FP8_E4M3, [E, H/128, cap] for
- *                    FP8_E4M3_TSCALE (4-byte aligned), NULL for BF16.  Per
- *                    128-block: scale = amax / 448,
+ *       expert_x_scale [E, cap, nb] fp32 for FP8_E4M3, [E, nb, cap] for
+ *                    FP8_E4M3_TSCALE (4-byte aligned), NULL for BF16;
+ *                    nb = ceil(H / 128), the last block holding the H % 128
+ *                    leftover elements when H is not a multiple of 128.  Per
+ *                    block: scale = amax / 448,
  *                    q = e4m3_rn_satfinite(x / scale); an all-zero block has
  *                    scale 0 and q = 0.
  * Work: the workspace moe_plan used; the call writes nothing if its status

@@ -138,8 +138,8 @@ def test_host_rejections_enqueue_nothing(lib):
     ("E <= 2048", (1, 4, 256, 2049, 2, 8, 0), (1, 4, 256, 2048, 2, 8, 0)),
     ("K <= 32", (1, 4, 256, 64, 33, 8, 0), (1, 4, 256, 64, 32, 8, 0)),
     ("H % 8 == 0", (1, 4, 260, 8, 2, 8, 0), (1, 4, 264, 8, 2, 8, 0)),
-    ("fp8: H % 128 == 0", (1, 4, 264, 8, 2, 8, 1), (1, 4, 256, 8, 2, 8, 1)),
-    ("fp8, transposed scales: H % 128 == 0", (1, 4, 264, 8, 2, 8, 2), (1, 4, 384, 8, 2, 8, 2)),
+    ("fp8: H % 16 == 0", (1, 4, 264, 8, 2, 8, 1), (1, 4, 272, 8, 2, 8, 1)),
+    ("fp8, transposed scales: H % 16 == 0", (1, 4, 392, 8, 2, 8, 2), (1, 4, 400, 8, 2, 8, 2)),
 ])
 def test_shape_limits(lib, fields, over, under):
     """Each limit of the shape check, from both sides: just over it the

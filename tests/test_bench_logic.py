@@ -15,7 +15,7 @@ def test_algorithmic_bytes_follow_the_formulas():
         plan = N * K * 4 * 3 + E * 4 + E * (R + 1) * 4          # idx in; slot_of, src_of, counts, offsets out
         assert cb["plan"] == plan
         assert cb["dispatch_bf16"] == N * H * 2 + 2 * N * K * 4 + N * K * H * 2
-        assert cb["dispatch_fp8"] == N * H * 2 + 2 * N * K * 4 + N * K * H + N * K * (H // 128) * 4
+        assert cb["dispatch_fp8"] == N * H * 2 + 2 * N * K * 4 + N * K * H + N * K * ((H + 127) // 128) * 4
         assert cb["combine"] == N * K * H * 2 + 3 * N * K * 4 + N * H * 2
         for p in ("bf16", "fp8"):
             assert cb["plan_dispatch_" + p] == cb["plan"] + cb["dispatch_" + p]

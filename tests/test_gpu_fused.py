@@ -55,6 +55,13 @@ SMALL = [
     ("ten_pairs_per_row", 1, 48, 2560, 24, 2, ("bf16", "fp8")),      # 20 blocks: 5 tasks of 2 pairs
     ("at_the_limit", 2, 1024, 256, 128, 8, ("bf16", "fp8")),
     ("beyond_the_limit", 2, 1025, 256, 128, 8, ("bf16", "fp8")),
+    # fp8 rows that are not a multiple of 128 long: the last scale block is
+    # short (H = 16: one block of 16; 144: 128 + 16; 400: 3 x 128 + 16;
+    # 7200: 56 x 128 + 32, eight tasks of four block pairs, the last partial)
+    ("short_block_h16", 2, 40, 16, 8, 2, ("fp8", "fp8t")),
+    ("short_block_h144", 3, 50, 144, 16, 4, ("bf16", "fp8", "fp8t")),
+    ("short_block_h400", 2, 64, 400, 37, 5, ("fp8", "fp8t")),
+    ("short_block_h7200", 2, 48, 7200, 64, 8, ("fp8", "fp8t")),
 ]
 
 
