@@ -227,7 +227,7 @@ class Oracle:
         if act_q is None:
             act_q = np.zeros((E, cap, I), np.uint8)
         if act_scale is None:
-            act_scale = np.zeros((E, cap, I // 128), np.float32)
+            act_scale = np.zeros((E, cap, (I + 127) // 128), np.float32)
         self.lib.oracle_silu_mul_quant(E, cap, I, _ptr(h), _ptr(cnt), _ptr(act_q), _ptr(act_scale))
         return act_q, act_scale
 

@@ -466,7 +466,7 @@ void oracle_silu_mul_quant(int E, int cap, int I, const uint16_t *expert_h,
                            float *act_scale) {
   float *a = (float *)malloc((size_t)I * sizeof(float));
   if (!a) abort();
-  const int nb = I / 128;
+  const int nb = (I + 127) / 128;   /* ceil_div(I, 128): the last block may be short */
   for (int e = 0; e < E; ++e) {
     int rows = expert_num_tokens[e];
     if (rows < 0) rows = 0;
@@ -480,14 +480,15 @@ void oracle_silu_mul_quant(int E, int cap, int I, const uint16_t *expert_h,
         a[i] = oracle_silu_f32(g) * u;
       }
       for (int b = 0; b < nb; ++b) {
+        const int end = (b + 1) * 128 < I ? (b + 1) * 128 : I;
         float amax = 0.0f;
-        for (int i = b * 128; i < (b + 1) * 128; ++i) {
+        for (int i = b * 128; i < end; ++i) {
           const float v = fabsf(a[i]);
           if (v > amax) amax = v;
         }
         const float sc = amax / 448.0f;
         act_scale[row * nb + b] = sc;
-        for (int i = b * 128; i < (b + 1) * 128; ++i)
+        for (int i = b * 128; i < end; ++i)
           act_q[row * I + i] = (amax == 0.0f) ? 0x00 : oracle_f32_to_e4m3(a[i] / sc);
       }
     }

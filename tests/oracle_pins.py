@@ -659,6 +659,34 @@ def check_silu_mul_quant(o):
     assert (sc[2, 0, 0] == 0) and (q[2, 0, :128] == 0).all(), "zero gate -> zero block"
 
 
+def check_silu_partial_block(o):
+    """An intermediate size that is not a multiple of 128 gives ceil(I/128)
+    scale blocks per row, the last one short (the same reading as the
+    dispatch's).  Metamorphic pin: the result equals that of rows whose gate
+    and up halves are zero-padded to a multiple of 128 (SiLU(0) * 0 = 0
+    changes no block maximum), truncated back; an all-zero short block has
+    scale 0."""
+    rng = np.random.default_rng(93)
+    E, cap = 3, 4
+    cnt = np.array([4, 1, 3], np.int32)
+    for I in (16, 144, 400):
+        nb, Ip = (I + 127) // 128, ((I + 127) // 128) * 128
+        g = rng.standard_normal((E, cap, I)).astype(np.float32) * 2
+        u = rng.standard_normal((E, cap, I)).astype(np.float32)
+        g[0, 1, (nb - 1) * 128:] = 0.0                     # an all-zero short block
+        h = torch_bf16_bits(np.concatenate([g, u], axis=2))
+        q, sc = o.silu_mul_quant(h, cnt)
+        assert q.shape == (E, cap, I) and sc.shape == (E, cap, nb), "ceil(I/128) scales"
+        gp = np.zeros((E, cap, Ip), np.float32)
+        up = np.zeros((E, cap, Ip), np.float32)
+        gp[..., :I], up[..., :I] = g, u
+        hp = torch_bf16_bits(np.concatenate([gp, up], axis=2))
+        qp, scp = o.silu_mul_quant(hp, cnt)
+        assert np.array_equal(q, qp[..., :I]), f"I={I}: short block bytes as if zero-padded"
+        assert np.array_equal(sc.view(np.uint32), scp.view(np.uint32)), f"I={I}: scales"
+        assert sc[0, 1, nb - 1] == 0 and (q[0, 1, (nb - 1) * 128:] == 0).all(), "zero short block"
+
+
 ALL_CHECKS = [
     check_bf16, check_e4m3_decode, check_e4m3_encode,
     check_plan_exhaustive, check_plan_random, check_plan_empty, check_plan_masked,
@@ -667,5 +695,5 @@ ALL_CHECKS = [
     check_dispatch_bf16, check_fp8_golden, check_fp8_properties, check_fp8_partial_block,
     check_dispatch_fp8,
     check_combine_golden, check_combine_identity, check_combine_bound, check_combine_shared,
-    check_router, check_exp_silu, check_silu_mul_quant,
+    check_router, check_exp_silu, check_silu_mul_quant, check_silu_partial_block,
 ]

@@ -65,6 +65,9 @@ MUTANTS = [
     ("silu_gate_up_swapped", "        const float g = oracle_bf16_to_f32(h[i]);\n        const float u = oracle_bf16_to_f32(h[I + i]);",
      "        const float u = oracle_bf16_to_f32(h[i]);\n        const float g = oracle_bf16_to_f32(h[I + i]);"),
     ("silu_count_off_by_one", "    for (int s = 0; s < rows; ++s) {", "    for (int s = 0; s + 1 < rows; ++s) {"),
+    ("silu_partial_block_dropped", "  const int nb = (I + 127) / 128;", "  const int nb = I / 128;"),
+    ("silu_partial_block_amax", "        for (int i = b * 128; i < end; ++i) {\n          const float v = fabsf(a[i]);",
+     "        for (int i = b * 128; i < (end - b * 128 < 128 ? end - 1 : end); ++i) {\n          const float v = fabsf(a[i]);"),
     ("shared_after_rounding",
      "      y[g * H + h] = oracle_f32_to_bf16(acc); /* shared + routed, one rounding */",
      "      y[g * H + h] = oracle_f32_to_bf16(oracle_bf16_to_f32(oracle_f32_to_bf16(acc - "
