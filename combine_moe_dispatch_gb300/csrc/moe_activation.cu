@@ -132,15 +132,18 @@ __device__ __forceinline__ int populated_expert(const int32_t *s_prefix, int E, 
 // The 2P blocks of task (row, seg): lane (half, sub) loads elements
 // [blk * 128 + sub * 8, + 8) of block blk = seg * 2P + 2 * it + half of the
 // gate and the up half.  EXACT: the row is a whole number of tasks, so every
-// block exists; otherwise blocks past the row read as zeros.
-template <int P, bool EXACT>
+// block exists; otherwise blocks past the row read as zeros.  SHORT
+// (I % 128 != 0, I % 16 == 0): the last block is short, and a lane's 8
+// elements past the row's end read as zeros.
+template <int P, bool EXACT, bool SHORT = false>
 __device__ __forceinline__ void load_task(const ActParams &p, int64_t row, int seg, int half, int sub,
                                           int nb, uint4 (&gv)[P], uint4 (&uv)[P]) {
   const uint16_t *gate = p.expert_h + row * 2 * p.I + (int64_t)seg * (2 * P * 128) + half * 128 + sub * 8;
   const uint16_t *up = gate + p.I;
 #pragma unroll
   for (int it = 0; it < P; ++it) {
-    const bool ok = EXACT || seg * 2 * P + it * 2 + half < nb;
+    const int blk = seg * 2 * P + it * 2 + half;
+    const bool ok = SHORT ? blk * 128 + sub * 8 < p.I : (EXACT || blk < nb);
     gv[it] = ok ? __ldcs(reinterpret_cast<const uint4 *>(gate + it * 256)) : make_uint4(0, 0, 0, 0);
     uv[it] = ok ? __ldcs(reinterpret_cast<const uint4 *>(up + it * 256)) : make_uint4(0, 0, 0, 0);
   }
@@ -149,7 +152,7 @@ __device__ __forceinline__ void load_task(const ActParams &p, int64_t row, int s
 // One task: SiLU(gate) * up for the 2P blocks in gv/uv, the block scales
 // (computed once each, by lanes 0 .. 2P-1, which also store them) and the
 // E4M3 bytes.  All 32 lanes call it together.
-template <int P, bool EXACT, bool TS>
+template <int P, bool EXACT, bool TS, bool SHORT = false>
 __device__ __forceinline__ void act_task(const ActParams &p, const float *s_tab, int64_t row, int seg,
                                          int lane, int nb, const uint4 (&gv)[P], const uint4 (&uv)[P]) {
   const int half = lane >> 4;
@@ -209,7 +212,9 @@ __device__ __forceinline__ void act_task(const ActParams &p, const float *s_tab,
   uint8_t *qrow = static_cast<uint8_t *>(p.act_q) + row * p.I + (int64_t)seg * (bpt * 128) + half * 128 + sub * 8;
 #pragma unroll
   for (int it = 0; it < P; ++it) {
-    if (EXACT || seg * bpt + it * 2 + half < nb) *reinterpret_cast<uint2 *>(qrow + it * 256) = q[it];
+    const int blk = seg * bpt + it * 2 + half;
+    const bool in = SHORT ? blk * 128 + sub * 8 < p.I : (EXACT || blk < nb);
+    if (in) *reinterpret_cast<uint2 *>(qrow + it * 256) = q[it];
   }
   if (lane < min(bpt, nb - seg * bpt)) {
     const int blk = seg * bpt + lane;
@@ -236,7 +241,7 @@ struct ActCursor {
   }
 };
 
-template <int P, bool EXACT, bool TS>
+template <int P, bool EXACT, bool TS, bool SHORT = false>
 __global__ void __launch_bounds__(kActThreads, P >= 2 ? 3 : 1)
 silu_quant_kernel(ActParams p) {
   __shared__ __align__(16) float s_tab[kSiluTabEntries];
@@ -255,7 +260,7 @@ silu_quant_kernel(ActParams p) {
   const int sub = lane & 15;
   const int64_t warp0 = ((int64_t)blockIdx.x * kActThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kActThreads) >> 5;
-  const int nb = p.I / 128;
+  const int nb = SHORT ? (p.I + 127) / 128 : p.I / 128;   // SHORT: the last block is short
   const int tpr = (nb + 2 * P - 1) / (2 * P);
   // each warp takes a contiguous range of tasks, so the row and its expert
   // advance incrementally from one task to the next
@@ -273,29 +278,30 @@ silu_quant_kernel(ActParams p) {
   c.row = (int64_t)c.e * p.cap + (c.rg - s_prefix[c.e]);
   // two register buffers in turn: the next task's rows load while this one computes
   uint4 ga[P], ua[P], gb[P], ub[P];
-  load_task<P, EXACT>(p, c.row, c.seg, half, sub, nb, ga, ua);
+  load_task<P, EXACT, SHORT>(p, c.row, c.seg, half, sub, nb, ga, ua);
   for (;;) {
     ActCursor nc = c;
     nc.next(s_prefix, p.E, p.cap, tpr);
-    if (n > 1) load_task<P, EXACT>(p, nc.row, nc.seg, half, sub, nb, gb, ub);
-    act_task<P, EXACT, TS>(p, s_tab, c.row, c.seg, lane, nb, ga, ua);
+    if (n > 1) load_task<P, EXACT, SHORT>(p, nc.row, nc.seg, half, sub, nb, gb, ub);
+    act_task<P, EXACT, TS, SHORT>(p, s_tab, c.row, c.seg, lane, nb, ga, ua);
     if (--n == 0) break;
     c = nc;
     nc.next(s_prefix, p.E, p.cap, tpr);
-    if (n > 1) load_task<P, EXACT>(p, nc.row, nc.seg, half, sub, nb, ga, ua);
-    act_task<P, EXACT, TS>(p, s_tab, c.row, c.seg, lane, nb, gb, ub);
+    if (n > 1) load_task<P, EXACT, SHORT>(p, nc.row, nc.seg, half, sub, nb, ga, ua);
+    act_task<P, EXACT, TS, SHORT>(p, s_tab, c.row, c.seg, lane, nb, gb, ub);
     if (--n == 0) break;
     c = nc;
   }
 }
 
 namespace {
-template <int P, bool EXACT, bool TS>
+template <int P, bool EXACT, bool TS, bool SHORT = false>
 cudaError_t launch_p(const ActParams &p, cudaStream_t stream) {
   const size_t smem = (size_t)(p.E + 1) * sizeof(int32_t);
   // enough warps for every row of every expert at full capacity, capped at a full device
-  const int64_t tasks = (int64_t)p.E * p.cap * ((p.I / 128 + 2 * P - 1) / (2 * P));
-  const int grid = persistent_grid((const void *)silu_quant_kernel<P, EXACT, TS>, kActThreads, tasks);
+  const int64_t tasks = (int64_t)p.E * p.cap * (((p.I + 127) / 128 + 2 * P - 1) / (2 * P));
+  const int grid =
+      persistent_grid((const void *)silu_quant_kernel<P, EXACT, TS, SHORT>, kActThreads, tasks);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -306,13 +312,14 @@ cudaError_t launch_p(const ActParams &p, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, silu_quant_kernel<P, EXACT, TS>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, silu_quant_kernel<P, EXACT, TS, SHORT>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 }  // namespace
 
 template <bool TS>
 cudaError_t launch_layout(const ActParams &p, cudaStream_t stream) {
+  if (p.I % 128 != 0) return launch_p<1, false, TS, true>(p, stream);   // a short last block
   const int nb = p.I / 128;
   if (nb % 4 == 0) return launch_p<2, true, TS>(p, stream);
   if (nb % 2 == 0) return launch_p<1, true, TS>(p, stream);

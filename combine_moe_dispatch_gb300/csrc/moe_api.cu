@@ -340,7 +340,9 @@ moe_status moe_silu_mul_quant(const moe_shape *shape, int32_t intermediate, cons
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   if (intermediate <= 0) return MOE_ERR_INVALID_ARG;
-  if (intermediate % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  // rows of any multiple of 16 elements: the last 128-element scale block may
+  // be short, and every 8-byte store of a row is then wholly inside it
+  if (intermediate % 16 != 0) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)shape->num_experts * shape->capacity * 2 * intermediate >= ((int64_t)1 << 46))
     return MOE_ERR_UNSUPPORTED;
   if (!expert_h || !expert_num_tokens || !act_q || !act_scale) return MOE_ERR_INVALID_ARG;

@@ -310,11 +310,12 @@ moe_status moe_router_topk(const moe_shape *shape, const float *logits, int32_t 
  * In:   expert_h [E, cap, 2*intermediate] bf16, 16-byte aligned;
  *       expert_num_tokens [E] int32 (from moe_plan);
  * Out:  act_q [E, cap, intermediate] E4M3 (16-byte aligned) and act_scale
- *       [E, cap, intermediate/128] fp32, or [E, intermediate/128, cap] when
- *       shape->payload is FP8_E4M3_TSCALE; rows below the count only.
+ *       [E, cap, nb] fp32, or [E, nb, cap] when shape->payload is
+ *       FP8_E4M3_TSCALE, nb = ceil(intermediate / 128) (the last block is
+ *       short when intermediate % 128 != 0); rows below the count only.
  * Work: the workspace of the plan that produced the counts; nothing is
  *       written if its status word is set.  Uses E and cap of `shape`.
- * Errors: INVALID_ARG, UNSUPPORTED (intermediate % 128 != 0), ALIGNMENT,
+ * Errors: INVALID_ARG, UNSUPPORTED (intermediate % 16 != 0), ALIGNMENT,
  *       WORKSPACE, CUDA. */
 moe_status moe_silu_mul_quant(const moe_shape *shape, int32_t intermediate, const void *expert_h,
                               const int32_t *expert_num_tokens, void *act_q, float *act_scale,

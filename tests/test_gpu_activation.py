@@ -15,7 +15,8 @@ pytestmark = pytest.mark.gpu
 
 def _buffers(E, cap, I):
     q = torch.full((E, cap, I), gpu_check.SENTINEL_BYTE, dtype=torch.uint8, device="cuda")
-    sc = torch.full((E, cap, I // 128), gpu_check.SENTINEL_SCALE, dtype=torch.float32, device="cuda")
+    sc = torch.full((E, cap, (I + 127) // 128), gpu_check.SENTINEL_SCALE, dtype=torch.float32,
+                    device="cuda")
     return q, sc
 
 
@@ -50,7 +51,7 @@ def _edge_rows(I):
 def _check(moe, E, cap, I, h_host, counts, q, sc):
     import oracle
     q_o = np.full((E, cap, I), gpu_check.SENTINEL_BYTE, np.uint8)
-    sc_o = np.full((E, cap, I // 128), gpu_check.SENTINEL_SCALE, np.float32)
+    sc_o = np.full((E, cap, (I + 127) // 128), gpu_check.SENTINEL_SCALE, np.float32)
     oracle.silu_mul_quant(h_host, counts, q_o, sc_o)
     q_g = q.cpu().numpy()
     sc_g = sc.cpu().numpy()
@@ -214,6 +215,36 @@ def test_silu_mul_quant_midpoint_rich_rows():
     qd, sc = _buffers(E, cap, I)
     moe.silu_mul_quant(shape, I, gpu_check.dev(h), gpu_check.dev(counts), qd, sc, ws)
     _check(moe, E, cap, I, h, counts, qd, sc)
+
+
+@pytest.mark.parametrize("I", [16, 144, 400, 2064])
+@pytest.mark.parametrize("tscale", [False, True])
+def test_silu_mul_quant_short_last_block(I, tscale):
+    """An intermediate size that is not a multiple of 128 (I % 16 == 0):
+    ceil(I/128) scales per row, the last block short.  Rows where the short
+    block is all zero, and where it holds the row's largest value; every
+    byte and scale bit for bit, untouched rows still the sentinel."""
+    import combine_moe_dispatch_gb300 as moe
+    E, cap = 5, 9
+    nb = (I + 127) // 128
+    counts = np.array([4, 0, 9, 11, 2], np.int32)
+    h = inputs.gate_up(E, cap, I, seed=I + 7)
+    hf = np.zeros((2, 2 * I), np.float32)
+    hf[:, I:] = 1.0
+    hf[0, :I] = np.linspace(-3, 3, I)
+    hf[0, (nb - 1) * 128:I] = 0.0                            # short block all zero
+    hf[1, :I] = np.linspace(-3, 3, I)
+    hf[1, I - 1] = 40.0                                      # short block holds the maximum
+    h[0, 0:2] = inputs.to_bf16_bits(hf)
+    pay = moe.PAYLOAD_FP8_E4M3_TSCALE if tscale else moe.PAYLOAD_FP8_E4M3
+    shape = moe.make_shape(1, 16, 256, E, 2, cap, pay)
+    ws = _workspace(moe, shape)
+    q = torch.full((E, cap, I), gpu_check.SENTINEL_BYTE, dtype=torch.uint8, device="cuda")
+    sdims = (E, nb, cap) if tscale else (E, cap, nb)
+    sc = torch.full(sdims, gpu_check.SENTINEL_SCALE, dtype=torch.float32, device="cuda")
+    moe.silu_mul_quant(shape, I, gpu_check.dev(h), gpu_check.dev(counts), q, sc, ws)
+    _check(moe, E, cap, I, h, counts, q, sc.transpose(1, 2) if tscale else sc)
+    assert moe.read_status(ws) == moe.Status.OK
 
 
 @pytest.mark.parametrize("I", [384, 2048])
