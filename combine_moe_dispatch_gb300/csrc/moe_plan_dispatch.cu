@@ -67,7 +67,7 @@
 //
 // Data errors: the status word ends up exactly as moe_plan would set it, and
 // the plan outputs are those of moe_plan.  But no block waits for the
-// verdict of the others, so the rows of entries whose expert is in range and
+// outcome of the others, so the rows of entries whose expert is in range and
 // whose slot is below cap may already have been written when the status
 // reports an error; moe_dispatch would write none.
 #include <cuda_bf16.h>

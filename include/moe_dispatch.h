@@ -224,9 +224,14 @@ moe_status moe_dispatch_ex(const moe_shape *shape, const void *x,
  *       moe_plan.  Unlike moe_dispatch, which writes nothing after a plan
  *       error, rows of entries whose expert is in range and whose slot is
  *       below cap may be written even when the status reports BAD_EXPERT or
- *       CAPACITY: no block waits for the others' verdict.
- * Ordering: not a programmatic dependent: the call waits for every earlier
- *       kernel in the stream, as moe_plan does.
+ *       CAPACITY: no block waits for the others' outcome.
+ * Ordering: the one-launch kernel is a programmatic dependent of the
+ *       previous kernel in the stream: its blocks may be scheduled while
+ *       that kernel drains, but they read nothing from global memory (x,
+ *       topk_idx, the workspace) before it has completed.  The two-launch
+ *       path is moe_plan, which waits for every earlier kernel, then
+ *       moe_dispatch_ex(MOE_DISPATCH_EARLY_X), whose early read of x is
+ *       therefore safe.
  * Host errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA. */
 moe_status moe_plan_dispatch(const moe_shape *shape, const void *x, const int32_t *topk_idx,
                              int32_t *expert_num_tokens, int32_t *expert_rank_offsets,
