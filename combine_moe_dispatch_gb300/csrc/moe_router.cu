@@ -13,7 +13,8 @@
 // lowest expert.  Each lane keeps its best remaining logit (value, then
 // lowest index); K rounds of a warp maximum over the lanes' bests and a
 // ballot of the lanes that hold it pick the experts, and only the winning
-// lane looks for its next best.
+// lane looks for its next best (in calls bound by latency, each lane keeps
+// its second-best ready as well: router_ff_kernel's TOP2).
 //   The weights are computed in float-float (pairs of fp32 values) rather
 // than fp64: this GPU's fp64 rate is a small fraction of its fp32 rate, and
 // the fp64 softmax cost 0.7 us of the 4.5 us call at DeepSeek-V3 decode.
